@@ -1,0 +1,139 @@
+"""Serial CPU oracle (TEST INFRASTRUCTURE ONLY).
+
+Python face of bb_oracle.c, the plain serial C implementation of the band ->
+bidiagonal bulge-chasing reduction (arXiv 2510.12705, Section III and the text
+of Algorithms 1-2; Householder convention of LAPACK xLARFG).  Only the tests,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package.  The CUDA library never calls it and shares no code with
+it.
+
+Functions take numpy arrays in the layout of ``band_inputs``: band storage of
+shape (n, ldab), A(i, j) = band[j, ku + i - j], ku = bw + tw.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bb_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_bb_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile bb_oracle.c with gcc (no contraction of multiply-adds)."""
+    srcs = [_SRC, os.path.join(_HERE, "bb_oracle_body.h")]
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(s) for s in srcs)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+                           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        for sfx in ("_d", "_f"):
+            getattr(lib, "oracle_larfg" + sfx).argtypes = [i64, p, p, i64, p]
+            getattr(lib, "oracle_larfg" + sfx).restype = None
+            getattr(lib, "oracle_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64, i64, i64]
+            getattr(lib, "oracle_reduce_band" + sfx).restype = ci
+            getattr(lib, "oracle_reduce_dense" + sfx).argtypes = [i64, i64, i64, p]
+            getattr(lib, "oracle_reduce_dense" + sfx).restype = ci
+            getattr(lib, "oracle_halfstep_band" + sfx).argtypes = [i64, i64, i64, i64, p, i64, i64, i64, ci]
+            getattr(lib, "oracle_halfstep_band" + sfx).restype = None
+            getattr(lib, "oracle_sweep_steps" + sfx).argtypes = [i64, i64, i64, i64]
+            getattr(lib, "oracle_sweep_steps" + sfx).restype = i64
+            getattr(lib, "oracle_extract_band" + sfx).argtypes = [i64, i64, p, i64, p, p]
+            getattr(lib, "oracle_extract_band" + sfx).restype = None
+        _lib = lib
+    return _lib
+
+
+def _sfx(arr: np.ndarray) -> str:
+    if arr.dtype == np.float64:
+        return "_d"
+    if arr.dtype == np.float32:
+        return "_f"
+    raise TypeError(f"unsupported dtype {arr.dtype}")
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def larfg(alpha: float, x: np.ndarray):
+    """LAPACK-convention reflector of (alpha, x): returns (beta, v_tail, tau)."""
+    x = np.array(x, copy=True)
+    lib = _load()
+    a = np.array([alpha], dtype=x.dtype)
+    tau = np.zeros(1, dtype=x.dtype)
+    getattr(lib, "oracle_larfg" + _sfx(x))(x.size, _ptr(a), _ptr(x), 1, _ptr(tau))
+    return a[0], x, tau[0]
+
+
+def pass_plan(bw: int, tw: int):
+    """[(b, t), ...]: b = bw; while b > 1: t = min(tw, b - 1); b -= t."""
+    plan, b = [], bw
+    while b > 1:
+        t = min(tw, b - 1)
+        plan.append((b, t))
+        b -= t
+    return plan
+
+
+def reduce_band(band: np.ndarray, n: int, bw: int, tw: int, pass_lo: int = 0,
+                pass_hi: int = 1 << 30) -> np.ndarray:
+    """Reduce band storage in place (serial order); returns the same array."""
+    assert band.flags.c_contiguous and band.shape[0] == n
+    ldab = band.shape[1]
+    rc = getattr(_load(), "oracle_reduce_band" + _sfx(band))(n, bw, tw, _ptr(band), ldab,
+                                                              pass_lo, pass_hi)
+    if rc != 0:
+        raise ValueError("oracle_reduce_band: invalid arguments")
+    return band
+
+
+def reduce_dense(a: np.ndarray, bw: int, tw: int) -> np.ndarray:
+    """Reduce a dense row-major n x n array in place (reflectors on whole rows/cols)."""
+    assert a.flags.c_contiguous and a.shape[0] == a.shape[1]
+    rc = getattr(_load(), "oracle_reduce_dense" + _sfx(a))(a.shape[0], bw, tw, _ptr(a))
+    if rc != 0:
+        raise ValueError("oracle_reduce_dense: invalid arguments")
+    return a
+
+
+def halfstep_band(band: np.ndarray, n: int, b: int, t: int, ku: int, r: int, k: int,
+                  side: int) -> None:
+    """One half-step (side 0: right/row reflector, 1: left/column) in place."""
+    getattr(_load(), "oracle_halfstep_band" + _sfx(band))(n, b, t, ku, _ptr(band),
+                                                          band.shape[1], r, k, side)
+
+
+def sweep_steps(n: int, b: int, t: int, r: int) -> int:
+    return int(_load().oracle_sweep_steps_d(n, b, t, r))
+
+
+def extract(band: np.ndarray, n: int, ku: int):
+    d = np.zeros(n, dtype=band.dtype)
+    e = np.zeros(max(n - 1, 0), dtype=band.dtype)
+    getattr(_load(), "oracle_extract_band" + _sfx(band))(n, ku, _ptr(band), band.shape[1],
+                                                         _ptr(d), _ptr(e))
+    return d, e
+
+
+def bidiagonal(band: np.ndarray, n: int, bw: int, tw: int):
+    """(d, e) of the reduction of a copy of band (serial oracle)."""
+    work = np.ascontiguousarray(band.copy())
+    reduce_band(work, n, bw, tw)
+    return extract(work, n, bw + tw)

@@ -1,0 +1,216 @@
+/*
+ * Body of the serial CPU oracle, written once and instantiated for float and
+ * double by bb_oracle.c (which defines REAL, SFX and the precision constants).
+ *
+ * TEST INFRASTRUCTURE ONLY: nothing on the product path may include, link or
+ * call this file.  See bb_oracle.c for the citations and the readings taken.
+ */
+
+#define CAT2(a, b) a##b
+#define CAT(a, b) CAT2(a, b)
+#define FN(name) CAT(name, SFX)
+
+/* Euclidean norm of x[0], x[inc], ..., x[(m-1)*inc]: plain sum of squares in
+ * index order.  When that sum under- or overflows while the entries are
+ * finite and not all zero, the same sum is taken on entries divided by the
+ * largest magnitude, so that a norm of zero means every entry is zero. */
+static REAL FN(norm2_)(int64_t m, const REAL* x, int64_t inc) {
+    REAL ssq = 0;
+    for (int64_t q = 0; q < m; ++q) {
+        REAL v = x[q * inc];
+        ssq = ssq + v * v;
+    }
+    if (isfinite(ssq) && ssq >= REAL_MIN_NORMAL) return SQRT(ssq);
+    REAL scale = 0;
+    for (int64_t q = 0; q < m; ++q) {
+        REAL a = FABS(x[q * inc]);
+        if (a > scale) scale = a;
+    }
+    if (scale == 0) return 0;
+    REAL s2 = 0;
+    for (int64_t q = 0; q < m; ++q) {
+        REAL v = x[q * inc] / scale;
+        s2 = s2 + v * v;
+    }
+    return scale * SQRT(s2);
+}
+
+/* Householder reflector in the LAPACK xLARFG convention.
+ *   input : alpha = x_1, x = (x_2 .. x_w) (m = w-1 entries, stride inc)
+ *   output: *alpha = beta, x overwritten by (v_2 .. v_w) (v_1 = 1), *tau
+ * so that (I - tau v v^T) (alpha, x)^T = (beta, 0, ..., 0)^T.
+ *   xi = ||x||;  xi == 0  ->  tau = 0, beta = alpha (identity, no sign flip)
+ *   else beta = -sign(alpha) * hypot(alpha, xi) with sign(+-0) = +,
+ *        tau = (beta - alpha) / beta,  v = x * (1 / (alpha - beta)).
+ * A beta below safmin = tiny/eps is handled as LAPACK does: x and alpha are
+ * scaled by 1/safmin (at most 20 times), beta recomputed, and scaled back. */
+void FN(oracle_larfg)(int64_t m, REAL* alpha, REAL* x, int64_t inc, REAL* tau) {
+    if (m <= 0) { *tau = 0; return; }
+    REAL xnorm = FN(norm2_)(m, x, inc);
+    if (xnorm == 0) { *tau = 0; return; }
+    REAL a = *alpha;
+    REAL beta = (a >= 0) ? -HYPOT(a, xnorm) : HYPOT(a, xnorm);
+    const REAL safmin = REAL_SAFMIN;
+    const REAL rsafmn = 1 / safmin;
+    int knt = 0;
+    if (FABS(beta) < safmin) {
+        do {
+            ++knt;
+            for (int64_t q = 0; q < m; ++q) x[q * inc] = x[q * inc] * rsafmn;
+            beta = beta * rsafmn;
+            a = a * rsafmn;
+        } while (FABS(beta) < safmin && knt < 20);
+        xnorm = FN(norm2_)(m, x, inc);
+        beta = (a >= 0) ? -HYPOT(a, xnorm) : HYPOT(a, xnorm);
+    }
+    *tau = (beta - a) / beta;
+    REAL scal = 1 / (a - beta);
+    for (int64_t q = 0; q < m; ++q) x[q * inc] = x[q * inc] * scal;
+    for (int j = 0; j < knt; ++j) beta = beta * safmin;
+    *alpha = beta;
+}
+
+/* ---------------------------------------------------------------------------
+ * One bulge-chasing step on an abstract matrix accessor.  ELEM(i, j) is an
+ * lvalue for A(i, j); the band and dense modes below instantiate it.
+ *
+ * Pass (b, t), b' = b - t; sweep r; step k:
+ *   c  = r + b' + k b,  p = r (k = 0) or c - b (k > 0),  ce = min(c + t, n-1)
+ *   right: reflector from A(p, c..ce); A(p, c) = beta, A(p, c+1..ce) = 0;
+ *          rows i in (p, ce]:  y = sum_m A(i, c+m) v_m,  A(i, c+m) -= (tau y) v_m
+ *   left : reflector from A(c..ce, c); A(c, c) = beta, A(c+1..ce, c) = 0;
+ *          cols j in (c, min(ce + b, n-1)]:
+ *                y = sum_m v_m A(c+m, j),  A(c+m, j) -= (tau y) v_m
+ * In the dense mode the row / column ranges of the two applications are the
+ * whole matrix instead of the windows above (entries outside the windows are
+ * exactly zero, so the arithmetic inside the windows is the same).
+ * ------------------------------------------------------------------------- */
+#define STEP_BODY(ROW_LO, ROW_HI, COL_LO, COL_HI, DO_RIGHT, DO_LEFT)                    \
+    do {                                                                                \
+        int64_t c = r + (b - t) + k * b;                                                \
+        int64_t p = (k == 0) ? r : c - b;                                               \
+        int64_t ce = (c + t < n - 1) ? c + t : n - 1;                                   \
+        int64_t cend = (ce + b < n - 1) ? ce + b : n - 1;                               \
+        int64_t w = ce - c + 1;                                                         \
+        REAL v[ORACLE_WMAX] = {0};                                                      \
+        (void)cend;                                                            \
+        REAL tau, beta;                                                                 \
+        if (DO_RIGHT) {                                                                 \
+            for (int64_t q = 0; q < w; ++q) v[q] = ELEM(p, c + q);                      \
+            beta = v[0];                                                                \
+            FN(oracle_larfg)(w - 1, &beta, v + 1, 1, &tau);                             \
+            v[0] = 1;                                                                   \
+            ELEM(p, c) = beta;                                                          \
+            for (int64_t q = 1; q < w; ++q) ELEM(p, c + q) = 0;                         \
+            if (tau != 0) {                                                             \
+                for (int64_t i = (ROW_LO); i <= (ROW_HI); ++i) {                        \
+                    if (i == p) continue;                                               \
+                    REAL y = 0;                                                         \
+                    for (int64_t q = 0; q < w; ++q) y = y + ELEM(i, c + q) * v[q];      \
+                    REAL s = tau * y;                                                   \
+                    for (int64_t q = 0; q < w; ++q) ELEM(i, c + q) = ELEM(i, c + q) - s * v[q]; \
+                }                                                                       \
+            }                                                                           \
+        }                                                                               \
+        if (DO_LEFT) {                                                                  \
+            for (int64_t q = 0; q < w; ++q) v[q] = ELEM(c + q, c);                      \
+            beta = v[0];                                                                \
+            FN(oracle_larfg)(w - 1, &beta, v + 1, 1, &tau);                             \
+            v[0] = 1;                                                                   \
+            ELEM(c, c) = beta;                                                          \
+            for (int64_t q = 1; q < w; ++q) ELEM(c + q, c) = 0;                         \
+            if (tau != 0) {                                                             \
+                for (int64_t j = (COL_LO); j <= (COL_HI); ++j) {                        \
+                    if (j == c) continue;                                               \
+                    REAL y = 0;                                                         \
+                    for (int64_t q = 0; q < w; ++q) y = y + v[q] * ELEM(c + q, j);      \
+                    REAL s = tau * y;                                                   \
+                    for (int64_t q = 0; q < w; ++q) ELEM(c + q, j) = ELEM(c + q, j) - s * v[q]; \
+                }                                                                       \
+            }                                                                           \
+        }                                                                               \
+    } while (0)
+
+/* Band mode: A(i, j) lives at band[(ku + i - j) + j * ldab]. */
+#define ELEM(i, j) band[(ku + (i) - (j)) + (j) * ldab]
+
+/* One half-step (side 0 = right/horizontal, 1 = left/vertical) of sweep r,
+ * step k of the pass (b, t), windows exactly as in STEP_BODY. */
+void FN(oracle_halfstep_band)(int64_t n, int64_t b, int64_t t, int64_t ku, REAL* band, int64_t ldab,
+                              int64_t r, int64_t k, int side) {
+    if (side == 0) STEP_BODY(p, ce, c, cend, 1, 0);
+    else           STEP_BODY(p, ce, c, cend, 0, 1);
+}
+
+/* Number of steps of sweep r in pass (b, t): k runs while c_k + 1 <= n - 1. */
+int64_t FN(oracle_sweep_steps)(int64_t n, int64_t b, int64_t t, int64_t r) {
+    int64_t last = n - 2 - r - (b - t);
+    return last < 0 ? 0 : last / b + 1;
+}
+
+/* Whole reduction in band storage, serial order: for each pass of the plan
+ * (b = bw; while b > 1: t = min(tw, b - 1); pass (b, t); b -= t), for each
+ * sweep r ascending, for each step k ascending: right, then left.
+ * Passes with index outside [pass_lo, pass_hi) are skipped (bandwidth still
+ * advances), so that a run can be split at pass boundaries.
+ * The fill rows 0..tw-1 and ku+1..ku+tw of every column are zeroed first when
+ * pass_lo == 0.  Returns 0, or -1 on invalid arguments. */
+int FN(oracle_reduce_band)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab,
+                           int64_t pass_lo, int64_t pass_hi) {
+    if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
+    if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
+    if (tw + 1 > ORACLE_WMAX) return -1;
+    int64_t ku = bw + tw;
+    if (pass_lo == 0) {
+        for (int64_t j = 0; j < n; ++j) {
+            for (int64_t q = 0; q < tw; ++q) band[q + j * ldab] = 0;
+            for (int64_t q = ku + 1; q <= ku + tw; ++q) band[q + j * ldab] = 0;
+        }
+    }
+    int64_t b = bw, pass = 0;
+    while (b > 1) {
+        int64_t t = (tw < b - 1) ? tw : b - 1;
+        if (pass >= pass_lo && pass < pass_hi) {
+            for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) {
+                int64_t K = FN(oracle_sweep_steps)(n, b, t, r);
+                for (int64_t k = 0; k < K; ++k) STEP_BODY(p, ce, c, cend, 1, 1);
+            }
+        }
+        b -= t;
+        ++pass;
+    }
+    return 0;
+}
+
+/* d_i = A(i, i), e_i = A(i, i+1) from band storage. */
+void FN(oracle_extract_band)(int64_t n, int64_t ku, const REAL* band, int64_t ldab, REAL* d, REAL* e) {
+    for (int64_t i = 0; i < n; ++i) d[i] = ELEM(i, i);
+    for (int64_t i = 0; i + 1 < n; ++i) e[i] = ELEM(i, i + 1);
+}
+#undef ELEM
+
+/* Dense mode: A is n x n, row-major, A(i, j) = a[i * n + j].  Each reflector
+ * is applied to every row (right) or every column (left) of the matrix, which
+ * is the definition of A <- A H and A <- H A; the band windows play no part.
+ * Same pass plan and serial order as the band mode. */
+#define ELEM(i, j) a[(i) * n + (j)]
+int FN(oracle_reduce_dense)(int64_t n, int64_t bw, int64_t tw, REAL* a) {
+    if (n < 1 || bw < 0 || bw >= n || tw < 1) return -1;
+    if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
+    if (tw + 1 > ORACLE_WMAX) return -1;
+    int64_t b = bw;
+    while (b > 1) {
+        int64_t t = (tw < b - 1) ? tw : b - 1;
+        for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) {
+            int64_t K = FN(oracle_sweep_steps)(n, b, t, r);
+            for (int64_t k = 0; k < K; ++k) STEP_BODY(0, n - 1, 0, n - 1, 1, 1);
+        }
+        b -= t;
+    }
+    return 0;
+}
+#undef ELEM
+
+#undef FN
+#undef CAT
+#undef CAT2
