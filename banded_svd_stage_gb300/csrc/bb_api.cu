@@ -1,0 +1,405 @@
+// C-ABI layer of libbb.so: argument checks, the pass planner, workspace
+// ownership and the launch sequence of one reduction.  See include/bb.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/bb.h"
+#include "bb_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+bb_status fail(bb_status st, const std::string& msg) {
+    g_last_error = msg;
+    return st;
+}
+
+bb_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(BB_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct PassPlan {
+    int b, t;
+};
+
+// b = bw; while b > 1: t = min(tw, b - 1); pass (b, t); b -= t.
+std::vector<PassPlan> plan_passes(int64_t bw, int64_t tw) {
+    std::vector<PassPlan> out;
+    int64_t b = bw;
+    while (b > 1 && tw >= 1) {
+        int64_t t = std::min(tw, b - 1);
+        out.push_back({(int)b, (int)t});
+        b -= t;
+    }
+    return out;
+}
+
+// Half-step lag of the persistent scheduler: half-step h of sweep r waits for
+// sweep r-1 to have completed h + lagh half-steps.  Two half-steps (one full
+// cycle) keep the windows disjoint while b - t >= 3; b - t == 2 brings sweep
+// r-2's next row block into reach and needs three; the last pass
+// (b - t == 1) needs four, the paper's three-cycle rule at half-step grain.
+int pass_lag_half(int b, int t) {
+    int bp = b - t;
+    return bp >= 3 ? 2 : (bp == 2 ? 3 : 4);
+}
+
+// Cycle lag of the per-cycle scheduler: the paper's separation condition
+// R + n*BW > R + 1 + BW + TW holds for n = 2 when BW > 1 + TW, else n = 3.
+int pass_lag_cycle(int b, int t) { return (b > t + 1) ? 2 : 3; }
+
+int64_t steps_of_sweep(int64_t n, int b, int t, int64_t r) {
+    int64_t last = n - 2 - r - (b - t);
+    return last < 0 ? 0 : last / b + 1;
+}
+
+size_t elem_size(bb_dtype d) { return d == BB_F64 ? 8 : 4; }
+
+bool is_device_pointer(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace
+
+struct bb_handle {
+    int64_t n = 0, bw = 0;
+    bb_dtype dtype = BB_F32;
+    int device = 0, num_sms = 0, clock_khz = 0;
+    int* d_progress = nullptr;  // n int32 per-sweep progress counters
+    int* d_status = nullptr;    // device status word
+    // parameters
+    int scheduler = 0, tpb = 0, max_ctas = 0, stall_sweep = -1, timing = 0;
+    int64_t wait_ms = 4000, pass_lo = 0, pass_hi = 1 << 30;
+    // staging buffers of bb_reduce_host
+    void* s_band = nullptr;
+    size_t s_band_bytes = 0;
+    void* s_de = nullptr;
+    // statistics of the last reduction
+    int64_t last_launches = 0;
+    std::vector<cudaEvent_t> ev;  // 2 per pass
+    int64_t last_passes = 0;
+};
+
+extern "C" {
+
+const char* bb_last_error(void) { return g_last_error.c_str(); }
+
+int64_t bb_required_ldab(int64_t bw, int64_t tw) { return bw + 2 * tw + 1; }
+
+int64_t bb_num_passes(int64_t bw, int64_t tw) { return (int64_t)plan_passes(bw, tw).size(); }
+
+bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t) {
+    auto plan = plan_passes(bw, tw);
+    if (i < 0 || i >= (int64_t)plan.size() || !b || !t)
+        return fail(BB_ERR_INVALID_ARG, "bb_pass_info: pass index out of range");
+    *b = plan[i].b;
+    *t = plan[i].t;
+    return BB_OK;
+}
+
+double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass) {
+    auto plan = plan_passes(bw, tw);
+    double total = 0;
+    for (int64_t pi = 0; pi < (int64_t)plan.size(); ++pi) {
+        if (pass >= 0 && pi != pass) continue;
+        const int b = plan[pi].b, t = plan[pi].t;
+        for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) {
+            const int64_t K = steps_of_sweep(n, b, t, r);
+            for (int64_t k = 0; k < K; ++k) {
+                const int64_t c = r + (b - t) + k * b;
+                const int64_t p = (k == 0) ? r : c - b;
+                const int64_t ce = std::min(c + t, n - 1);
+                const int64_t cend = std::min(ce + b, n - 1);
+                const int64_t w = ce - c + 1;
+                total += 2.0 * elem_bytes * (double)((ce - p + 1) * w + w * (cend - c + 1));
+            }
+        }
+    }
+    return total;
+}
+
+int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass) {
+    auto plan = plan_passes(bw, tw);
+    int64_t total = 0;
+    for (int64_t pi = 0; pi < (int64_t)plan.size(); ++pi) {
+        if (pass >= 0 && pi != pass) continue;
+        const int b = plan[pi].b, t = plan[pi].t;
+        for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) total += steps_of_sweep(n, b, t, r);
+    }
+    return total;
+}
+
+bb_handle* bb_create(int64_t n, int64_t bw, bb_dtype dtype) {
+    if (dtype != BB_F32 && dtype != BB_F64) {
+        fail(BB_ERR_DTYPE, "bb_create: unknown dtype");
+        return nullptr;
+    }
+    if (n < 1 || n > (int64_t)1 << 30 || bw < 0 || bw >= n) {
+        fail(BB_ERR_INVALID_ARG, "bb_create: need n >= 1 and 0 <= bw < n");
+        return nullptr;
+    }
+    bb_handle* h = new bb_handle();
+    h->n = n;
+    h->bw = bw;
+    h->dtype = dtype;
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->clock_khz, cudaDevAttrClockRate, h->device);
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_progress, sizeof(int) * (size_t)n);
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) {
+        cuda_fail(e, "bb_create");
+        bb_destroy(h);
+        return nullptr;
+    }
+    if (h->clock_khz <= 0) h->clock_khz = 2000000;
+    return h;
+}
+
+void bb_destroy(bb_handle* h) {
+    if (!h) return;
+    if (h->d_progress) cudaFree(h->d_progress);
+    if (h->d_status) cudaFree(h->d_status);
+    if (h->s_band) cudaFree(h->s_band);
+    if (h->s_de) cudaFree(h->s_de);
+    for (auto ev : h->ev) cudaEventDestroy(ev);
+    delete h;
+}
+
+bb_status bb_set_param(bb_handle* h, int param, int64_t value) {
+    if (!h) return fail(BB_ERR_INVALID_ARG, "bb_set_param: null handle");
+    switch (param) {
+        case BB_PARAM_SCHEDULER:
+            if (value != 0 && value != 1) return fail(BB_ERR_INVALID_ARG, "scheduler must be 0 or 1");
+            h->scheduler = (int)value;
+            return BB_OK;
+        case BB_PARAM_TPB:
+            if (value != 0 && (value < 32 || value > 1024 || value % 32 != 0))
+                return fail(BB_ERR_INVALID_ARG, "tpb must be 0 or a multiple of 32 in [32, 1024]");
+            h->tpb = (int)value;
+            return BB_OK;
+        case BB_PARAM_MAX_CTAS:
+            if (value < 0 || value > (1 << 20)) return fail(BB_ERR_INVALID_ARG, "max_ctas out of range");
+            h->max_ctas = (int)value;
+            return BB_OK;
+        case BB_PARAM_WAIT_BUDGET_MS:
+            if (value < 1 || value > 600000) return fail(BB_ERR_INVALID_ARG, "wait budget out of range");
+            h->wait_ms = value;
+            return BB_OK;
+        case BB_PARAM_PASS_LO:
+            if (value < 0) return fail(BB_ERR_INVALID_ARG, "pass_lo < 0");
+            h->pass_lo = value;
+            return BB_OK;
+        case BB_PARAM_PASS_HI:
+            if (value < 0) return fail(BB_ERR_INVALID_ARG, "pass_hi < 0");
+            h->pass_hi = value;
+            return BB_OK;
+        case BB_PARAM_STALL_SWEEP:
+            if (value < -1 || value >= h->n) return fail(BB_ERR_INVALID_ARG, "stall sweep out of range");
+            h->stall_sweep = (int)value;
+            return BB_OK;
+        case BB_PARAM_TIMING:
+            h->timing = value ? 1 : 0;
+            return BB_OK;
+        default:
+            return fail(BB_ERR_INVALID_ARG, "unknown parameter");
+    }
+}
+
+int64_t bb_get_param(const bb_handle* h, int param) {
+    if (!h) return -1;
+    switch (param) {
+        case BB_PARAM_SCHEDULER: return h->scheduler;
+        case BB_PARAM_TPB: return h->tpb;
+        case BB_PARAM_MAX_CTAS: return h->max_ctas;
+        case BB_PARAM_WAIT_BUDGET_MS: return h->wait_ms;
+        case BB_PARAM_PASS_LO: return h->pass_lo;
+        case BB_PARAM_PASS_HI: return h->pass_hi;
+        case BB_PARAM_STALL_SWEEP: return h->stall_sweep;
+        case BB_PARAM_TIMING: return h->timing;
+        default: return -1;
+    }
+}
+
+int64_t bb_last_launches(const bb_handle* h) { return h ? h->last_launches : -1; }
+int64_t bb_last_num_passes(const bb_handle* h) { return h ? h->last_passes : -1; }
+
+bb_status bb_last_pass_ms(bb_handle* h, int64_t i, double* ms) {
+    if (!h || !ms) return fail(BB_ERR_INVALID_ARG, "bb_last_pass_ms: null argument");
+    if (!h->timing || i < 0 || i >= h->last_passes || (size_t)(2 * i + 1) >= h->ev.size())
+        return fail(BB_ERR_INVALID_ARG, "bb_last_pass_ms: no timing for this pass");
+    float f = 0;
+    cudaError_t e = cudaEventElapsedTime(&f, h->ev[2 * i], h->ev[2 * i + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "bb_last_pass_ms");
+    *ms = f;
+    return BB_OK;
+}
+
+bb_status bb_status_sync(bb_handle* h, bb_stream_t stream) {
+    if (!h) return fail(BB_ERR_INVALID_ARG, "bb_status_sync: null handle");
+    cudaStream_t s = (cudaStream_t)stream;
+    int st = 0;
+    cudaError_t e = cudaMemcpyAsync(&st, h->d_status, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "bb_status_sync");
+    if (st != 0) {
+        e = cudaMemsetAsync(h->d_status, 0, sizeof(int), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "bb_status_sync: clearing status");
+        return fail((bb_status)st, st == BB_ERR_TIMEOUT ? "device-side progress wait timed out"
+                                                        : "device reported an error");
+    }
+    return BB_OK;
+}
+
+}  // extern "C"
+
+static bb_status check_reduce_args(bb_handle* h, int64_t ldab, int64_t tw) {
+    if (!h) return fail(BB_ERR_INVALID_ARG, "null handle");
+    const int64_t tw_max = std::max<int64_t>(1, h->bw - 1);
+    if (tw < 1 || tw > tw_max) return fail(BB_ERR_INVALID_ARG, "need 1 <= tw <= max(1, bw - 1)");
+    if (tw + 1 > bb::kMaxW) return fail(BB_ERR_INVALID_ARG, "tw > 64 is not supported");
+    if (ldab < bb_required_ldab(h->bw, tw)) return fail(BB_ERR_LDAB, "ldab < bw + 2*tw + 1");
+    if ((double)ldab * (double)h->n > 9.0e18 / 8) return fail(BB_ERR_INVALID_ARG, "band too large");
+    // shared memory of the widest pass (the first): tile of (b + t + 1) columns
+    auto plan = plan_passes(h->bw, tw);
+    for (auto& ps : plan) {
+        int w = ps.t + 1;
+        int wm = w <= 9 ? 9 : (w <= 17 ? 17 : (w <= 33 ? 33 : 65));
+        size_t smem = elem_size(h->dtype) * ((size_t)wm + 2 + (size_t)(ps.b + ps.t + 1) * (wm | 1));
+        if (smem > 227 * 1024)
+            return fail(BB_ERR_INVALID_ARG, "bandwidth too large for the shared-memory tile");
+    }
+    return BB_OK;
+}
+
+template <typename T>
+static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T* d, T* e,
+                             cudaStream_t s) {
+    const int64_t n = h->n;
+    const int ku = (int)(h->bw + tw);
+    cudaError_t err;
+    h->last_launches = 0;
+    h->last_passes = 0;
+    auto plan = plan_passes(h->bw, tw);
+    const int64_t lo = std::max<int64_t>(0, h->pass_lo);
+    const int64_t hi = std::min<int64_t>((int64_t)plan.size(), h->pass_hi);
+    if (lo == 0) {
+        err = bb::run_zero_fill<T>(band, n, ldab, (int)tw, ku, s);
+        if (err != cudaSuccess) return cuda_fail(err, "zero fill launch");
+        h->last_launches += 1;
+    }
+    if (h->timing) {
+        size_t need = 2 * (size_t)std::max<int64_t>(0, hi - lo);
+        while (h->ev.size() < need) {
+            cudaEvent_t ev;
+            err = cudaEventCreate(&ev);
+            if (err != cudaSuccess) return cuda_fail(err, "cudaEventCreate");
+            h->ev.push_back(ev);
+        }
+    }
+    for (int64_t pi = lo; pi < hi; ++pi) {
+        const int b = plan[pi].b, t = plan[pi].t;
+        bb::PassArgs P;
+        P.n = n;
+        P.ldab = ldab;
+        P.b = b;
+        P.t = t;
+        P.bp = b - t;
+        P.ku = ku;
+        P.nsweeps = (int)std::max<int64_t>(0, n - (b - t) - 1);
+        P.lag = pass_lag_cycle(b, t);
+        P.lagh = pass_lag_half(b, t);
+        P.stall_sweep = h->stall_sweep;
+        P.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+        bb::LaunchCfg cfg;
+        cfg.tpb = h->tpb ? h->tpb : bb::auto_tpb(b, t);
+        cfg.max_ctas = h->max_ctas;
+        cfg.num_sms = h->num_sms;
+        bb::LaunchStats st;
+        if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo)], s);
+        err = bb::run_pass<T>(band, P, h->scheduler, cfg, h->d_progress, h->d_status, s, &st);
+        if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo) + 1], s);
+        h->last_launches += st.launches;
+        if (err != cudaSuccess) return cuda_fail(err, "pass launch");
+        h->last_passes += 1;
+    }
+    err = bb::run_extract<T>(band, n, ldab, ku, d, e, s);
+    if (err != cudaSuccess) return cuda_fail(err, "extract launch");
+    h->last_launches += 1;
+    return BB_OK;
+}
+
+extern "C" {
+
+bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
+                    void* e_out, bb_stream_t stream) {
+    bb_status st = check_reduce_args(h, ldab, tw);
+    if (st != BB_OK) return st;
+    if (!band_ptr || !d_out || (h->n > 1 && !e_out))
+        return fail(BB_ERR_INVALID_ARG, "null band, d or e pointer");
+    if (!is_device_pointer(band_ptr) || !is_device_pointer(d_out) ||
+        (h->n > 1 && !is_device_pointer(e_out)))
+        return fail(BB_ERR_INVALID_ARG, "band, d and e must be device pointers");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (h->dtype == BB_F32)
+        return reduce_impl<float>(h, (float*)band_ptr, ldab, tw, (float*)d_out, (float*)e_out, s);
+    return reduce_impl<double>(h, (double*)band_ptr, ldab, tw, (double*)d_out, (double*)e_out, s);
+}
+
+bb_status bb_reduce_host(bb_handle* h, const void* band_host, int64_t ldab, int64_t tw,
+                         void* d_host, void* e_host, bb_stream_t stream) {
+    bb_status st = check_reduce_args(h, ldab, tw);
+    if (st != BB_OK) return st;
+    if (!band_host || !d_host || (h->n > 1 && !e_host))
+        return fail(BB_ERR_INVALID_ARG, "null band, d or e pointer");
+    const size_t es = elem_size(h->dtype);
+    const size_t band_bytes = es * (size_t)ldab * (size_t)h->n;
+    cudaError_t err;
+    if (h->s_band_bytes < band_bytes) {
+        if (h->s_band) cudaFree(h->s_band);
+        h->s_band = nullptr;
+        h->s_band_bytes = 0;
+        err = cudaMalloc(&h->s_band, band_bytes);
+        if (err != cudaSuccess) return fail(BB_ERR_NOMEM, "staging band allocation failed");
+        h->s_band_bytes = band_bytes;
+    }
+    if (!h->s_de) {
+        err = cudaMalloc(&h->s_de, es * (size_t)(2 * h->n));
+        if (err != cudaSuccess) return fail(BB_ERR_NOMEM, "staging d/e allocation failed");
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    err = cudaMemcpyAsync(h->s_band, band_host, band_bytes, cudaMemcpyHostToDevice, s);
+    if (err != cudaSuccess) return cuda_fail(err, "band copy to device");
+    char* dd = (char*)h->s_de;
+    char* ee = dd + es * (size_t)h->n;
+    st = bb_reduce(h, h->s_band, ldab, tw, dd, ee, stream);
+    if (st != BB_OK) return st;
+    err = cudaMemcpyAsync(d_host, dd, es * (size_t)h->n, cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess && h->n > 1)
+        err = cudaMemcpyAsync(e_host, ee, es * (size_t)(h->n - 1), cudaMemcpyDeviceToHost, s);
+    if (err != cudaSuccess) return cuda_fail(err, "d/e copy to host");
+    return bb_status_sync(h, stream);
+}
+
+}  // extern "C"
+
+namespace bb {
+int auto_tpb(int b, int t) {
+    int rows = b + t;
+    int tpb = ((rows + 31) / 32) * 32;
+    return std::min(1024, std::max(64, tpb));
+}
+}  // namespace bb

@@ -1,0 +1,119 @@
+// Launch logic shared by the per-precision translation units.
+#pragma once
+
+#include <algorithm>
+
+#include "bb_internal.h"
+
+namespace bb {
+
+inline int wmax_bucket(int w) {
+    if (w <= 9) return 9;
+    if (w <= 17) return 17;
+    if (w <= 33) return 33;
+    return 65;
+}
+
+template <typename T, int WMAX>
+size_t smem_bytes(const PassArgs& P) {
+    const int wp = WMAX | 1;
+    const size_t ncol = (size_t)P.b + P.t + 1;
+    return sizeof(T) * ((size_t)WMAX + 2 + ncol * wp);
+}
+
+template <typename T, int WMAX>
+cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCfg& cfg,
+                       int* progress, int* status, cudaStream_t stream, LaunchStats* stats) {
+    const size_t smem = smem_bytes<T, WMAX>(P);
+    const int tpb = std::min(cfg.tpb, MaxThreads<T, WMAX>::value);
+    cudaError_t err;
+    if (scheduler == 0) {
+        auto kern = pass_persistent_kernel<T, WMAX>;
+        if (smem > 48 * 1024) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (err != cudaSuccess) return err;
+        }
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, tpb, smem);
+        if (err != cudaSuccess) return err;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        long long grid = (long long)per_sm * cfg.num_sms;
+        if (cfg.max_ctas > 0) grid = std::min<long long>(grid, cfg.max_ctas);
+        grid = std::min<long long>(grid, P.nsweeps);
+        if (grid < 1) return cudaSuccess;
+        err = cudaMemsetAsync(progress, 0, sizeof(int) * (size_t)P.nsweeps, stream);
+        if (err != cudaSuccess) return err;
+        T* band_arg = band;
+        PassArgs p_arg = P;
+        int* prog_arg = progress;
+        int* stat_arg = status;
+        void* args[] = {&band_arg, &p_arg, &prog_arg, &stat_arg};
+        err = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(tpb), args,
+                                          smem, stream);
+        if (stats) {
+            stats->launches += 1;
+            stats->grid = (int)grid;
+        }
+        return err;
+    }
+    // Per-cycle scheduler.
+    auto kern = pass_cycle_kernel<T, WMAX>;
+    if (smem > 48 * 1024) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    const long long S = P.nsweeps;
+    if (S <= 0) return cudaSuccess;
+    auto steps = [&](long long r) -> long long {
+        long long last = P.n - 2 - r - P.bp;
+        return last < 0 ? 0 : last / P.b + 1;
+    };
+    long long tmax = 0;
+    for (long long r = 0; r < S; ++r) tmax = std::max(tmax, P.lag * r + steps(r) - 1);
+    long long r_lo = 0;
+    for (long long T0 = 0; T0 <= tmax; ++T0) {
+        // active sweeps: 0 <= T0 - lag r <= K_r - 1
+        while (r_lo < S && T0 - P.lag * r_lo > steps(r_lo) - 1) ++r_lo;
+        long long r_hi = std::min(S - 1, T0 / P.lag);
+        if (r_hi < r_lo) continue;
+        kern<<<(unsigned)(r_hi - r_lo + 1), tpb, smem, stream>>>(band, P, (int)T0, (int)r_lo);
+        if (stats) stats->launches += 1;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t run_pass(T* band, const PassArgs& P, int scheduler, const LaunchCfg& cfg,
+                     int* progress, int* status, cudaStream_t stream, LaunchStats* stats) {
+    switch (wmax_bucket(P.t + 1)) {
+        case 9: return run_pass_w<T, 9>(band, P, scheduler, cfg, progress, status, stream, stats);
+        case 17: return run_pass_w<T, 17>(band, P, scheduler, cfg, progress, status, stream, stats);
+        case 33: return run_pass_w<T, 33>(band, P, scheduler, cfg, progress, status, stream, stats);
+        default: return run_pass_w<T, 65>(band, P, scheduler, cfg, progress, status, stream, stats);
+    }
+}
+
+template <typename T>
+cudaError_t run_zero_fill(T* band, long long n, long long ldab, int tw, int ku, cudaStream_t s) {
+    long long total = n * 2LL * tw;
+    if (total <= 0) return cudaSuccess;
+    int blocks = (int)std::min<long long>((total + 255) / 256, 4096);
+    zero_fill_kernel<T><<<blocks, 256, 0, s>>>(band, n, ldab, tw, ku);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t run_extract(const T* band, long long n, long long ldab, int ku, T* d, T* e,
+                        cudaStream_t s) {
+    int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
+    extract_kernel<T><<<blocks, 256, 0, s>>>(band, n, ldab, ku, d, e);
+    return cudaGetLastError();
+}
+
+#define BB_INSTANTIATE(T)                                                                          \
+    template cudaError_t run_pass<T>(T*, const PassArgs&, int, const LaunchCfg&, int*, int*,       \
+                                     cudaStream_t, LaunchStats*);                                  \
+    template cudaError_t run_zero_fill<T>(T*, long long, long long, int, int, cudaStream_t);       \
+    template cudaError_t run_extract<T>(const T*, long long, long long, int, T*, T*, cudaStream_t);
+
+}  // namespace bb

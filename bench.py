@@ -1,0 +1,402 @@
+"""Benchmark of the band -> bidiagonal reduction on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--scheduler 0|1] [--no-sweep]
+
+One step is one whole reduction (every pass down to bidiagonal form, plus the
+fill-row zeroing and the d/e extraction) of one synthetic band.  Before each
+step the pristine band is copied into the work buffer and L2 is flushed by
+writing a 256 MiB buffer, both outside the timed events, so every timed step
+starts with its input resident in HBM and not in L2.
+
+metric: effective GB/s = algorithmic bytes of the reduction (each step's
+right and left blocks read once and written once; bb_model_bytes) / device
+time per reduction.  ms_per_step is the device time of one reduction.
+
+With --gpus N (under torchrun) every rank reduces its own band (seed offset
+by the rank): independent replicas, no collective on the data path; the value
+is all ranks' bytes over the slowest rank's time.
+
+--impl reference times the CPU oracle (the plain serial implementation the
+tests check the GPU against) on the host, on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import band_inputs as bi  # noqa: E402
+
+METRIC = "band→bidiagonal ms/reduction and effective GB/s (% of HBM peak), N=4k–32k"
+MAIN_WORKLOAD = bi.WORKLOADS[1].name
+SWEEP_WORKLOADS = [w.name for w in bi.WORKLOADS[1:]]
+HBM_FALLBACK_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return HBM_FALLBACK_GBS, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(values_per_rank_ms: float, units: float, group=None):
+    """Max over ranks of the time and sum over ranks of the units."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return values_per_rank_ms, units
+    dev = "cpu" if dist.get_backend(group) == "gloo" else torch.device("cuda", torch.cuda.current_device())
+    t = torch.tensor([values_per_rank_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    mhz.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, flag in zip(names, parts[5:9]):
+                    if flag.lower() == "active":
+                        reasons.add(nm)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int, with_e2e: bool):
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    from banded_svd_stage_gb300.tensor import Reducer
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    tdt = torch.float32 if w.dtype == "f32" else torch.float64
+    esz = 4 if w.dtype == "f32" else 8
+    band_np = bi.make_band(w.n, w.bw, w.tw, w.dtype, w.dist, w.graded, w.seed + 1000 * rank)
+    pristine = torch.from_numpy(band_np).to(dev)
+    work = torch.empty_like(pristine)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    red = Reducer(w.n, w.bw, tdt, scheduler=scheduler)
+    red.enable_timing(True)
+    d = torch.empty(w.n, dtype=tdt, device=dev)
+    e = torch.empty(w.n, dtype=tdt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    model_bytes = bb.bb_model_bytes(w.n, w.bw, w.tw, esz)
+    npass = bb.bb_num_passes(w.bw, w.tw)
+    pass_bytes = [bb.bb_model_bytes(w.n, w.bw, w.tw, esz, i) for i in range(npass)]
+
+    def one(timed_events):
+        work.copy_(pristine)
+        flush.fill_(rank + 1)
+        if timed_events:
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+        red.reduce_(work, w.tw, d, e, stream)
+        if timed_events:
+            ev1.record(stream)
+            return ev0, ev1
+        return None
+
+    for _ in range(warmup):
+        one(False)
+    red.check(stream)
+    torch.cuda.synchronize()
+    events, pass_ms, launches = [], [], 0
+    for _ in range(steps):
+        events.append(one(True))
+        launches += bb.bb_last_launches(red.h)
+        torch.cuda.synchronize()
+        pass_ms.append(red.pass_ms())
+    red.check(stream)
+    ms = [a.elapsed_time(b) for a, b in events]
+    # dominant kernel: the pass kernel, one launch per pass (persistent scheduler)
+    per_pass_ms = np.array(pass_ms)  # steps x passes
+    e2e = None
+    if with_e2e:
+        e2e = run_e2e(w, band_np, steps, warmup, scheduler, model_bytes)
+    red.close()
+    return {
+        "ms": ms, "model_bytes": model_bytes, "pass_bytes": pass_bytes,
+        "pass_ms_mean": per_pass_ms.mean(axis=0).tolist(), "launches": launches,
+        "e2e": e2e, "band_bytes": band_np.nbytes, "esz": esz,
+    }
+
+
+def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
+    """bb_reduce_host from pinned host memory: H2D of the band, reduction, D2H
+    of d and e, inside the timed region (host wall clock around the call,
+    which synchronizes)."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    h = bb.bb_create(w.n, w.bw, bb.dtype_code(w.dtype))
+    bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, scheduler)
+    src = torch.from_numpy(band_np).pin_memory()
+    tdt = torch.float32 if w.dtype == "f32" else torch.float64
+    d = torch.empty(w.n, dtype=tdt).pin_memory()
+    e = torch.empty(w.n, dtype=tdt).pin_memory()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    times = []
+    for i in range(warmup + steps):
+        flush.fill_(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        bb.bb_reduce_host(h, src, band_np.shape[1], w.tw, d, e, stream)
+        t1 = time.perf_counter()
+        if i >= warmup:
+            times.append((t1 - t0) * 1e3)
+    bb.bb_destroy(h)
+    ms = statistics.median(times)
+    return {"value": model_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(band_np.nbytes),
+            "d2h_bytes_per_step": int((2 * w.n - 1) * (4 if w.dtype == "f32" else 8))}
+
+
+def cpu_oracle_rate(w: bi.Workload, budget_s: float = 12.0):
+    """The oracle, as it stands, on one host core: whole reductions of the
+    workload repeated until about budget_s seconds have elapsed (one at least)."""
+    import oracle
+    band = bi.make_workload(w)
+    model_bytes = None
+    try:
+        import banded_svd_stage_gb300 as bb
+        model_bytes = bb.bb_model_bytes(w.n, w.bw, w.tw, 4 if w.dtype == "f32" else 8)
+    except Exception:
+        model_bytes = _model_bytes_py(w)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.bidiagonal(band, w.n, w.bw, w.tw)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el / reps * (reps + 1) > 2.5 * budget_s:
+            break
+    sec = el / reps
+    return {"value": model_bytes / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "ms_per_reduction": sec * 1e3,
+            "sample": f"{reps} whole serial reductions of {w.name} ({el:.1f} s)"}
+
+
+def _model_bytes_py(w):
+    s = 4 if w.dtype == "f32" else 8
+    tot, b = 0, w.bw
+    while b > 1:
+        t = min(w.tw, b - 1)
+        bp = b - t
+        for r in range(0, w.n - bp - 1):
+            c = r + bp
+            k = 0
+            while c + 1 <= w.n - 1:
+                p = r if k == 0 else c - b
+                ce = min(c + t, w.n - 1)
+                cend = min(ce + b, w.n - 1)
+                ww = ce - c + 1
+                tot += 2 * s * ((ce - p + 1) * ww + ww * (cend - c + 1))
+                k += 1
+                c += b
+        b -= t
+    return tot
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if that summary was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        from banded_svd_stage_gb300.buildlib import source_digest
+        if data.get("source_digest") != source_digest():
+            return None
+        return data.get("per_launch", {}).get(kernel, {}).get(workload)
+    except Exception:
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=MAIN_WORKLOAD)
+    ap.add_argument("--scheduler", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    w = bi.by_name(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        times = []
+        import oracle
+        band = bi.make_workload(w)
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.bidiagonal(band, w.n, w.bw, w.tw)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        mb = _model_bytes_py(w) if w.n <= 4096 else None
+        if mb is None:
+            import banded_svd_stage_gb300 as bb
+            mb = bb.bb_model_bytes(w.n, w.bw, w.tw, 4 if w.dtype == "f32" else 8)
+        sec = sum(times) / len(times)
+        val = mb / sec / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+                "data": "synthetic", "config": {"workload": w.name, "n": w.n, "bw": w.bw, "tw": w.tw},
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"whole serial reductions of {w.name}, one per step"},
+                "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    hbm, peak_src = measured_peaks()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t_wall0 = time.perf_counter()
+    res = run_ours(w, args.steps, args.warmup, args.scheduler, rank, with_e2e=(world == 1))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop() if sampler else None
+    ms_step = sum(res["ms"]) / len(res["ms"])
+    ms_max, bytes_all = aggregate(ms_step, res["model_bytes"])
+    value = bytes_all / (ms_max * 1e-3) / 1e9
+    # roofline of the dominant kernel (the per-pass kernel: one launch a pass)
+    tot_pass_ms = sum(res["pass_ms_mean"])
+    achieved = sum(res["pass_bytes"]) / (tot_pass_ms * 1e-3) / 1e9 if tot_pass_ms > 0 else None
+    kname = "pass_persistent_kernel" if args.scheduler == 0 else "pass_cycle_kernel"
+    traffic = traffic_for(kname, w.name)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
+            "kernel": kname, "peak_source": peak_src,
+            "launches_per_step": len(res["pass_ms_mean"]) if args.scheduler == 0 else None,
+            "achieved_def": "sum over passes of algorithmic bytes / sum of per-pass CUDA-event time"}
+
+    sweep = []
+    if rank == 0 and world == 1 and not args.no_sweep:
+        for name in SWEEP_WORKLOADS:
+            if name == w.name:
+                continue
+            ww = bi.by_name(name)
+            r2 = run_ours(ww, max(2, min(args.steps, 3)), 1, args.scheduler, rank, with_e2e=False)
+            m2 = statistics.median(r2["ms"])
+            g2 = r2["model_bytes"] / (m2 * 1e-3) / 1e9
+            sweep.append({"workload": name, "ms_per_reduction": m2, "min_ms": min(r2["ms"]),
+                          "effective_gbs": g2, "frac_of_hbm": g2 / hbm,
+                          "pass_ms": r2["pass_ms_mean"]})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_oracle_rate(w)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "n": w.n, "bw": w.bw, "tw": w.tw, "dist": w.dist,
+                       "graded": w.graded, "scheduler": "persistent" if args.scheduler == 0 else "per-cycle",
+                       "l2": "flushed between steps (256 MiB write); band restored before each step",
+                       "parallelism": f"replicas x{world}"},
+            "frac_of_hbm": value / hbm,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": res["e2e"],
+            "gpu_launches": res["launches"] * world,
+            "clocks": clocks,
+            "wall_s": wall,
+            "per_workload": sweep,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

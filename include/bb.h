@@ -1,0 +1,152 @@
+/*
+ * bb.h -- C ABI of the GB300 band -> bidiagonal reduction library (libbb.so).
+ *
+ * The library performs the second stage of a two-stage SVD: it reduces an
+ * upper-banded n x n matrix of bandwidth bw to upper bidiagonal form (main
+ * diagonal d, superdiagonal e) by Householder bulge chasing, as described in
+ * "Accelerating Bidiagonalization of Banded Matrices through Memory-Aware
+ * Bulge-Chasing on GPUs" (arXiv 2510.12705), Section III:
+ *   - successive band reduction: each pass lowers the bandwidth from b to
+ *     b - t by annihilating t entries per reflector; passes repeat until the
+ *     bandwidth is 1 (plan: b = bw; while b > 1 { t = min(tw, b - 1); b -= t });
+ *   - within a pass, sweep r annihilates t entries of row r, then chases the
+ *     bulge down the band, one horizontal and one vertical reflector per
+ *     cycle, moving b columns per cycle;
+ *   - consecutive sweeps run concurrently, separated by the cycle lag that
+ *     keeps their data windows disjoint (the paper's three-cycle rule).
+ * Reflectors follow the LAPACK xLARFG convention (beta = -sign(alpha)||x||,
+ * tau = (beta - alpha)/beta, v_1 = 1; annihilated entries become exactly 0),
+ * the reading taken of the paper's tile-QR reference.  Results are therefore
+ * defined up to the signs of d and e; |d| and |e| are unique.
+ *
+ * Storage (all pointers below are device pointers unless stated otherwise):
+ *   compact column-major band storage with fill rows, LAPACK "gb" style with
+ *   ku = bw + tw upper and kl = tw lower diagonals:
+ *       A(i, j) = band[(ku + i - j) + j * ldab],   0 <= i, j < n
+ *   The input band occupies band rows tw .. tw + bw (0 <= j - i <= bw); band
+ *   rows 0 .. tw-1 and ku+1 .. ku+tw hold the bulge fill and are zeroed by
+ *   bb_reduce.  ldab >= bw + 2*tw + 1.  Rows beyond ku + tw are not touched.
+ *
+ * Threading: a handle may be used by one host thread at a time, with at most
+ * one bb_reduce in flight.  All calls are asynchronous on the given stream
+ * unless stated otherwise.
+ */
+#ifndef BB_H_
+#define BB_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of the band, d and e. */
+typedef enum { BB_F32 = 0, BB_F64 = 1 } bb_dtype;
+
+/* Return codes. */
+typedef enum {
+    BB_OK = 0,
+    BB_ERR_INVALID_ARG = 1, /* a size, pointer or parameter is out of range     */
+    BB_ERR_LDAB = 2,        /* ldab < bw + 2*tw + 1                              */
+    BB_ERR_DTYPE = 3,       /* dtype unknown                                     */
+    BB_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed       */
+    BB_ERR_TIMEOUT = 5,     /* a device-side wait gave up (latched on the device) */
+    BB_ERR_NOMEM = 6        /* a device or host allocation failed                */
+} bb_status;
+
+/* A cudaStream_t, passed as a plain pointer (NULL = the legacy default stream). */
+typedef void* bb_stream_t;
+
+/* Opaque handle: owns the per-sweep progress counters (n int32), a device
+ * status word, and (only after bb_reduce_host) staging buffers. */
+typedef struct bb_handle bb_handle;
+
+/* Create a handle for n x n matrices of upper bandwidth bw (0 <= bw < n) and
+ * element type dtype, on the current CUDA device.  Allocates device memory.
+ * Returns NULL on error; bb_last_error() says why. */
+bb_handle* bb_create(int64_t n, int64_t bw, bb_dtype dtype);
+
+/* Reduce the band in place to bidiagonal form and write d (n entries) and e
+ * (n-1 entries).  band_ptr, d_out and e_out are device pointers owned by the
+ * caller; band_ptr holds ldab * n elements and is overwritten (destroyed).
+ * tw: entries annihilated per reflector, 1 <= tw <= max(1, bw - 1), tw <= 64.
+ * Stream-ordered and asynchronous: the return code covers argument checks and
+ * launch errors only.  A device-side failure (a progress wait that ran out of
+ * its budget) is latched in the handle's status word and reported by
+ * bb_status_sync.  Covers the paper's Algorithms 1 and 2 (Section III). */
+bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
+                    void* e_out, bb_stream_t stream);
+
+/* Same as bb_reduce with HOST buffers: copies band_host (ldab * n elements,
+ * not modified) to a device staging buffer owned by the handle, reduces it,
+ * copies d and e back to d_host / e_host, and synchronizes the stream before
+ * returning (so device-side failures are reported here too).  Pinned host
+ * memory gives the fastest copies.  The first call allocates the staging
+ * buffers (kept until bb_destroy). */
+bb_status bb_reduce_host(bb_handle* h, const void* band_host, int64_t ldab, int64_t tw,
+                         void* d_host, void* e_host, bb_stream_t stream);
+
+/* Free the handle and everything it owns.  NULL is ignored. */
+void bb_destroy(bb_handle* h);
+
+/* Smallest valid ldab: bw + 2*tw + 1. */
+int64_t bb_required_ldab(int64_t bw, int64_t tw);
+
+/* Synchronize the stream, then return and clear the handle's device status
+ * word: BB_OK, or BB_ERR_TIMEOUT if a wait in an earlier bb_reduce gave up
+ * (its results are then invalid). */
+bb_status bb_status_sync(bb_handle* h, bb_stream_t stream);
+
+/* Tuning and test parameters (bb_set_param / bb_get_param). */
+enum {
+    BB_PARAM_SCHEDULER = 0,     /* 0: persistent kernel with progress flags (default);
+                                   1: one kernel launch per cycle                       */
+    BB_PARAM_TPB = 1,           /* threads per block, multiple of 32 in [32, 1024];
+                                   0 = automatic (default)                              */
+    BB_PARAM_MAX_CTAS = 2,      /* cap on the persistent grid; 0 = co-resident maximum  */
+    BB_PARAM_WAIT_BUDGET_MS = 3,/* bound of one device-side wait, in ms (default 4000)  */
+    BB_PARAM_PASS_LO = 4,       /* run only passes [PASS_LO, PASS_HI) (default 0 .. all); */
+    BB_PARAM_PASS_HI = 5,       /*   the fill rows are zeroed only when PASS_LO == 0    */
+    BB_PARAM_STALL_SWEEP = 6,   /* fault injection: the CTA running this sweep of every
+                                   pass never reports progress (-1 = off, default)      */
+    BB_PARAM_TIMING = 7         /* 1: record CUDA events around every pass launch, read
+                                   back with bb_last_pass_ms (default 0)                */
+};
+bb_status bb_set_param(bb_handle* h, int param, int64_t value);
+int64_t bb_get_param(const bb_handle* h, int param);
+
+/* Pass plan of (bw, tw): number of passes, and the (b, t) of pass i. */
+int64_t bb_num_passes(int64_t bw, int64_t tw);
+bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t);
+
+/* Algorithmic bytes of pass i (or of all passes when i < 0) of an n x n
+ * reduction with element size elem_bytes: every element of each step's right
+ * block (rows p..ce x cols c..ce) and left block (rows c..ce x cols c..cend)
+ * counted once read and once written.  This is the traffic model behind the
+ * effective GB/s figure. */
+double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass);
+
+/* Number of steps (one horizontal plus one vertical reflector each) of pass
+ * i (all passes when i < 0). */
+int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass);
+
+/* Kernel launches made by the last bb_reduce / bb_reduce_host on this handle
+ * (fill-row zeroing, the passes, and the d/e extraction). */
+int64_t bb_last_launches(const bb_handle* h);
+
+/* With BB_PARAM_TIMING on: after the stream of the last bb_reduce has been
+ * synchronized, the number of passes it ran and the device time of pass i in
+ * milliseconds (CUDA events recorded on the launching stream around the
+ * pass's kernel launches).  Returns BB_ERR_INVALID_ARG if i is out of range
+ * or timing was off. */
+int64_t bb_last_num_passes(const bb_handle* h);
+bb_status bb_last_pass_ms(bb_handle* h, int64_t i, double* ms);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char* bb_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BB_H_ */

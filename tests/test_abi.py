@@ -1,0 +1,101 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/bb.h declares, and its host-side planner and traffic model agree with
+an enumeration written here from the definition of the windows."""
+import os
+import re
+
+import pytest
+
+import banded_svd_stage_gb300 as bb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "bb.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(bb_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bb.build()
+    return bb.lib()
+
+
+def test_header_declares_the_core_entry_points():
+    names = declared_functions()
+    for core in ("bb_create", "bb_reduce", "bb_destroy"):
+        assert core in names
+
+
+def test_library_exports_every_declared_function(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(bb.BBError):
+        bb.bb_create(100, 8, bb.BB_F32)
+    assert bb.bb_last_error()
+
+
+def test_null_handle_and_bad_params(lib):
+    assert lib.bb_reduce(None, None, 10, 1, None, None, None) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_set_param(None, 0, 0) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_status_sync(None, None) == bb.BB_ERR_INVALID_ARG
+    bb.bb_destroy(None)
+
+
+def _plan(bw, tw):
+    out, b = [], bw
+    while b > 1:
+        t = min(tw, b - 1)
+        out.append((b, t))
+        b -= t
+    return out
+
+
+def _enumerate(n, bw, tw, s):
+    """Steps and modeled bytes from the windows: right block rows p..ce x cols
+    c..ce, left block rows c..ce x cols c..cend, each element read + written."""
+    steps, byts = 0, 0
+    for (b, t) in _plan(bw, tw):
+        bp = b - t
+        for r in range(0, n - bp - 1):
+            k = 0
+            while True:
+                c = r + bp + k * b
+                if c + 1 > n - 1:
+                    break
+                p = r if k == 0 else c - b
+                ce = min(c + t, n - 1)
+                cend = min(ce + b, n - 1)
+                w = ce - c + 1
+                steps += 1
+                byts += 2 * s * ((ce - p + 1) * w + w * (cend - c + 1))
+                k += 1
+    return steps, byts
+
+
+@pytest.mark.parametrize("n,bw,tw", [(2, 1, 1), (10, 3, 1), (64, 16, 8), (100, 17, 5), (257, 64, 16),
+                                     (300, 40, 39)])
+def test_planner_and_traffic_model(lib, n, bw, tw):
+    plan = _plan(bw, tw)
+    assert bb.bb_num_passes(bw, tw) == len(plan)
+    for i, bt in enumerate(plan):
+        assert bb.bb_pass_info(bw, tw, i) == bt
+    steps, byts = _enumerate(n, bw, tw, 4)
+    assert bb.bb_model_steps(n, bw, tw) == steps
+    assert bb.bb_model_bytes(n, bw, tw, 4) == pytest.approx(byts, rel=1e-12)
+    per_pass = sum(bb.bb_model_bytes(n, bw, tw, 4, i) for i in range(len(plan)))
+    assert per_pass == pytest.approx(byts, rel=1e-12)
+
+
+def test_required_ldab(lib):
+    assert bb.bb_required_ldab(256, 32) == 321
+    assert bb.bb_required_ldab(8, 7) == 23

@@ -1,0 +1,191 @@
+"""Parity of the CUDA library (through the C ABI) with the CPU oracle.
+
+Acceptance (the oracle runs in the same precision as the GPU path):
+  * singular values of the bidiagonal: max |sigma - sigma_ref| / ||A||_F at
+    most 1e-12 (float64) or 2e-5 (float32);
+  * |d| and |e|: max | |d|-|d_ref| |, | |e|-|e_ref| | / ||A||_F at most
+    max(that tolerance, 32 x the oracle's own change under a one-ulp input
+    perturbation) -- see gpu_helpers.DE_FACTOR for why the entries need the
+    measured conditioning while the singular values do not.
+"""
+import numpy as np
+import pytest
+
+import band_inputs as bi
+import banded_svd_stage_gb300 as bb
+import oracle
+from gpu_helpers import (DE_FACTOR, TOL, de_error, fourth_moment_band, fourth_moment_bidiagonal,
+                         fro_of_band, gpu_reduce, off_bidiagonal_nonzeros, oracle_sensitivity, record,
+                         sigma_bidiagonal)
+
+pytestmark = pytest.mark.gpu
+
+EDGE_CASES = [
+    # (n, bw, tw): tiny orders, ragged ends, every lag class, several tiles
+    (1, 0, 1), (2, 1, 1), (3, 2, 1), (4, 3, 1), (5, 3, 2), (8, 4, 3), (16, 8, 7), (24, 6, 2),
+    (24, 6, 4), (33, 10, 4), (40, 8, 7), (48, 12, 5), (64, 16, 8), (64, 16, 15), (50, 20, 9),
+    (60, 9, 8), (70, 17, 16), (30, 29, 7), (45, 40, 13), (97, 33, 32), (130, 64, 32),
+    (300, 100, 33), (257, 128, 64), (600, 96, 32), (1000, 64, 16), (777, 256, 32),
+]
+
+
+def check_against_oracle(band, n, bw, tw, dt, scheduler, params=None):
+    d_ref, e_ref = oracle.bidiagonal(band, n, bw, tw)
+    d, e = gpu_reduce(band, n, bw, tw, dt, scheduler, params)
+    return assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler)
+
+
+def assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler=0):
+    fro = max(fro_of_band(band), 1e-300)
+    s = sigma_bidiagonal(d, e)
+    s_ref = sigma_bidiagonal(d_ref, e_ref)
+    serr = float(np.abs(s - s_ref).max()) / fro if n else 0.0
+    err = de_error(d, e, d_ref, e_ref, fro)
+    tol_de, sens = TOL[dt], None
+    if err > tol_de:
+        sens = oracle_sensitivity(band, n, bw, tw)
+        tol_de = max(TOL[dt], DE_FACTOR * sens)
+    record("parity", n=n, bw=bw, tw=tw, dt=dt, scheduler=scheduler, sigma_err=serr, de_err=err,
+           de_sens=sens, de_tol=tol_de)
+    assert serr <= TOL[dt], f"sigma error {serr:.3e} > {TOL[dt]}"
+    assert err <= tol_de, f"|d|,|e| error {err:.3e} > {tol_de:.3e} (oracle sensitivity {sens})"
+    return err
+
+
+@pytest.mark.parametrize("scheduler", [0, 1])
+@pytest.mark.parametrize("dt", ["f64", "f32"])
+@pytest.mark.parametrize("n,bw,tw", EDGE_CASES)
+def test_edge_cases(n, bw, tw, dt, scheduler):
+    band = bi.make_band(n, bw, tw, dt, "normal", seed=n + 17 * bw + tw)
+    check_against_oracle(band, n, bw, tw, dt, scheduler)
+
+
+@pytest.mark.parametrize("scheduler", [0, 1])
+def test_workload_n256_full(scheduler):
+    w = bi.WORKLOADS[0]
+    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler)
+
+
+@pytest.mark.parametrize("scheduler", [0, 1])
+def test_workload_n4096_full(scheduler):
+    w = bi.WORKLOADS[1]
+    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler)
+
+
+def test_workload_n8192_full():
+    w = bi.WORKLOADS[2]
+    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, 0)
+
+
+@pytest.mark.parametrize("idx", [3, 4])
+@pytest.mark.parametrize("n", [1536, 2111])
+def test_wide_workloads_at_oracle_size(idx, n):
+    # the n16384 and n32768 recipes (same bw, tw, dtype, distribution) at a
+    # size the oracle finishes in seconds; 2111 leaves a ragged last block
+    w = bi.WORKLOADS[idx]
+    check_against_oracle(bi.make_workload(w, n=n), n, w.bw, w.tw, w.dtype, 0)
+
+
+@pytest.mark.parametrize("idx", [2, 3])
+def test_full_size_passes_keep_band_structure_and_moments(idx):
+    """After every pass at full size the band has exactly the planned
+    bandwidth (all entries outside it are 0) and ||A||_F and ||A^T A||_F are
+    unchanged: each pass is an orthogonal two-sided transform to a band."""
+    w = bi.WORKLOADS[idx]
+    band = bi.make_workload(w)
+    ku = w.bw + w.tw
+    fro = fro_of_band(band)
+    m4 = fourth_moment_band(band, w.n, w.bw, w.tw)
+    for pi, (b, t) in enumerate(oracle.pass_plan(w.bw, w.tw)):
+        _, _, got = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0,
+                               {bb.BB_PARAM_PASS_LO: 0, bb.BB_PARAM_PASS_HI: pi + 1}, return_band=True)
+        bnew = b - t
+        j = np.arange(w.n)[:, None]
+        q = np.arange(got.shape[1])[None, :]
+        i = j + q - ku
+        inside = (j - i >= 0) & (j - i <= bnew)
+        valid = (i >= 0) & (i < w.n)
+        assert np.count_nonzero(got[valid & ~inside]) == 0, f"pass {pi}: entries outside bandwidth {bnew}"
+        g = np.zeros((w.n, bnew + 2 * w.tw + 1), dtype=np.float64)
+        g[:, w.tw: w.tw + bnew + 1] = got[:, ku - bnew: ku + 1]
+        tol2 = 1e-13 if w.dtype == "f64" else 2e-5
+        assert abs(fro_of_band(g) - fro) <= tol2 * fro
+        tol4 = 1e-12 if w.dtype == "f64" else 1e-4
+        assert abs(fourth_moment_band(g, w.n, bnew, w.tw) - m4) <= tol4 * m4
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_full_size_properties(idx):
+    """Full workloads in the benchmark's launch configuration: the result is
+    exactly bidiagonal, and the second and fourth moments of the singular
+    values (||A||_F^2 and ||A^T A||_F^2) are preserved."""
+    w = bi.WORKLOADS[idx]
+    band = bi.make_workload(w)
+    d, e, after = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0, return_band=True)
+    assert off_bidiagonal_nonzeros(after, w.n, w.bw + w.tw) == 0
+    fro = fro_of_band(band)
+    f2 = np.sqrt(float(d.astype(np.float64) @ d.astype(np.float64) + e.astype(np.float64) @ e.astype(np.float64)))
+    tol2 = 1e-13 if w.dtype == "f64" else 2e-5
+    assert abs(f2 - fro) <= tol2 * fro
+    m4 = fourth_moment_band(band, w.n, w.bw, w.tw)
+    m4b = fourth_moment_bidiagonal(d, e)
+    tol4 = 1e-12 if w.dtype == "f64" else 1e-4
+    assert abs(m4b - m4) <= tol4 * m4
+
+
+@pytest.mark.parametrize("idx", [2, 3])
+def test_full_size_schedulers_agree_bitwise(idx):
+    """The per-cycle and the persistent schedulers run the same half-steps
+    with the same arithmetic in different interleavings; any race would make
+    them differ."""
+    w = bi.WORKLOADS[idx]
+    band = bi.make_workload(w)
+    d0, e0 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0)
+    d1, e1 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 1)
+    assert np.array_equal(d0, d1) and np.array_equal(e0, e1)
+
+
+def test_persistent_deterministic_and_grid_independent():
+    w = bi.WORKLOADS[2]
+    band = bi.make_workload(w)
+    d0, e0 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0)
+    d1, e1 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0, {bb.BB_PARAM_MAX_CTAS: 7})
+    d2, e2 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0, {bb.BB_PARAM_TPB: 256})
+    assert np.array_equal(d0, d1) and np.array_equal(e0, e1)
+    assert np.array_equal(d0, d2) and np.array_equal(e0, e2)
+
+
+def test_reduce_host_matches_device():
+    w = bi.WORKLOADS[1]
+    band = bi.make_workload(w)
+    d0, e0 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0)
+    h = bb.bb_create(w.n, w.bw, bb.BB_F32)
+    d = np.zeros(w.n, np.float32)
+    e = np.zeros(w.n - 1, np.float32)
+    src = band.copy()
+    bb.bb_reduce_host(h, src, band.shape[1], w.tw, d, e)
+    bb.bb_destroy(h)
+    assert np.array_equal(src, band)  # host input untouched
+    assert np.array_equal(d, d0) and np.array_equal(e, e0)
+
+
+def test_larger_ldab_and_untouched_rows():
+    n, bw, tw = 500, 40, 12
+    band = bi.make_band(n, bw, tw, "f64", "normal", seed=3, ldab=bw + 2 * tw + 1 + 5)
+    band[:, bw + 2 * tw + 1:] = 7.0  # rows beyond ku + tw must not be touched
+    d, e, after = gpu_reduce(band, n, bw, tw, "f64", 0, return_band=True)
+    assert np.all(after[:, bw + 2 * tw + 1:] == 7.0)
+    inner = np.ascontiguousarray(band[:, : bw + 2 * tw + 1])
+    d_ref, e_ref = oracle.bidiagonal(inner, n, bw, tw)
+    assert_parity(d, e, d_ref, e_ref, inner, n, bw, tw, "f64")
+
+
+def test_garbage_in_fill_rows_is_cleared():
+    n, bw, tw = 400, 30, 9
+    band = bi.make_band(n, bw, tw, "f32", "normal", seed=8)
+    clean = band.copy()
+    band[:, :tw] = 123.0
+    band[:, bw + tw + 1:] = -55.0
+    d_ref, e_ref = oracle.bidiagonal(clean, n, bw, tw)
+    d, e = gpu_reduce(band, n, bw, tw, "f32", 0)
+    assert_parity(d, e, d_ref, e_ref, clean, n, bw, tw, "f32")
