@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             "bb_last_num_passes": ([p], i64),
             "bb_last_pass_ms": ([p, i64, ctypes.POINTER(cd)], ci),
             "bb_last_error": ([], ctypes.c_char_p),
+            "bb_reduce_noalloc": ([p, i64, i64, i64, i64, ci, p, p, p], ci),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -171,6 +172,14 @@ def bb_last_pass_ms(h, i: int) -> float:
     ms = ctypes.c_double()
     _check(lib().bb_last_pass_ms(h, i, ctypes.byref(ms)))
     return ms.value
+
+
+def bb_reduce_noalloc(band, n: int, bw: int, ldab: int, tw: int, dtype: int, d_out, e_out,
+                      stream=None) -> None:
+    """Reduction with no device allocation (fixed in-library scratch, n <= 65536);
+    synchronizes the stream before returning."""
+    _check(lib().bb_reduce_noalloc(_addr(band), n, bw, ldab, tw, dtype, _addr(d_out), _addr(e_out),
+                                   _stream(stream)))
 
 
 def dtype_code(dtype) -> int:

@@ -403,3 +403,7 @@ int auto_tpb(int b, int t) {
     return std::min(1024, std::max(64, tpb));
 }
 }  // namespace bb
+
+namespace bb {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace bb

@@ -145,6 +145,29 @@ bb_status bb_last_pass_ms(bb_handle* h, int64_t i, double* ms);
 /* Message of the last error on the calling thread ("" if none). */
 const char* bb_last_error(void);
 
+/* The whole reduction without allocating device memory (the paper has no
+ * counterpart; this is a library convenience).  For callers that cannot
+ * allocate when they need the reduction: their device memory belongs to
+ * another allocator or a fixed pool, or they cannot afford cudaMalloc /
+ * cudaFree there (cudaFree synchronizes the device; both can stall or fail
+ * under a memory budget).  bb_create allocates, so those callers use this
+ * instead.  The caller passes the band (ldab * n elements, overwritten) and
+ * d_out (n) / e_out (n-1), all device pointers, with the same meaning and
+ * limits as bb_reduce, plus n <= 65536.  Larger n is rejected with
+ * BB_ERR_INVALID_ARG and nothing is launched.
+ * Scratch: the persistent scheduler's progress counters and status word live
+ * in a fixed array of the library's device image (65536 + 64 int32, held by
+ * every device that loads the library until the process exits).  The first
+ * call on a device looks up that array's device address (cudaGetSymbolAddress)
+ * with the device current; make that first call before any stream capture.
+ * Every call uses the same array: calls that overlapped on the GPU would race,
+ * so the function serializes its callers, clears the status word each call,
+ * and returns only after the work on `stream` has finished (it synchronizes
+ * the stream) -- which also lets it report a device-side timeout
+ * (BB_ERR_TIMEOUT) directly.  Calls no allocating CUDA or library routine. */
+bb_status bb_reduce_noalloc(void* band_ptr, int64_t n, int64_t bw, int64_t ldab, int64_t tw,
+                            bb_dtype dtype, void* d_out, void* e_out, bb_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
