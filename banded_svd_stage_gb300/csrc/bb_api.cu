@@ -277,8 +277,8 @@ static bb_status check_reduce_args(bb_handle* h, int64_t ldab, int64_t tw) {
     auto plan = plan_passes(h->bw, tw);
     for (auto& ps : plan) {
         int w = ps.t + 1;
-        int wm = w <= 9 ? 9 : (w <= 17 ? 17 : (w <= 33 ? 33 : 65));
-        size_t smem = elem_size(h->dtype) * ((size_t)wm + 2 + (size_t)(ps.b + ps.t + 1) * (wm | 1));
+        int wm = w <= 8 ? 8 : w <= 9 ? 9 : w <= 16 ? 16 : w <= 17 ? 17 : w <= 32 ? 32 : w <= 33 ? 33 : 65;
+        size_t smem = elem_size(h->dtype) * ((size_t)wm + 2 + (size_t)(2 * (ps.b + ps.t) + 1) * (wm | 1));
         if (smem > 227 * 1024)
             return fail(BB_ERR_INVALID_ARG, "bandwidth too large for the shared-memory tile");
     }

@@ -156,151 +156,278 @@ __device__ __forceinline__ T warp_larfg(T (&x)[NPL], int w, int lane, T* s_v, T*
     return beta;
 }
 
-// Shared-memory layout of one CTA.
-//   v[WMAX]          reflector of the current half-step
-//   tau              its scalar
-//   tile[ncol][WP]   the column block of the left half-step: rows c..ce of
-//                    columns c..cend, column-major with odd column stride WP
+// Shared-memory layout of one CTA (ncolmax = b + t + 1 of the pass).
+//   v[WMAX]              reflector of the current half-step
+//   tau                  its scalar
+//   tile[ncolmax][WP]    the column block of the left half-step: rows c..ce of
+//                        columns c..cend, column-major with odd column stride WP
+//   rtile[ncolmax-1][WP] the row block of the right half-step: rows p+1..ce of
+//                        columns c..ce, row-major with odd row stride WP
 template <typename T>
 struct Smem {
     T* v;
     T* tau;
     T* tile;
+    T* rtile;
     int wp;
 };
 
 template <typename T, int WMAX>
-__device__ __forceinline__ Smem<T> carve_smem(unsigned char* raw) {
+__device__ __forceinline__ Smem<T> carve_smem(unsigned char* raw, int ncolmax) {
     Smem<T> s;
     T* p = reinterpret_cast<T*>(raw);
+    s.wp = WMAX | 1;
     s.v = p;
     s.tau = p + WMAX;
     s.tile = p + WMAX + 2;
-    s.wp = WMAX | 1;
+    s.rtile = s.tile + (size_t)ncolmax * s.wp;
     return s;
+}
+
+// Asynchronous 4- or 8-byte copy global -> shared (no register staging); the
+// copies a thread issued are complete after cp_async_wait_all().
+template <typename T>
+__device__ __forceinline__ void cp_async_elem(T* smem_dst, const T* gsrc) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(gsrc), "n"(sizeof(T))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Geometry of step k of sweep r (pass (b, t), b' = b - t):
+//   c = r + b' + k b, p = r (k = 0) or c - b, ce = min(c + t, n-1),
+//   cend = min(ce + b, n-1); right block rows p..ce x cols c..ce, left block
+//   rows c..ce x cols c..cend.
+struct StepGeom {
+    long long c, p, ce, cend;
+    int w;      // ce - c + 1: reflector length
+    int nrows;  // ce - p: rows p+1..ce of the right apply
+    int ncol;   // cend - c + 1: columns of the left block
+};
+
+__device__ __forceinline__ StepGeom step_geom(const PassArgs& P, int r, int k) {
+    StepGeom g;
+    g.c = (long long)r + P.bp + (long long)k * P.b;
+    g.p = (k == 0) ? (long long)r : g.c - P.b;
+    g.ce = min(g.c + (long long)P.t, P.n - 1);
+    g.cend = min(g.ce + (long long)P.b, P.n - 1);
+    g.w = (int)(g.ce - g.c + 1);
+    g.nrows = (int)(g.ce - g.p);
+    g.ncol = (int)(g.cend - g.c + 1);
+    return g;
+}
+
+// Rows of the right block (from row c - 1, or c + 1 on the last pass) and
+// columns of the left block (from column c + b - 1, or c + b + 1) that the
+// half-step awaited by the progress wait may still write.  Everything before
+// them was last written by half-steps already known to be complete when the
+// previous wait of the same sweep returned, so it may be read before the
+// wait.  (Exhaustive check over all (n, b, t) with b < 26 of the half-step
+// protocol; for b - t == 2 nothing is late and the rule is conservative.)
+__device__ __forceinline__ long long late_row(const PassArgs& P, long long c) {
+    return (P.lagh == 4) ? c + 1 : c - 1;
+}
+__device__ __forceinline__ long long late_col(const PassArgs& P, long long c) {
+    return (P.lagh == 4) ? c + P.b + 1 : c + P.b - 1;
 }
 
 // ---------------------------------------------------------------------------
 // Right (horizontal) half-step of sweep r, step k: reflector from row p over
-// columns c..ce, applied from the right to rows p+1..ce.  Rows c..ce of the
-// result (the part the left half-step needs) are also left in the tile.
+// columns c..ce, applied from the right to rows p+1..ce.  Rows p+1..c-1 are
+// stored; rows c..ce (the square the left half-step starts from) are left in
+// the tile only and reach memory with the left half-step's block.  That is
+// safe for the progress protocol: any later half-step that touches the square
+// also touches the left half-step's block, so it already waits for the left
+// half-step.
+//
+// Split in two around the progress wait.  right_pre (k >= 1): the reflector
+// input, row p = c - b, is row 0 of the previous left block, still in the
+// tile, so the reflector is built before the wait, and rows before late_row
+// start copying into rtile.  right_post copies the late rows (or, for k = 0,
+// everything after building the reflector from memory) and applies.
 // ---------------------------------------------------------------------------
-template <typename T, int WMAX>
-__device__ __forceinline__ void right_half(T* __restrict__ band, const PassArgs& P, int r, int k,
-                                           const Smem<T>& sm) {
-    constexpr int NPL = (WMAX + 31) / 32;
-    const long long stride = P.ldab - 1;
-    T* __restrict__ base = band + P.ku;
-    const long long c = (long long)r + P.bp + (long long)k * P.b;
-    const long long p = (k == 0) ? (long long)r : c - P.b;
-    const long long ce = min(c + (long long)P.t, P.n - 1);
-    const int w = (int)(ce - c + 1);
-    const int nrows = (int)(ce - p);  // rows p+1 .. ce
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    const int lane = tid & 31;
 
-    // Stage: warp 0 holds row p (entries m = lane + 32 q); every thread loads
-    // the first chunk of its rows before the reflector is known.
-    T xp[NPL];
-    if (tid < 32) {
-#pragma unroll
-        for (int q = 0; q < NPL; ++q) {
-            int m = lane + 32 * q;
-            xp[q] = (m < w) ? __ldcg(base + p + (c + m) * stride) : T(0);
-        }
-    }
-    T x[WMAX];
-    int i_loc = tid;  // row p + 1 + i_loc
-    if (i_loc < nrows) {
-        const T* src = base + (p + 1 + i_loc) + c * stride;
+// Copy rows [i0, i1) (local: row p + 1 + i) of the right block into rtile.
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ void copy_rows(const T* __restrict__ base, long long stride, const StepGeom& g,
+                                          int i0, int i1, const Smem<T>& sm) {
+    const int W = FULL ? WMAX : g.w;
+    for (int i = i0 + (int)threadIdx.x; i < i1; i += blockDim.x) {
+        const T* src = base + (g.p + 1 + i) + g.c * stride;
+        T* dst = sm.rtile + i * sm.wp;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < w) x[m] = __ldcg(src + m * stride);
+            if (m < W) cp_async_elem<T>(dst + m, src + m * stride);
     }
-    if (tid < 32) {
-        T beta = warp_larfg<T, NPL>(xp, w, lane, sm.v, sm.tau);
-        // row p becomes (beta, 0, ..., 0)
+}
+
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ bool right_pre(T* __restrict__ band, const PassArgs& P, int r, int k,
+                                          const Smem<T>& sm) {
+    constexpr int NPL = (WMAX + 31) / 32;
+    if (k == 0) return false;
+    const StepGeom g = step_geom(P, r, k);
+    const int W = FULL ? WMAX : g.w;
+    const int lane = threadIdx.x & 31;
+    const long long stride = P.ldab - 1;
+    T* __restrict__ base = band + P.ku;
+    const int i_late = (int)min((long long)g.nrows, max(0LL, late_row(P, g.c) - g.p - 1));
+    copy_rows<T, WMAX, FULL>(base, stride, g, 0, i_late, sm);
+    cp_async_commit();
+    if (threadIdx.x < 32) {
+        T xp[NPL];
 #pragma unroll
         for (int q = 0; q < NPL; ++q) {
-            int m = lane + 32 * q;
-            if (m < w) base[p + (c + m) * stride] = (m == 0) ? beta : T(0);
+            const int m = lane + 32 * q;
+            xp[q] = (m < W) ? sm.tile[(P.b + m) * sm.wp] : T(0);
+        }
+        T beta = warp_larfg<T, NPL>(xp, W, lane, sm.v, sm.tau);
+#pragma unroll
+        for (int q = 0; q < NPL; ++q) {
+            const int m = lane + 32 * q;
+            if (m < W) base[g.p + (g.c + m) * stride] = (m == 0) ? beta : T(0);
         }
     }
+    return true;
+}
+
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ void right_post(T* __restrict__ band, const PassArgs& P, int r, int k,
+                                           const Smem<T>& sm, bool pre) {
+    constexpr int NPL = (WMAX + 31) / 32;
+    const StepGeom g = step_geom(P, r, k);
+    const int W = FULL ? WMAX : g.w;
+    const long long stride = P.ldab - 1;
+    T* __restrict__ base = band + P.ku;
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
+    if (pre) {
+        const int i_late = (int)min((long long)g.nrows, max(0LL, late_row(P, g.c) - g.p - 1));
+        copy_rows<T, WMAX, FULL>(base, stride, g, i_late, g.nrows, sm);
+    } else {
+        copy_rows<T, WMAX, FULL>(base, stride, g, 0, g.nrows, sm);
+        if (tid < 32) {
+            T xp[NPL];
+#pragma unroll
+            for (int q = 0; q < NPL; ++q) {
+                const int m = lane + 32 * q;
+                xp[q] = (m < W) ? __ldcg(base + g.p + (g.c + m) * stride) : T(0);
+            }
+            T beta = warp_larfg<T, NPL>(xp, W, lane, sm.v, sm.tau);
+#pragma unroll
+            for (int q = 0; q < NPL; ++q) {
+                const int m = lane + 32 * q;
+                if (m < W) base[g.p + (g.c + m) * stride] = (m == 0) ? beta : T(0);
+            }
+        }
+    }
+    cp_async_commit();
+    cp_async_wait_all();
     __syncthreads();
     const T tau = *sm.tau;
-    const long long row_c = c - p - 1;  // local index of row c
-    for (; i_loc < nrows; i_loc += nthr) {
-        if (i_loc >= nthr) {  // later chunks: load now
-            const T* src = base + (p + 1 + i_loc) + c * stride;
+    const int row_c = (int)(g.c - g.p - 1);  // local index of row c
+    for (int i = tid; i < g.nrows; i += nthr) {
+        T x[WMAX];
+        const T* src = sm.rtile + i * sm.wp;
 #pragma unroll
-            for (int m = 0; m < WMAX; ++m)
-                if (m < w) x[m] = __ldcg(src + m * stride);
-        }
+        for (int m = 0; m < WMAX; ++m)
+            if (m < W) x[m] = src[m];
         if (tau != T(0)) {
             T y = 0;
 #pragma unroll
             for (int m = 0; m < WMAX; ++m)
-                if (m < w) y = fma(x[m], sm.v[m], y);
+                if (m < W) y = fma(x[m], sm.v[m], y);
             const T s = tau * y;
 #pragma unroll
             for (int m = 0; m < WMAX; ++m)
-                if (m < w) x[m] = fma(-s, sm.v[m], x[m]);
+                if (m < W) x[m] = fma(-s, sm.v[m], x[m]);
         }
-        T* dst = base + (p + 1 + i_loc) + c * stride;
-#pragma unroll
-        for (int m = 0; m < WMAX; ++m)
-            if (m < w) dst[m * stride] = x[m];
-        const long long rr = i_loc - row_c;  // row c + rr
-        if (rr >= 0) {
+        const int rr = i - row_c;  // row c + rr
+        if (rr < 0) {
+            T* dst = base + (g.p + 1 + i) + g.c * stride;
 #pragma unroll
             for (int m = 0; m < WMAX; ++m)
-                if (m < w) sm.tile[m * sm.wp + rr] = x[m];
+                if (m < W) dst[m * stride] = x[m];
+        } else {
+#pragma unroll
+            for (int m = 0; m < WMAX; ++m)
+                if (m < W) sm.tile[m * sm.wp + rr] = x[m];
         }
     }
 }
 
 // ---------------------------------------------------------------------------
 // Left (vertical) half-step of sweep r, step k: reflector from column c over
-// rows c..ce, applied from the left to columns c+1..cend.  Expects the tile's
-// first w columns to hold rows c..ce of columns c..ce (left there by the
-// right half-step of the same step, which this CTA ran just before).
+// rows c..ce, applied from the left to columns c+1..cend.  The tile's first w
+// columns hold rows c..ce of columns c..ce (left there by the right half-step
+// of the same step).  left_pre builds the reflector from the tile and starts
+// copying the columns before late_col; left_post copies the rest, applies and
+// stores the whole block (columns c..cend, rows c..ce).
 // ---------------------------------------------------------------------------
-template <typename T, int WMAX>
-__device__ __forceinline__ void left_half(T* __restrict__ band, const PassArgs& P, int r, int k,
-                                          const Smem<T>& sm) {
+
+// Copy columns [j0, j1) (local indices) of rows c..ce of the left block from
+// memory into the tile; element e -> (column j0 + e / w, row e % w), so that
+// consecutive threads read consecutive addresses.
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ void copy_columns(const T* __restrict__ base, long long stride, const StepGeom& g,
+                                             int j0, int j1, const Smem<T>& sm) {
+    const int w = FULL ? WMAX : g.w;
+    if (j1 <= j0) return;
+    const int total = (j1 - j0) * w;
+    // e / w == umulhi(e, magic) for e < 2^16 and w >= 2 (a step has w >= 2)
+    const unsigned magic = 0xffffffffu / (unsigned)w + 1u;
+    const T* src0 = base + g.c + (g.c + j0) * stride;
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+        const int jl = (int)__umulhi((unsigned)e, magic);
+        const int m = e - jl * w;
+        cp_async_elem<T>(sm.tile + (j0 + jl) * sm.wp + m, src0 + m + (long long)jl * stride);
+    }
+}
+
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ void left_pre(T* __restrict__ band, const PassArgs& P, int r, int k,
+                                         const Smem<T>& sm) {
     constexpr int NPL = (WMAX + 31) / 32;
+    const StepGeom g = step_geom(P, r, k);
+    const int W = FULL ? WMAX : g.w;
+    const int lane = threadIdx.x & 31;
     const long long stride = P.ldab - 1;
     T* __restrict__ base = band + P.ku;
-    const long long c = (long long)r + P.bp + (long long)k * P.b;
-    const long long ce = min(c + (long long)P.t, P.n - 1);
-    const long long cend = min(ce + (long long)P.b, P.n - 1);
-    const int w = (int)(ce - c + 1);
-    const int ncol = (int)(cend - c + 1);
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    const int lane = tid & 31, warp = tid >> 5, nwarp = nthr >> 5;
-    const int wp = sm.wp;
-
-    // Stage the columns ce+1 .. cend (a warp per column, lanes over rows).
-    for (int jl = w + warp; jl < ncol; jl += nwarp) {
-        const T* src = base + c + (c + jl) * stride;
-        for (int m = lane; m < w; m += 32) sm.tile[jl * wp + m] = __ldcg(src + m);
-    }
-    __syncthreads();
-    if (tid < 32) {
+    __syncthreads();  // the right half-step's rows are in the tile
+    const int jlate = (int)min((long long)g.ncol, max((long long)W, late_col(P, g.c) - g.c));
+    copy_columns<T, WMAX, FULL>(base, stride, g, W, jlate, sm);
+    cp_async_commit();
+    if (threadIdx.x < 32) {
         T xc[NPL];
 #pragma unroll
         for (int q = 0; q < NPL; ++q) {
-            int m = lane + 32 * q;
-            xc[q] = (m < w) ? sm.tile[m] : T(0);
+            const int m = lane + 32 * q;
+            xc[q] = (m < W) ? sm.tile[m] : T(0);
         }
-        T beta = warp_larfg<T, NPL>(xc, w, lane, sm.v, sm.tau);
+        T beta = warp_larfg<T, NPL>(xc, W, lane, sm.v, sm.tau);
         __syncwarp();
 #pragma unroll
         for (int q = 0; q < NPL; ++q) {
-            int m = lane + 32 * q;
-            if (m < w) sm.tile[m] = (m == 0) ? beta : T(0);
+            const int m = lane + 32 * q;
+            if (m < W) sm.tile[m] = (m == 0) ? beta : T(0);
         }
     }
+}
+
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ void left_post(T* __restrict__ band, const PassArgs& P, int r, int k,
+                                          const Smem<T>& sm) {
+    const StepGeom g = step_geom(P, r, k);
+    const int W = FULL ? WMAX : g.w;
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const long long stride = P.ldab - 1;
+    T* __restrict__ base = band + P.ku;
+    const int wp = sm.wp, w = W, ncol = g.ncol;
+    const long long c = g.c;
+    const int jlate = (int)min((long long)ncol, max((long long)w, late_col(P, c) - c));
+    copy_columns<T, WMAX, FULL>(base, stride, g, jlate, ncol, sm);
+    cp_async_commit();
+    cp_async_wait_all();
     __syncthreads();
     const T tau = *sm.tau;
     if (tau != T(0)) {
@@ -321,10 +448,16 @@ __device__ __forceinline__ void left_half(T* __restrict__ band, const PassArgs& 
         }
     }
     __syncthreads();
-    // Write the whole block back (columns c .. cend, rows c .. ce).
-    for (int jl = warp; jl < ncol; jl += nwarp) {
-        T* dst = base + c + (c + jl) * stride;
-        for (int m = lane; m < w; m += 32) dst[m] = sm.tile[jl * wp + m];
+    // Write the whole block back (columns c .. cend, rows c .. ce), element
+    // e -> (column e / w, row e % w), so that consecutive threads write
+    // consecutive addresses across column boundaries.
+    const int total = ncol * w;
+    const unsigned magic = 0xffffffffu / (unsigned)w + 1u;
+    T* dst0 = base + c + c * stride;
+    for (int e = tid; e < total; e += nthr) {
+        const int jl = (int)__umulhi((unsigned)e, magic);
+        const int m = e - jl * w;
+        dst0[m + (long long)jl * stride] = sm.tile[jl * wp + m];
     }
 }
 
@@ -345,7 +478,7 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
     return v;
 }
 
-// Block-wide wait until *flag >= target.  Thread 0 spins with acquire loads;
+// Block-wide wait until *flag >= target.  Thread 0 spins with relaxed loads;
 // the wait is bounded by P.wait_budget SM clock cycles and by an iteration
 // cap, and gives up early if another CTA has already latched an error.  On
 // giving up it latches kStatusTimeout and the block returns false.
@@ -353,11 +486,11 @@ __device__ __forceinline__ bool block_wait(const int* flag, int target, int* sta
                                            const PassArgs& P, int* s_flag) {
     if (threadIdx.x == 0) {
         int ok = 1;
-        if (ld_acquire_gpu(flag) < target) {
+        if (ld_relaxed_gpu(flag) < target) {
             const long long t0 = clock64();
             unsigned int it = 0;
             for (;;) {
-                if (ld_acquire_gpu(flag) >= target) break;
+                if (ld_relaxed_gpu(flag) >= target) break;
                 ++it;
                 if ((it & 255u) == 0u) {
                     if (ld_relaxed_gpu(status) != kStatusOk) { ok = 0; break; }
@@ -369,6 +502,9 @@ __device__ __forceinline__ bool block_wait(const int* flag, int target, int* sta
                 }
             }
         }
+        // the value seen is final (counters only grow): one acquire load
+        // orders this block's later reads after the producer's writes
+        if (ok) (void)ld_acquire_gpu(flag);
         *s_flag = ok;
     }
     __syncthreads();
@@ -395,8 +531,28 @@ __device__ __forceinline__ void block_publish(int* flag, int value) {
 // addressing state, so the block size is capped to leave it the registers.
 template <typename T, int WMAX>
 struct MaxThreads {
-    static constexpr int value = (WMAX * sizeof(T) <= 33 * 4) ? 512 : 256;
+    static constexpr int value = (WMAX * sizeof(T) <= 17 * 4) ? 512 : ((WMAX * sizeof(T) <= 33 * 4) ? 384 : 256);
 };
+
+// One step (right then left half-step) of sweep r under the persistent
+// scheduler; false if a wait gave up.
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ bool persistent_step(T* __restrict__ band, const PassArgs& P, int r, int k,
+                                                int K, int Hprev, bool publish, int* __restrict__ progress,
+                                                int* __restrict__ status, const Smem<T>& sm, int* s_flag) {
+    const bool pre = right_pre<T, WMAX, FULL>(band, P, r, k, sm);
+    if (r > 0 && !block_wait(progress + r - 1, min(2 * k + P.lagh, Hprev), status, P, s_flag)) return false;
+    right_post<T, WMAX, FULL>(band, P, r, k, sm, pre);
+    if (publish) block_publish(progress + r, 2 * k + 1);
+    left_pre<T, WMAX, FULL>(band, P, r, k, sm);
+    if (r > 0 && !block_wait(progress + r - 1, min(2 * k + 1 + P.lagh, Hprev), status, P, s_flag))
+        return false;
+    left_post<T, WMAX, FULL>(band, P, r, k, sm);
+    if (k == K - 1 && r > 0 && !block_wait(progress + r - 1, Hprev, status, P, s_flag)) return false;
+    if (publish) block_publish(progress + r, 2 * k + 2);
+    else __syncthreads();
+    return true;
+}
 
 template <typename T, int WMAX>
 __global__ void __launch_bounds__(MaxThreads<T, WMAX>::value)
@@ -404,24 +560,19 @@ pass_persistent_kernel(T* __restrict__ band, PassArgs P, int* __restrict__ progr
                        int* __restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_flag;
-    const Smem<T> sm = carve_smem<T, WMAX>(smem_raw);
+    const Smem<T> sm = carve_smem<T, WMAX>(smem_raw, P.b + P.t + 1);
     if (ld_relaxed_gpu(status) != kStatusOk) return;
     for (int r = blockIdx.x; r < P.nsweeps; r += gridDim.x) {
         const int K = sweep_steps(P, r);
         const int Hprev = (r > 0) ? 2 * sweep_steps(P, r - 1) : 0;
         const bool publish = (r != P.stall_sweep);
         for (int k = 0; k < K; ++k) {
-            if (r > 0 && !block_wait(progress + r - 1, min(2 * k + P.lagh, Hprev), status, P, &s_flag))
-                return;
-            right_half<T, WMAX>(band, P, r, k, sm);
-            if (publish) block_publish(progress + r, 2 * k + 1);
-            else __syncthreads();
-            if (r > 0 && !block_wait(progress + r - 1, min(2 * k + 1 + P.lagh, Hprev), status, P, &s_flag))
-                return;
-            left_half<T, WMAX>(band, P, r, k, sm);
-            if (k == K - 1 && r > 0 && !block_wait(progress + r - 1, Hprev, status, P, &s_flag)) return;
-            if (publish) block_publish(progress + r, 2 * k + 2);
-            else __syncthreads();
+            const bool ok = (step_geom(P, r, k).w == WMAX)
+                                ? persistent_step<T, WMAX, true>(band, P, r, k, K, Hprev, publish, progress,
+                                                                 status, sm, &s_flag)
+                                : persistent_step<T, WMAX, false>(band, P, r, k, K, Hprev, publish, progress,
+                                                                  status, sm, &s_flag);
+            if (!ok) return;
         }
     }
 }
@@ -429,16 +580,23 @@ pass_persistent_kernel(T* __restrict__ band, PassArgs P, int* __restrict__ progr
 // Per-cycle scheduler (one launch per cycle): block b runs step
 // k = cycle - lag * r of sweep r = r_first + b.  Steps in one cycle touch
 // disjoint windows, and the launch boundary orders consecutive cycles.
+template <typename T, int WMAX, bool FULL>
+__device__ __forceinline__ void cycle_step(T* __restrict__ band, const PassArgs& P, int r, int k,
+                                           const Smem<T>& sm) {
+    right_post<T, WMAX, FULL>(band, P, r, k, sm, false);
+    left_pre<T, WMAX, FULL>(band, P, r, k, sm);
+    left_post<T, WMAX, FULL>(band, P, r, k, sm);
+}
+
 template <typename T, int WMAX>
 __global__ void __launch_bounds__(MaxThreads<T, WMAX>::value)
 pass_cycle_kernel(T* __restrict__ band, PassArgs P, int cycle, int r_first) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    const Smem<T> sm = carve_smem<T, WMAX>(smem_raw);
+    const Smem<T> sm = carve_smem<T, WMAX>(smem_raw, P.b + P.t + 1);
     const int r = r_first + blockIdx.x;
     const int k = cycle - P.lag * r;
-    right_half<T, WMAX>(band, P, r, k, sm);
-    __syncthreads();
-    left_half<T, WMAX>(band, P, r, k, sm);
+    if (step_geom(P, r, k).w == WMAX) cycle_step<T, WMAX, true>(band, P, r, k, sm);
+    else cycle_step<T, WMAX, false>(band, P, r, k, sm);
 }
 
 // Zero the fill rows 0..tw-1 and ku+1..ku+tw of every column.

@@ -1,0 +1,6 @@
+// double pass kernels for reflector lengths 32, 33 and up to 65.
+#include "bb_launch.cuh"
+
+namespace bb {
+BB_INSTANTIATE_W(double, 32) BB_INSTANTIATE_W(double, 33) BB_INSTANTIATE_W(double, 65)
+}  // namespace bb

@@ -7,18 +7,20 @@
 
 namespace bb {
 
+// Reflector lengths the kernels are compiled for: the exact t + 1 of common
+// tile widths (interior steps then run without predicates) and buckets for
+// the rest (predicated on the run-time length).
 inline int wmax_bucket(int w) {
-    if (w <= 9) return 9;
-    if (w <= 17) return 17;
-    if (w <= 33) return 33;
-    return 65;
+    for (int c : {8, 9, 16, 17, 32, 33, 65})
+        if (w <= c) return c;
+    return 0;
 }
 
 template <typename T, int WMAX>
 size_t smem_bytes(const PassArgs& P) {
     const int wp = WMAX | 1;
     const size_t ncol = (size_t)P.b + P.t + 1;
-    return sizeof(T) * ((size_t)WMAX + 2 + ncol * wp);
+    return sizeof(T) * ((size_t)WMAX + 2 + (2 * ncol - 1) * wp);
 }
 
 template <typename T, int WMAX>
@@ -38,6 +40,11 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
         if (err != cudaSuccess) return err;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         long long grid = (long long)per_sm * cfg.num_sms;
+        // Sweeps in flight at once: sweep 0 has about 2n/b half-steps and each
+        // later sweep starts lagh half-steps after its predecessor.  CTAs
+        // beyond that only spin on their first flag.
+        const long long in_flight = (2 * (P.n - P.bp)) / ((long long)P.b * P.lagh) + 2;
+        grid = std::min<long long>(grid, in_flight + in_flight / 4 + 8);
         if (cfg.max_ctas > 0) grid = std::min<long long>(grid, cfg.max_ctas);
         grid = std::min<long long>(grid, P.nsweeps);
         if (grid < 1) return cudaSuccess;
@@ -86,10 +93,11 @@ template <typename T>
 cudaError_t run_pass(T* band, const PassArgs& P, int scheduler, const LaunchCfg& cfg,
                      int* progress, int* status, cudaStream_t stream, LaunchStats* stats) {
     switch (wmax_bucket(P.t + 1)) {
-        case 9: return run_pass_w<T, 9>(band, P, scheduler, cfg, progress, status, stream, stats);
-        case 17: return run_pass_w<T, 17>(band, P, scheduler, cfg, progress, status, stream, stats);
-        case 33: return run_pass_w<T, 33>(band, P, scheduler, cfg, progress, status, stream, stats);
-        default: return run_pass_w<T, 65>(band, P, scheduler, cfg, progress, status, stream, stats);
+#define BB_CASE(W) \
+        case W: return run_pass_w<T, W>(band, P, scheduler, cfg, progress, status, stream, stats);
+        BB_CASE(8) BB_CASE(9) BB_CASE(16) BB_CASE(17) BB_CASE(32) BB_CASE(33) BB_CASE(65)
+#undef BB_CASE
+        default: return cudaErrorInvalidValue;
     }
 }
 
@@ -110,6 +118,14 @@ cudaError_t run_extract(const T* band, long long n, long long ldab, int ku, T* d
     return cudaGetLastError();
 }
 
+// Explicit instantiation: one translation unit per (type, width group) so
+// that the build compiles them in parallel.
+#define BB_INSTANTIATE_W(T, W)                                                                     \
+    template cudaError_t run_pass_w<T, W>(T*, const PassArgs&, int, const LaunchCfg&, int*, int*,  \
+                                          cudaStream_t, LaunchStats*);
+#define BB_EXTERN_W(T, W)                                                                          \
+    extern template cudaError_t run_pass_w<T, W>(T*, const PassArgs&, int, const LaunchCfg&, int*, \
+                                                 int*, cudaStream_t, LaunchStats*);
 #define BB_INSTANTIATE(T)                                                                          \
     template cudaError_t run_pass<T>(T*, const PassArgs&, int, const LaunchCfg&, int*, int*,       \
                                      cudaStream_t, LaunchStats*);                                  \

@@ -134,8 +134,9 @@ extern "C" bb_status bb_reduce_noalloc(void* band_ptr, int64_t n, int64_t bw, in
     if (ldab < bw + 2 * tw + 1) return fail(BB_ERR_LDAB, "ldab < bw + 2*tw + 1");
     {
         const size_t es = dtype == BB_F64 ? 8 : 4;
-        const int wm = tw + 1 <= 9 ? 9 : (tw + 1 <= 17 ? 17 : (tw + 1 <= 33 ? 33 : 65));
-        const size_t smem = es * ((size_t)wm + 2 + (size_t)(bw + tw + 1) * (wm | 1));
+        const int w1 = (int)tw + 1;
+        const int wm = w1 <= 8 ? 8 : w1 <= 9 ? 9 : w1 <= 16 ? 16 : w1 <= 17 ? 17 : w1 <= 32 ? 32 : w1 <= 33 ? 33 : 65;
+        const size_t smem = es * ((size_t)wm + 2 + (size_t)(2 * (bw + tw) + 1) * (wm | 1));
         if (smem > 227 * 1024) return fail(BB_ERR_INVALID_ARG, "bandwidth too large for the shared-memory tile");
     }
     if (!band_ptr || !d_out || (n > 1 && !e_out)) return fail(BB_ERR_INVALID_ARG, "null band, d or e pointer");
