@@ -22,7 +22,11 @@ BB_OK, BB_ERR_INVALID_ARG, BB_ERR_LDAB, BB_ERR_DTYPE, BB_ERR_CUDA, BB_ERR_TIMEOU
 STATUS_NAMES = {0: "BB_OK", 1: "BB_ERR_INVALID_ARG", 2: "BB_ERR_LDAB", 3: "BB_ERR_DTYPE",
                 4: "BB_ERR_CUDA", 5: "BB_ERR_TIMEOUT", 6: "BB_ERR_NOMEM"}
 (BB_PARAM_SCHEDULER, BB_PARAM_TPB, BB_PARAM_MAX_CTAS, BB_PARAM_WAIT_BUDGET_MS, BB_PARAM_PASS_LO,
- BB_PARAM_PASS_HI, BB_PARAM_STALL_SWEEP, BB_PARAM_TIMING) = range(8)
+ BB_PARAM_PASS_HI, BB_PARAM_STALL_SWEEP, BB_PARAM_TIMING, BB_PARAM_GROUP_SIZE) = range(9)
+BB_ERR_INTERNAL = 7
+STATUS_NAMES[7] = "BB_ERR_INTERNAL"
+# scheduler values
+SCHED_AUTO, SCHED_CYCLE, SCHED_FLAGS, SCHED_GROUP = 0, 1, 2, 3
 
 
 class BBError(RuntimeError):
@@ -67,6 +71,8 @@ def lib() -> ctypes.CDLL:
             "bb_last_pass_ms": ([p, i64, ctypes.POINTER(cd)], ci),
             "bb_last_error": ([], ctypes.c_char_p),
             "bb_reduce_noalloc": ([p, i64, i64, i64, i64, ci, p, p, p], ci),
+            "bb_last_pass_kernel": ([p, i64], i64),
+            "bb_last_pass_group": ([p, i64], i64),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -166,6 +172,14 @@ def bb_last_launches(h) -> int:
 
 def bb_last_num_passes(h) -> int:
     return int(lib().bb_last_num_passes(h))
+
+
+def bb_last_pass_kernel(h, i: int) -> int:
+    return int(lib().bb_last_pass_kernel(h, i))
+
+
+def bb_last_pass_group(h, i: int) -> int:
+    return int(lib().bb_last_pass_group(h, i))
 
 
 def bb_last_pass_ms(h, i: int) -> float:

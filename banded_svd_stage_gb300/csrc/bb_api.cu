@@ -79,7 +79,7 @@ struct bb_handle {
     int* d_progress = nullptr;  // n int32 per-sweep progress counters
     int* d_status = nullptr;    // device status word
     // parameters
-    int scheduler = 0, tpb = 0, max_ctas = 0, stall_sweep = -1, timing = 0;
+    int scheduler = 0, tpb = 0, max_ctas = 0, stall_sweep = -1, timing = 0, group_size = 0;
     int64_t wait_ms = 4000, pass_lo = 0, pass_hi = 1 << 30;
     // staging buffers of bb_reduce_host
     void* s_band = nullptr;
@@ -89,6 +89,7 @@ struct bb_handle {
     int64_t last_launches = 0;
     std::vector<cudaEvent_t> ev;  // 2 per pass
     int64_t last_passes = 0;
+    std::vector<int> pass_kernel, pass_group;  // per pass of the last reduction
 };
 
 extern "C" {
@@ -182,7 +183,7 @@ bb_status bb_set_param(bb_handle* h, int param, int64_t value) {
     if (!h) return fail(BB_ERR_INVALID_ARG, "bb_set_param: null handle");
     switch (param) {
         case BB_PARAM_SCHEDULER:
-            if (value != 0 && value != 1) return fail(BB_ERR_INVALID_ARG, "scheduler must be 0 or 1");
+            if (value < 0 || value > 3) return fail(BB_ERR_INVALID_ARG, "scheduler must be 0, 1, 2 or 3");
             h->scheduler = (int)value;
             return BB_OK;
         case BB_PARAM_TPB:
@@ -213,6 +214,10 @@ bb_status bb_set_param(bb_handle* h, int param, int64_t value) {
         case BB_PARAM_TIMING:
             h->timing = value ? 1 : 0;
             return BB_OK;
+        case BB_PARAM_GROUP_SIZE:
+            if (value < 0 || value > 32) return fail(BB_ERR_INVALID_ARG, "group size must be in [0, 32]");
+            h->group_size = (int)value;
+            return BB_OK;
         default:
             return fail(BB_ERR_INVALID_ARG, "unknown parameter");
     }
@@ -229,11 +234,21 @@ int64_t bb_get_param(const bb_handle* h, int param) {
         case BB_PARAM_PASS_HI: return h->pass_hi;
         case BB_PARAM_STALL_SWEEP: return h->stall_sweep;
         case BB_PARAM_TIMING: return h->timing;
+        case BB_PARAM_GROUP_SIZE: return h->group_size;
         default: return -1;
     }
 }
 
 int64_t bb_last_launches(const bb_handle* h) { return h ? h->last_launches : -1; }
+
+int64_t bb_last_pass_kernel(const bb_handle* h, int64_t i) {
+    if (!h || i < 0 || i >= (int64_t)h->pass_kernel.size()) return -1;
+    return h->pass_kernel[i];
+}
+int64_t bb_last_pass_group(const bb_handle* h, int64_t i) {
+    if (!h || i < 0 || i >= (int64_t)h->pass_group.size()) return -1;
+    return h->pass_group[i];
+}
 int64_t bb_last_num_passes(const bb_handle* h) { return h ? h->last_passes : -1; }
 
 bb_status bb_last_pass_ms(bb_handle* h, int64_t i, double* ms) {
@@ -259,7 +274,8 @@ bb_status bb_status_sync(bb_handle* h, bb_stream_t stream) {
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_fail(e, "bb_status_sync: clearing status");
         return fail((bb_status)st, st == BB_ERR_TIMEOUT ? "device-side progress wait timed out"
-                                                        : "device reported an error");
+                                   : st == BB_ERR_INTERNAL ? "device-side consistency check failed"
+                                                           : "device reported an error");
     }
     return BB_OK;
 }
@@ -293,6 +309,8 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
     cudaError_t err;
     h->last_launches = 0;
     h->last_passes = 0;
+    h->pass_kernel.clear();
+    h->pass_group.clear();
     auto plan = plan_passes(h->bw, tw);
     const int64_t lo = std::max<int64_t>(0, h->pass_lo);
     const int64_t hi = std::min<int64_t>((int64_t)plan.size(), h->pass_hi);
@@ -328,6 +346,7 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         cfg.tpb = h->tpb ? h->tpb : bb::auto_tpb(b, t);
         cfg.max_ctas = h->max_ctas;
         cfg.num_sms = h->num_sms;
+        cfg.group_size = h->group_size;
         bb::LaunchStats st;
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo)], s);
         err = bb::run_pass<T>(band, P, h->scheduler, cfg, h->d_progress, h->d_status, s, &st);
@@ -335,6 +354,8 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         h->last_launches += st.launches;
         if (err != cudaSuccess) return cuda_fail(err, "pass launch");
         h->last_passes += 1;
+        h->pass_kernel.push_back(st.kernel);
+        h->pass_group.push_back(st.group);
     }
     err = bb::run_extract<T>(band, n, ldab, ku, d, e, s);
     if (err != cudaSuccess) return cuda_fail(err, "extract launch");
@@ -397,6 +418,69 @@ bb_status bb_reduce_host(bb_handle* h, const void* band_host, int64_t ldab, int6
 }  // extern "C"
 
 namespace bb {
+
+int group_footprint(const PassArgs& P, int g) {
+    // Replays the group kernel's buffer bookkeeping for the group at sweep 0.
+    const int ng = (int)std::min<long long>(g, P.nsweeps);
+    if (ng <= 0) return 0;
+    const int L = P.lagh;
+    auto steps = [&](long long r) -> long long {
+        long long last = P.n - 2 - r - P.bp;
+        return last < 0 ? 0 : last / P.b + 1;
+    };
+    auto maxcol = [&](long long r, long long h) -> long long {
+        const long long k = h >> 1;
+        const long long c = r + P.bp + k * P.b;
+        const long long ce = std::min(c + P.t, P.n - 1);
+        return (h & 1) ? std::min(ce + P.b, P.n - 1) : ce;
+    };
+    auto mincol = [&](long long r, long long h) -> long long { return r + P.bp + (h >> 1) * P.b; };
+    long long tend = 0;
+    for (int jj = 0; jj < ng; ++jj) tend = std::max(tend, (long long)L * jj + 2 * steps(jj));
+    long long A = P.bp, B = A - 1, fp = 0;
+    for (long long tau = 0; tau < tend; ++tau) {
+        long long xneed = -1;
+        for (int jj = 0; jj < ng; ++jj) {
+            const long long h = tau - (long long)L * jj;
+            if (h >= 0 && h < 2 * steps(jj)) xneed = std::max(xneed, maxcol(jj, h));
+        }
+        if (xneed > B) {
+            fp = std::max(fp, xneed - A + 1);
+            B = xneed;
+        }
+        long long anew = B + 1;
+        for (int jj = 0; jj < ng; ++jj) {
+            const long long h = tau + 1 - (long long)L * jj;
+            if (h < 2 * steps(jj)) anew = std::min(anew, mincol(jj, std::max(h, 0LL)));
+        }
+        if (tau == tend - 1) anew = B + 1;
+        if (anew > A) A = anew;
+    }
+    return (int)fp;
+}
+
+bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out) {
+    const size_t budget = 220 * 1024;
+    const int ld = P.b + 2 * P.t + 1;
+    GroupArgs best{};
+    const int gcap = group_max_warps(wmax, elem);
+    const int gmax = requested > 0 ? std::min(requested, gcap) : gcap;
+    for (int g = 1; g <= gmax; ++g) {
+        GroupArgs ga;
+        ga.g = g;
+        ga.ngroups = (int)((P.nsweeps + g - 1) / g);
+        ga.lds = ld + (ld & 1);  // even: conflict-free column-block access
+        ga.nslot = std::max(1, group_footprint(P, g));
+        if (group_smem_bytes(ga, wmax, elem) > budget) break;
+        best = ga;
+        if (requested > 0 && g == requested) break;
+    }
+    if (best.g == 0) return false;
+    if (requested > 0 && best.g != requested) return false;
+    *out = best;
+    return true;
+}
+
 int auto_tpb(int b, int t) {
     int rows = b + t;
     int tpb = ((rows + 31) / 32) * 32;

@@ -25,7 +25,7 @@
 
 namespace bb {
 
-enum : int { kStatusOk = 0, kStatusTimeout = 5 };
+enum : int { kStatusOk = 0, kStatusTimeout = 5, kStatusInternal = 7 };
 
 struct PassArgs {
     long long n;          // matrix order
@@ -519,6 +519,11 @@ __device__ __forceinline__ void block_publish(int* flag, int value) {
         __threadfence();
         st_release_gpu(flag, value);
     }
+}
+
+__device__ __forceinline__ void block_publish_if(int* flag, int value, bool publish) {
+    if (publish) block_publish(flag, value);
+    else __syncthreads();
 }
 
 // Persistent scheduler: CTAs take sweeps r = blockIdx.x, blockIdx.x + grid,

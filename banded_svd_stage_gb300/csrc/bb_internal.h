@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "bb_device.cuh"
+#include "bb_group.cuh"
 
 namespace bb {
 
@@ -13,15 +14,36 @@ namespace bb {
 constexpr int kMaxW = 65;
 
 struct LaunchCfg {
-    int tpb;       // threads per block
-    int max_ctas;  // cap on the persistent grid (0: co-resident maximum)
-    int num_sms;
+    int tpb = 0;         // threads per block (flag and per-cycle kernels)
+    int max_ctas = 0;    // cap on the persistent grid (0: co-resident maximum)
+    int num_sms = 0;
+    int group_size = 0;  // requested sweeps per group (0: largest that fits, <= 16)
+    GroupArgs group{};   // filled by plan_group
 };
 
 struct LaunchStats {
     int64_t launches = 0;  // kernel launches issued
     int grid = 0;          // persistent grid of the last pass
+    int kernel = 0;        // 1 per-cycle, 2 flag kernel, 3 group kernel
+    int group = 0;         // sweeps per group (group kernel)
 };
+
+// Shared memory of the group kernel: per-sweep reflectors and scalars, then
+// the circular column buffer.
+inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem) {
+    return elem * ((size_t)GA.g * wmax + (size_t)((GA.g + 1) & ~1) + (size_t)GA.nslot * GA.lds);
+}
+
+// Largest group (<= requested, or <= 16 when requested == 0) whose column
+// buffer fits in shared memory; false if not even one sweep fits.
+bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out);
+
+// Largest group size the group kernel is compiled for (see GroupMaxWarps).
+inline int group_max_warps(int wmax, size_t elem) { return (wmax * (int)elem <= 17 * 4) ? 16 : 8; }
+
+// Columns the group starting at sweep 0 holds at most (the buffer size the
+// group kernel needs; groups further down the matrix hold no more).
+int group_footprint(const PassArgs& P, int g);
 
 // One pass of the reduction on `stream`.  scheduler 0: persistent kernel
 // (cooperative launch); 1: one launch per cycle.

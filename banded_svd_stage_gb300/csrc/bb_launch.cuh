@@ -3,6 +3,7 @@
 
 #include <algorithm>
 
+#include "bb_group.cuh"
 #include "bb_internal.h"
 
 namespace bb {
@@ -29,7 +30,41 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
     const size_t smem = smem_bytes<T, WMAX>(P);
     const int tpb = std::min(cfg.tpb, MaxThreads<T, WMAX>::value);
     cudaError_t err;
-    if (scheduler == 0) {
+    if (scheduler == 3) {
+        if (P.nsweeps <= 0) return cudaSuccess;
+        GroupArgs GA = cfg.group;
+        auto kern = pass_group_kernel<T, WMAX>;
+        const size_t gsmem = group_smem_bytes(GA, WMAX, sizeof(T));
+        if (gsmem > 48 * 1024) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
+            if (err != cudaSuccess) return err;
+        }
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * GA.g, gsmem);
+        if (err != cudaSuccess) return err;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        long long grid = std::min<long long>((long long)per_sm * cfg.num_sms, GA.ngroups);
+        if (cfg.max_ctas > 0) grid = std::min<long long>(grid, cfg.max_ctas);
+        err = cudaMemsetAsync(progress, 0, sizeof(int) * (size_t)GA.ngroups, stream);
+        if (err != cudaSuccess) return err;
+        T* band_arg = band;
+        PassArgs p_arg = P;
+        GroupArgs g_arg = GA;
+        int* prog_arg = progress;
+        int* stat_arg = status;
+        void* args[] = {&band_arg, &p_arg, &g_arg, &prog_arg, &stat_arg};
+        err = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * GA.g), args,
+                                          gsmem, stream);
+        if (stats) {
+            stats->launches += 1;
+            stats->grid = (int)grid;
+            stats->kernel = 3;
+            stats->group = GA.g;
+        }
+        return err;
+    }
+    if (stats) stats->kernel = (scheduler == 1) ? 1 : 2;
+    if (scheduler != 1) {
         auto kern = pass_persistent_kernel<T, WMAX>;
         if (smem > 48 * 1024) {
             err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -90,9 +125,22 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
 }
 
 template <typename T>
-cudaError_t run_pass(T* band, const PassArgs& P, int scheduler, const LaunchCfg& cfg,
+cudaError_t run_pass(T* band, const PassArgs& P, int scheduler, const LaunchCfg& cfg_in,
                      int* progress, int* status, cudaStream_t stream, LaunchStats* stats) {
-    switch (wmax_bucket(P.t + 1)) {
+    LaunchCfg cfg = cfg_in;
+    const int wmax = wmax_bucket(P.t + 1);
+    if (scheduler == 0) {
+        // automatic: the flag kernel, which measures faster than the group
+        // kernel on every workload so far (per-tick column hand-over and
+        // bookkeeping of the group kernel still cost more than the flag
+        // hand-offs they replace)
+        scheduler = 2;
+    } else if (scheduler == 3) {
+        // group kernel where one group's columns fit shared memory
+        const bool ok = plan_group(P, wmax, sizeof(T), cfg.group_size, &cfg.group);
+        scheduler = ok ? 3 : 2;
+    }
+    switch (wmax) {
 #define BB_CASE(W) \
         case W: return run_pass_w<T, W>(band, P, scheduler, cfg, progress, status, stream, stats);
         BB_CASE(8) BB_CASE(9) BB_CASE(16) BB_CASE(17) BB_CASE(32) BB_CASE(33) BB_CASE(65)

@@ -174,6 +174,7 @@ def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int,
         pass_ms.append(red.pass_ms())
     red.check(stream)
     ms = [a.elapsed_time(b) for a, b in events]
+    kernels = red.pass_kernels()
     # dominant kernel: the pass kernel, one launch per pass (persistent scheduler)
     per_pass_ms = np.array(pass_ms)  # steps x passes
     e2e = None
@@ -183,7 +184,7 @@ def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int,
     return {
         "ms": ms, "model_bytes": model_bytes, "pass_bytes": pass_bytes,
         "pass_ms_mean": per_pass_ms.mean(axis=0).tolist(), "launches": launches,
-        "e2e": e2e, "band_bytes": band_np.nbytes, "esz": esz,
+        "e2e": e2e, "band_bytes": band_np.nbytes, "esz": esz, "kernels": kernels,
     }
 
 
@@ -369,7 +370,7 @@ def main():
             g2 = r2["model_bytes"] / (m2 * 1e-3) / 1e9
             sweep.append({"workload": name, "ms_per_reduction": m2, "min_ms": min(r2["ms"]),
                           "effective_gbs": g2, "frac_of_hbm": g2 / hbm,
-                          "pass_ms": r2["pass_ms_mean"]})
+                          "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"]})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -390,6 +391,7 @@ def main():
             "gpu_launches": res["launches"] * world,
             "clocks": clocks,
             "wall_s": wall,
+            "pass_kernels": res["kernels"],
             "per_workload": sweep,
         }
         print(json.dumps(line))

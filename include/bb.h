@@ -51,7 +51,8 @@ typedef enum {
     BB_ERR_DTYPE = 3,       /* dtype unknown                                     */
     BB_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed       */
     BB_ERR_TIMEOUT = 5,     /* a device-side wait gave up (latched on the device) */
-    BB_ERR_NOMEM = 6        /* a device or host allocation failed                */
+    BB_ERR_NOMEM = 6,       /* a device or host allocation failed                */
+    BB_ERR_INTERNAL = 7     /* a device-side consistency check failed (a bug)    */
 } bb_status;
 
 /* A cudaStream_t, passed as a plain pointer (NULL = the legacy default stream). */
@@ -99,8 +100,13 @@ bb_status bb_status_sync(bb_handle* h, bb_stream_t stream);
 
 /* Tuning and test parameters (bb_set_param / bb_get_param). */
 enum {
-    BB_PARAM_SCHEDULER = 0,     /* 0: persistent kernel with progress flags (default);
-                                   1: one kernel launch per cycle                       */
+    BB_PARAM_SCHEDULER = 0,     /* 0: automatic (default): currently the flag kernel
+                                      for every pass (fastest measured);
+                                   1: one kernel launch per cycle;
+                                   2: persistent flag kernel (one CTA per sweep, per-
+                                      sweep progress counters) for every pass;
+                                   3: group kernel (CTA per group of sweeps, columns in
+                                      shared memory) wherever one sweep fits, else 2  */
     BB_PARAM_TPB = 1,           /* threads per block, multiple of 32 in [32, 1024];
                                    0 = automatic (default)                              */
     BB_PARAM_MAX_CTAS = 2,      /* cap on the persistent grid; 0 = co-resident maximum  */
@@ -109,8 +115,10 @@ enum {
     BB_PARAM_PASS_HI = 5,       /*   the fill rows are zeroed only when PASS_LO == 0    */
     BB_PARAM_STALL_SWEEP = 6,   /* fault injection: the CTA running this sweep of every
                                    pass never reports progress (-1 = off, default)      */
-    BB_PARAM_TIMING = 7         /* 1: record CUDA events around every pass launch, read
+    BB_PARAM_TIMING = 7,        /* 1: record CUDA events around every pass launch, read
                                    back with bb_last_pass_ms (default 0)                */
+    BB_PARAM_GROUP_SIZE = 8     /* sweeps per group of the group kernel: 0 = largest
+                                   that fits shared memory, at most 16 (default)        */
 };
 bb_status bb_set_param(bb_handle* h, int param, int64_t value);
 int64_t bb_get_param(const bb_handle* h, int param);
@@ -133,6 +141,12 @@ int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass);
 /* Kernel launches made by the last bb_reduce / bb_reduce_host on this handle
  * (fill-row zeroing, the passes, and the d/e extraction). */
 int64_t bb_last_launches(const bb_handle* h);
+
+/* Kernel that ran pass i of the last reduction: 1 per-cycle, 2 flag kernel,
+ * 3 group kernel (-1 if out of range), and, for the group kernel, its group
+ * size (sweeps per CTA; 0 otherwise). */
+int64_t bb_last_pass_kernel(const bb_handle* h, int64_t i);
+int64_t bb_last_pass_group(const bb_handle* h, int64_t i);
 
 /* With BB_PARAM_TIMING on: after the stream of the last bb_reduce has been
  * synchronized, the number of passes it ran and the device time of pass i in

@@ -17,7 +17,8 @@ from gpu_helpers import TOL, fro_of_band, sigma_bidiagonal
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_sweep_times_out_and_context_survives():
+@pytest.mark.parametrize("sched", [0, 2, 3])
+def test_stalled_sweep_times_out_and_context_survives(sched):
     n, bw, tw = 2000, 32, 8
     band = bi.make_band(n, bw, tw, "f32", "normal", seed=1)
     dev = torch.device("cuda:0")
@@ -26,6 +27,7 @@ def test_stalled_sweep_times_out_and_context_survives():
     e = torch.empty(n - 1, dtype=torch.float32, device=dev)
     h = bb.bb_create(n, bw, bb.BB_F32)
     try:
+        bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, sched)
         bb.bb_set_param(h, bb.BB_PARAM_WAIT_BUDGET_MS, 50)
         bb.bb_set_param(h, bb.BB_PARAM_STALL_SWEEP, 5)
         s = torch.cuda.current_stream(dev)

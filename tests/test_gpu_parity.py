@@ -52,7 +52,10 @@ def assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler=0):
     return err
 
 
-@pytest.mark.parametrize("scheduler", [0, 1])
+SCHEDULERS = [bb.SCHED_AUTO, bb.SCHED_CYCLE, bb.SCHED_FLAGS, bb.SCHED_GROUP]
+
+
+@pytest.mark.parametrize("scheduler", SCHEDULERS)
 @pytest.mark.parametrize("dt", ["f64", "f32"])
 @pytest.mark.parametrize("n,bw,tw", EDGE_CASES)
 def test_edge_cases(n, bw, tw, dt, scheduler):
@@ -60,21 +63,30 @@ def test_edge_cases(n, bw, tw, dt, scheduler):
     check_against_oracle(band, n, bw, tw, dt, scheduler)
 
 
-@pytest.mark.parametrize("scheduler", [0, 1])
+@pytest.mark.parametrize("scheduler", SCHEDULERS)
 def test_workload_n256_full(scheduler):
     w = bi.WORKLOADS[0]
     check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler)
 
 
-@pytest.mark.parametrize("scheduler", [0, 1])
+@pytest.mark.parametrize("scheduler", SCHEDULERS)
 def test_workload_n4096_full(scheduler):
     w = bi.WORKLOADS[1]
     check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler)
 
 
-def test_workload_n8192_full():
+@pytest.mark.parametrize("scheduler", [bb.SCHED_AUTO, bb.SCHED_FLAGS])
+def test_workload_n8192_full(scheduler):
     w = bi.WORKLOADS[2]
-    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, 0)
+    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler)
+
+
+@pytest.mark.parametrize("g", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("n,bw,tw,dt", [(700, 40, 12, "f64"), (1001, 16, 15, "f32"), (613, 9, 2, "f64"),
+                                        (900, 64, 32, "f32")])
+def test_group_sizes(n, bw, tw, dt, g):
+    band = bi.make_band(n, bw, tw, dt, "normal", seed=n + g)
+    check_against_oracle(band, n, bw, tw, dt, bb.SCHED_GROUP, {bb.BB_PARAM_GROUP_SIZE: g})
 
 
 @pytest.mark.parametrize("idx", [3, 4])
@@ -133,24 +145,26 @@ def test_full_size_properties(idx):
     assert abs(m4b - m4) <= tol4 * m4
 
 
-@pytest.mark.parametrize("idx", [2, 3])
+@pytest.mark.parametrize("idx", [2, 3, 4])
 def test_full_size_schedulers_agree_bitwise(idx):
-    """The per-cycle and the persistent schedulers run the same half-steps
-    with the same arithmetic in different interleavings; any race would make
-    them differ."""
+    """The per-cycle, flag and group schedulers run the same half-steps with
+    the same arithmetic in different interleavings and on different copies
+    (memory or shared memory); any race would make them differ."""
     w = bi.WORKLOADS[idx]
     band = bi.make_workload(w)
-    d0, e0 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0)
-    d1, e1 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 1)
-    assert np.array_equal(d0, d1) and np.array_equal(e0, e1)
+    ref = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, bb.SCHED_FLAGS)
+    for sched in (bb.SCHED_AUTO, bb.SCHED_GROUP) + ((bb.SCHED_CYCLE,) if idx < 4 else ()):
+        d1, e1 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, sched)
+        assert np.array_equal(ref[0], d1) and np.array_equal(ref[1], e1), sched
 
 
-def test_persistent_deterministic_and_grid_independent():
+@pytest.mark.parametrize("sched", [bb.SCHED_FLAGS, bb.SCHED_GROUP])
+def test_persistent_deterministic_and_grid_independent(sched):
     w = bi.WORKLOADS[2]
     band = bi.make_workload(w)
-    d0, e0 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0)
-    d1, e1 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0, {bb.BB_PARAM_MAX_CTAS: 7})
-    d2, e2 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, 0, {bb.BB_PARAM_TPB: 256})
+    d0, e0 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, sched)
+    d1, e1 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, sched, {bb.BB_PARAM_MAX_CTAS: 7})
+    d2, e2 = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, sched, {bb.BB_PARAM_TPB: 256})
     assert np.array_equal(d0, d1) and np.array_equal(e0, e1)
     assert np.array_equal(d0, d2) and np.array_equal(e0, e2)
 
