@@ -257,8 +257,10 @@ __device__ __forceinline__ void copy_rows(const T* __restrict__ base, long long 
         const T* src = base + (g.p + 1 + i) + g.c * stride;
         T* dst = sm.rtile + i * sm.wp;
 #pragma unroll
-        for (int m = 0; m < WMAX; ++m)
-            if (m < W) cp_async_elem<T>(dst + m, src + m * stride);
+        for (int m = 0; m < WMAX; ++m) {
+            if (m < W) cp_async_elem<T>(dst + m, src);
+            src += stride;
+        }
     }
 }
 
@@ -346,8 +348,10 @@ __device__ __forceinline__ void right_post(T* __restrict__ band, const PassArgs&
         if (rr < 0) {
             T* dst = base + (g.p + 1 + i) + g.c * stride;
 #pragma unroll
-            for (int m = 0; m < WMAX; ++m)
-                if (m < W) dst[m * stride] = x[m];
+            for (int m = 0; m < WMAX; ++m) {
+                if (m < W) *dst = x[m];
+                dst += stride;
+            }
         } else {
 #pragma unroll
             for (int m = 0; m < WMAX; ++m)
@@ -366,21 +370,28 @@ __device__ __forceinline__ void right_post(T* __restrict__ band, const PassArgs&
 // ---------------------------------------------------------------------------
 
 // Copy columns [j0, j1) (local indices) of rows c..ce of the left block from
-// memory into the tile; element e -> (column j0 + e / w, row e % w), so that
-// consecutive threads read consecutive addresses.
+// memory into the tile.  Thread t takes row m = t % w of columns
+// j0 + t / w, + nct / w, ... (consecutive threads read consecutive
+// addresses of a column), walking its column pointer by a fixed increment.
 template <typename T, int WMAX, bool FULL>
 __device__ __forceinline__ void copy_columns(const T* __restrict__ base, long long stride, const StepGeom& g,
                                              int j0, int j1, const Smem<T>& sm) {
     const int w = FULL ? WMAX : g.w;
     if (j1 <= j0) return;
-    const int total = (j1 - j0) * w;
-    // e / w == umulhi(e, magic) for e < 2^16 and w >= 2 (a step has w >= 2)
-    const unsigned magic = 0xffffffffu / (unsigned)w + 1u;
-    const T* src0 = base + g.c + (g.c + j0) * stride;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-        const int jl = (int)__umulhi((unsigned)e, magic);
-        const int m = e - jl * w;
-        cp_async_elem<T>(sm.tile + (j0 + jl) * sm.wp + m, src0 + m + (long long)jl * stride);
+    const int nthr = blockDim.x;
+    const int per = nthr / w;  // columns per round
+    const int t = threadIdx.x;
+    if (t >= per * w) return;
+    const int m = t % w;
+    int jl = j0 + t / w;
+    const T* src = base + (g.c + m) + (g.c + jl) * stride;
+    T* dst = sm.tile + jl * sm.wp + m;
+    const long long sstep = (long long)per * stride;
+    const int dstep = per * sm.wp;
+    for (; jl < j1; jl += per) {
+        cp_async_elem<T>(dst, src);
+        src += sstep;
+        dst += dstep;
     }
 }
 
@@ -448,16 +459,21 @@ __device__ __forceinline__ void left_post(T* __restrict__ band, const PassArgs& 
         }
     }
     __syncthreads();
-    // Write the whole block back (columns c .. cend, rows c .. ce), element
-    // e -> (column e / w, row e % w), so that consecutive threads write
-    // consecutive addresses across column boundaries.
-    const int total = ncol * w;
-    const unsigned magic = 0xffffffffu / (unsigned)w + 1u;
-    T* dst0 = base + c + c * stride;
-    for (int e = tid; e < total; e += nthr) {
-        const int jl = (int)__umulhi((unsigned)e, magic);
-        const int m = e - jl * w;
-        dst0[m + (long long)jl * stride] = sm.tile[jl * wp + m];
+    // Write the whole block back (columns c .. cend, rows c .. ce); thread t
+    // takes row t % w of columns t / w, + nthr / w, ...
+    const int per = nthr / w;
+    if (tid < per * w) {
+        const int m = tid % w;
+        int jl = tid / w;
+        T* dst = base + (c + m) + (c + jl) * stride;
+        const T* src = sm.tile + jl * wp + m;
+        const long long gstep = (long long)per * stride;
+        const int sstep = per * wp;
+        for (; jl < ncol; jl += per) {
+            *dst = *src;
+            dst += gstep;
+            src += sstep;
+        }
     }
 }
 
@@ -566,7 +582,10 @@ pass_persistent_kernel(T* __restrict__ band, PassArgs P, int* __restrict__ progr
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_flag;
     const Smem<T> sm = carve_smem<T, WMAX>(smem_raw, P.b + P.t + 1);
-    if (ld_relaxed_gpu(status) != kStatusOk) return;
+    // one read of the status word for the whole CTA, so that all threads agree
+    if (threadIdx.x == 0) s_flag = ld_relaxed_gpu(status);
+    __syncthreads();
+    if (s_flag != kStatusOk) return;
     for (int r = blockIdx.x; r < P.nsweeps; r += gridDim.x) {
         const int K = sweep_steps(P, r);
         const int Hprev = (r > 0) ? 2 * sweep_steps(P, r - 1) : 0;

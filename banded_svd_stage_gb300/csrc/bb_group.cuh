@@ -214,7 +214,10 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     const int warp = threadIdx.x >> 5;
     const int L = P.lagh;
     __shared__ int s_nsteps[32];  // steps of each sweep of the group
-    if (ld_relaxed_gpu(status) != kStatusOk) return;
+    // one read of the status word for the whole CTA, so that all threads agree
+    if (threadIdx.x == 0) s_flag = ld_relaxed_gpu(status);
+    __syncthreads();
+    if (s_flag != kStatusOk) return;
     for (int G = blockIdx.x; G < GA.ngroups; G += gridDim.x) {
         const int r0 = G * GA.g;
         const int ng = min(GA.g, P.nsweeps - r0);

@@ -292,6 +292,7 @@ def main():
     ap.add_argument("--scheduler", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (e2e) leg")
     args = ap.parse_args()
     rank, world, local = dist_env()
     w = bi.by_name(args.workload)
@@ -339,7 +340,7 @@ def main():
     if sampler:
         sampler.start()
     t_wall0 = time.perf_counter()
-    res = run_ours(w, args.steps, args.warmup, args.scheduler, rank, with_e2e=(world == 1))
+    res = run_ours(w, args.steps, args.warmup, args.scheduler, rank, with_e2e=(world == 1 and not args.no_e2e))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
