@@ -419,8 +419,12 @@ bb_status bb_reduce_host(bb_handle* h, const void* band_host, int64_t ldab, int6
 
 namespace bb {
 
-int group_footprint(const PassArgs& P, int g) {
-    // Replays the group kernel's buffer bookkeeping for the group at sweep 0.
+int group_footprint(const PassArgs& P, int g, int ahead) {
+    // Replays the group kernel's buffer bookkeeping for the group at sweep 0:
+    // the loader copies in tick u's columns once the storer has written back
+    // what ticks < u - ahead alone touch, so the buffer holds the columns from
+    // the first one a tick >= tau touches up to the last one ticks
+    // <= tau + ahead touch.
     const int ng = (int)std::min<long long>(g, P.nsweeps);
     if (ng <= 0) return 0;
     const int L = P.lagh;
@@ -437,24 +441,23 @@ int group_footprint(const PassArgs& P, int g) {
     auto mincol = [&](long long r, long long h) -> long long { return r + P.bp + (h >> 1) * P.b; };
     long long tend = 0;
     for (int jj = 0; jj < ng; ++jj) tend = std::max(tend, (long long)L * jj + 2 * steps(jj));
-    long long A = P.bp, B = A - 1, fp = 0;
+    std::vector<long long> xrun(tend), amin(tend);
+    long long x = -1;
     for (long long tau = 0; tau < tend; ++tau) {
-        long long xneed = -1;
+        long long a = P.n;
         for (int jj = 0; jj < ng; ++jj) {
             const long long h = tau - (long long)L * jj;
-            if (h >= 0 && h < 2 * steps(jj)) xneed = std::max(xneed, maxcol(jj, h));
+            if (h >= 0 && h < 2 * steps(jj)) x = std::max(x, maxcol(jj, h));
+            if (h < 2 * steps(jj)) a = std::min(a, mincol(jj, std::max(h, 0LL)));
         }
-        if (xneed > B) {
-            fp = std::max(fp, xneed - A + 1);
-            B = xneed;
-        }
-        long long anew = B + 1;
-        for (int jj = 0; jj < ng; ++jj) {
-            const long long h = tau + 1 - (long long)L * jj;
-            if (h < 2 * steps(jj)) anew = std::min(anew, mincol(jj, std::max(h, 0LL)));
-        }
-        if (tau == tend - 1) anew = B + 1;
-        if (anew > A) A = anew;
+        xrun[tau] = x;
+        amin[tau] = a;
+    }
+    long long fp = 0, amax = -1;
+    for (long long tau = 0; tau < tend; ++tau) {
+        amax = std::max(amax, amin[tau]);  // the kernel's A never moves back
+        const long long u = std::min(tau + ahead, tend - 1);
+        fp = std::max(fp, xrun[u] - amax + 1);
     }
     return (int)fp;
 }
@@ -470,7 +473,8 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
         ga.g = g;
         ga.ngroups = (int)((P.nsweeps + g - 1) / g);
         ga.lds = ld + (ld & 1);  // even: conflict-free column-block access
-        ga.nslot = std::max(1, group_footprint(P, g));
+        ga.ahead = kGroupAhead;
+        ga.nslot = std::max(1, group_footprint(P, g, ga.ahead));
         if (group_smem_bytes(ga, wmax, elem) > budget) break;
         best = ga;
         if (requested > 0 && g == requested) break;

@@ -38,12 +38,17 @@ inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem) {
 // buffer fits in shared memory; false if not even one sweep fits.
 bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out);
 
-// Largest group size the group kernel is compiled for (see GroupMaxWarps).
-inline int group_max_warps(int wmax, size_t elem) { return (wmax * (int)elem <= 17 * 4) ? 16 : 8; }
+// Largest group size the group kernel is compiled for (GroupMaxWarps, minus
+// the loader and the storer warps).
+inline int group_max_warps(int wmax, size_t elem) { return ((wmax * (int)elem <= 17 * 4) ? 16 : 8) - 2; }
 
-// Columns the group starting at sweep 0 holds at most (the buffer size the
-// group kernel needs; groups further down the matrix hold no more).
-int group_footprint(const PassArgs& P, int g);
+// Ticks the group kernel's loader runs ahead of its storer.
+constexpr int kGroupAhead = 3;
+
+// Columns the group starting at sweep 0 holds at most when its loader runs
+// `ahead` ticks ahead (the buffer size the group kernel needs; groups further
+// down the matrix hold no more).
+int group_footprint(const PassArgs& P, int g, int ahead);
 
 // One pass of the reduction on `stream`.  scheduler 0: persistent kernel
 // (cooperative launch); 1: one launch per cycle.

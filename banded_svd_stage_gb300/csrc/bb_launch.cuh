@@ -35,12 +35,11 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
         GroupArgs GA = cfg.group;
         auto kern = pass_group_kernel<T, WMAX>;
         const size_t gsmem = group_smem_bytes(GA, WMAX, sizeof(T));
-        if (gsmem > 48 * 1024) {
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
-            if (err != cudaSuccess) return err;
-        }
+        // always raise the dynamic limit: static shared memory counts against 48 KB too
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
+        if (err != cudaSuccess) return err;
         int per_sm = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * GA.g, gsmem);
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 2), gsmem);
         if (err != cudaSuccess) return err;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         long long grid = std::min<long long>((long long)per_sm * cfg.num_sms, GA.ngroups);
@@ -53,7 +52,7 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
         int* prog_arg = progress;
         int* stat_arg = status;
         void* args[] = {&band_arg, &p_arg, &g_arg, &prog_arg, &stat_arg};
-        err = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * GA.g), args,
+        err = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 2)), args,
                                           gsmem, stream);
         if (stats) {
             stats->launches += 1;
@@ -66,10 +65,8 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
     if (stats) stats->kernel = (scheduler == 1) ? 1 : 2;
     if (scheduler != 1) {
         auto kern = pass_persistent_kernel<T, WMAX>;
-        if (smem > 48 * 1024) {
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (err != cudaSuccess) return err;
-        }
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
         int per_sm = 0;
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, tpb, smem);
         if (err != cudaSuccess) return err;
@@ -100,10 +97,8 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
     }
     // Per-cycle scheduler.
     auto kern = pass_cycle_kernel<T, WMAX>;
-    if (smem > 48 * 1024) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-    }
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
     const long long S = P.nsweeps;
     if (S <= 0) return cudaSuccess;
     auto steps = [&](long long r) -> long long {

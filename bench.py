@@ -61,6 +61,11 @@ def dist_env():
     return rank, world, local
 
 
+def replica_seed(w: bi.Workload, rank: int) -> int:
+    """Seed of rank `rank`'s band: every replica reduces a different matrix."""
+    return w.seed + 1000 * rank
+
+
 def aggregate(values_per_rank_ms: float, units: float, group=None):
     """Max over ranks of the time and sum over ranks of the units."""
     import torch
@@ -136,7 +141,7 @@ def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int,
     dev = torch.device("cuda", torch.cuda.current_device())
     tdt = torch.float32 if w.dtype == "f32" else torch.float64
     esz = 4 if w.dtype == "f32" else 8
-    band_np = bi.make_band(w.n, w.bw, w.tw, w.dtype, w.dist, w.graded, w.seed + 1000 * rank)
+    band_np = bi.make_band(w.n, w.bw, w.tw, w.dtype, w.dist, w.graded, replica_seed(w, rank))
     pristine = torch.from_numpy(band_np).to(dev)
     work = torch.empty_like(pristine)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -393,6 +398,7 @@ def main():
             "clocks": clocks,
             "wall_s": wall,
             "pass_kernels": res["kernels"],
+            "pass_ms": res["pass_ms_mean"],
             "per_workload": sweep,
         }
         print(json.dumps(line))
