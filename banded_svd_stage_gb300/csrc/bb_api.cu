@@ -85,6 +85,10 @@ struct bb_handle {
     void* s_band = nullptr;
     size_t s_band_bytes = 0;
     void* s_de = nullptr;
+    // working copy of the band with a 16-byte aligned column stride (group
+    // kernel on a caller layout its bulk copies cannot address)
+    void* work = nullptr;
+    size_t work_bytes = 0;
     // statistics of the last reduction
     int64_t last_launches = 0;
     std::vector<cudaEvent_t> ev;  // 2 per pass
@@ -175,6 +179,7 @@ void bb_destroy(bb_handle* h) {
     if (h->d_status) cudaFree(h->d_status);
     if (h->s_band) cudaFree(h->s_band);
     if (h->s_de) cudaFree(h->s_de);
+    if (h->work) cudaFree(h->work);
     for (auto ev : h->ev) cudaEventDestroy(ev);
     delete h;
 }
@@ -314,8 +319,49 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
     auto plan = plan_passes(h->bw, tw);
     const int64_t lo = std::max<int64_t>(0, h->pass_lo);
     const int64_t hi = std::min<int64_t>((int64_t)plan.size(), h->pass_hi);
+    auto pass_args = [&](int64_t pi, int64_t ld) {
+        const int b = plan[pi].b, t = plan[pi].t;
+        bb::PassArgs P;
+        P.n = n;
+        P.ldab = ld;
+        P.b = b;
+        P.t = t;
+        P.bp = b - t;
+        P.ku = ku;
+        P.nsweeps = (int)std::max<int64_t>(0, n - (b - t) - 1);
+        P.lag = pass_lag_cycle(b, t);
+        P.lagh = pass_lag_half(b, t);
+        P.stall_sweep = h->stall_sweep;
+        P.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+        return P;
+    };
+    // The group kernel moves whole columns with bulk copies, which need a
+    // 16-byte aligned column stride: on any other layout the reduction runs
+    // on an aligned working copy (one strided copy in, one out).
+    T* wb = band;
+    int64_t ldw = ldab;
+    bool any_group = false;
+    for (int64_t pi = lo; pi < hi; ++pi)
+        any_group = any_group || bb::choose_group(pass_args(pi, ldab), h->scheduler, h->group_size, sizeof(T), nullptr);
+    if (any_group && !bb::group_layout_ok(band, ldab, sizeof(T))) {
+        const int64_t q = 16 / (int64_t)sizeof(T);
+        ldw = (ldab + q - 1) / q * q;
+        const size_t bytes = sizeof(T) * (size_t)ldw * (size_t)n;
+        if (h->work_bytes < bytes) {
+            if (h->work) cudaFree(h->work);
+            h->work = nullptr;
+            h->work_bytes = 0;
+            err = cudaMalloc(&h->work, bytes);
+            if (err != cudaSuccess) return fail(BB_ERR_NOMEM, "working band allocation failed");
+            h->work_bytes = bytes;
+        }
+        wb = (T*)h->work;
+        err = cudaMemcpy2DAsync(wb, sizeof(T) * ldw, band, sizeof(T) * ldab, sizeof(T) * ldab, (size_t)n,
+                                cudaMemcpyDeviceToDevice, s);
+        if (err != cudaSuccess) return cuda_fail(err, "copy to the working band");
+    }
     if (lo == 0) {
-        err = bb::run_zero_fill<T>(band, n, ldab, (int)tw, ku, s);
+        err = bb::run_zero_fill<T>(wb, n, ldw, (int)tw, ku, s);
         if (err != cudaSuccess) return cuda_fail(err, "zero fill launch");
         h->last_launches += 1;
     }
@@ -329,27 +375,15 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         }
     }
     for (int64_t pi = lo; pi < hi; ++pi) {
-        const int b = plan[pi].b, t = plan[pi].t;
-        bb::PassArgs P;
-        P.n = n;
-        P.ldab = ldab;
-        P.b = b;
-        P.t = t;
-        P.bp = b - t;
-        P.ku = ku;
-        P.nsweeps = (int)std::max<int64_t>(0, n - (b - t) - 1);
-        P.lag = pass_lag_cycle(b, t);
-        P.lagh = pass_lag_half(b, t);
-        P.stall_sweep = h->stall_sweep;
-        P.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+        const bb::PassArgs P = pass_args(pi, ldw);
         bb::LaunchCfg cfg;
-        cfg.tpb = h->tpb ? h->tpb : bb::auto_tpb(b, t);
+        cfg.tpb = h->tpb ? h->tpb : bb::auto_tpb(P.b, P.t);
         cfg.max_ctas = h->max_ctas;
         cfg.num_sms = h->num_sms;
         cfg.group_size = h->group_size;
         bb::LaunchStats st;
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo)], s);
-        err = bb::run_pass<T>(band, P, h->scheduler, cfg, h->d_progress, h->d_status, s, &st);
+        err = bb::run_pass<T>(wb, P, h->scheduler, cfg, h->d_progress, h->d_status, s, &st);
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo) + 1], s);
         h->last_launches += st.launches;
         if (err != cudaSuccess) return cuda_fail(err, "pass launch");
@@ -357,9 +391,14 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         h->pass_kernel.push_back(st.kernel);
         h->pass_group.push_back(st.group);
     }
-    err = bb::run_extract<T>(band, n, ldab, ku, d, e, s);
+    err = bb::run_extract<T>(wb, n, ldw, ku, d, e, s);
     if (err != cudaSuccess) return cuda_fail(err, "extract launch");
     h->last_launches += 1;
+    if (wb != band) {
+        err = cudaMemcpy2DAsync(band, sizeof(T) * ldab, wb, sizeof(T) * ldw, sizeof(T) * ldab, (size_t)n,
+                                cudaMemcpyDeviceToDevice, s);
+        if (err != cudaSuccess) return cuda_fail(err, "copy back from the working band");
+    }
     return BB_OK;
 }
 
@@ -464,7 +503,6 @@ int group_footprint(const PassArgs& P, int g, int ahead) {
 
 bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out) {
     const size_t budget = 220 * 1024;
-    const int ld = P.b + 2 * P.t + 1;
     GroupArgs best{};
     const int gcap = group_max_warps(wmax, elem);
     const int gmax = requested > 0 ? std::min(requested, gcap) : gcap;
@@ -472,7 +510,12 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
         GroupArgs ga;
         ga.g = g;
         ga.ngroups = (int)((P.nsweeps + g - 1) / g);
-        ga.lds = ld + (ld & 1);  // even: conflict-free column-block access
+        // rows top .. top + lds - 1 hold the pass's rows ku-b-t .. ku+t, both
+        // ends rounded out to 16 bytes (the extra rows are ones the pass
+        // leaves alone: copied in and written back unchanged)
+        const int q = (int)(16 / elem);
+        ga.top = (P.ku - P.b - P.t) / q * q;
+        ga.lds = (P.ku + P.t + 1 - ga.top + q - 1) / q * q;
         ga.ahead = kGroupAhead;
         ga.nslot = std::max(1, group_footprint(P, g, ga.ahead));
         if (group_smem_bytes(ga, wmax, elem) > budget) break;

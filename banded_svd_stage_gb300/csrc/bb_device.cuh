@@ -494,7 +494,7 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
     return v;
 }
 
-// Block-wide wait until *flag >= target.  Thread 0 spins with relaxed loads;
+// Block-wide wait until *flag >= target.  Thread 0 spins with acquire loads;
 // the wait is bounded by P.wait_budget SM clock cycles and by an iteration
 // cap, and gives up early if another CTA has already latched an error.  On
 // giving up it latches kStatusTimeout and the block returns false.
@@ -502,11 +502,13 @@ __device__ __forceinline__ bool block_wait(const int* flag, int target, int* sta
                                            const PassArgs& P, int* s_flag) {
     if (threadIdx.x == 0) {
         int ok = 1;
-        if (ld_relaxed_gpu(flag) < target) {
+        // every poll is an acquire load, so the one that sees the target
+        // already orders this block's later reads after the producer's writes
+        if (ld_acquire_gpu(flag) < target) {
             const long long t0 = clock64();
             unsigned int it = 0;
             for (;;) {
-                if (ld_relaxed_gpu(flag) >= target) break;
+                if (ld_acquire_gpu(flag) >= target) break;
                 ++it;
                 if ((it & 255u) == 0u) {
                     if (ld_relaxed_gpu(status) != kStatusOk) { ok = 0; break; }
@@ -518,9 +520,6 @@ __device__ __forceinline__ bool block_wait(const int* flag, int target, int* sta
                 }
             }
         }
-        // the value seen is final (counters only grow): one acquire load
-        // orders this block's later reads after the producer's writes
-        if (ok) (void)ld_acquire_gpu(flag);
         *s_flag = ok;
     }
     __syncthreads();

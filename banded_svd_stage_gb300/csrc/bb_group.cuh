@@ -27,13 +27,14 @@
 
 namespace bb {
 
-constexpr int kPublishEvery = 4;  // ticks between two publications of a group's watermark
 
 struct GroupArgs {
     int g;        // sweeps per group
     int ngroups;  // ceil(nsweeps / g)
     int nslot;    // columns of the circular buffer
-    int lds;      // shared-memory stride between buffered columns (even)
+    int top;      // first band row a buffered column holds (a multiple of 16 bytes / element)
+    int lds;      // rows a buffered column holds = stride between buffered columns
+                  // (a multiple of 16 bytes / element, so lds - 1 is odd)
     int ahead;    // ticks the loader may run ahead of the storer (1 .. kMaxStages - 2)
 };
 
@@ -47,51 +48,74 @@ __device__ __forceinline__ long long half_min_col(const PassArgs& P, int r, int 
     return (long long)r + P.bp + (long long)(h >> 1) * P.b;
 }
 
-// Accessor of the buffered band: A(i, j) of the pass lives at
-// cols[slot(j) * lds + (i - j + b + t)], slot(j) = j mod nslot.
+// Accessor of the buffered band: A(i, j) lives at
+// cols[slot(j) * lds + (i - j + off)], slot(j) = j mod nslot, off = ku - top:
+// buffered column j is band rows top .. top + lds - 1 of column j.
 template <typename T>
 struct ColBuf {
     T* cols;
-    int nslot, lds, off;  // off = b + t
-    __device__ __forceinline__ int slot(long long j) const { return (int)j % nslot; }
-    __device__ __forceinline__ T* col(long long j) const { return cols + (size_t)slot(j) * lds; }
+    int nslot, lds, off;
+    __device__ __forceinline__ int slot(int j) const { return j % nslot; }
+    __device__ __forceinline__ T* col(int j) const { return cols + slot(j) * lds; }
 };
 
-// Right half-step of sweep r, step k on the buffered band, by one warp.
+// Geometry of step k of sweep r in 32-bit arithmetic (the group kernel runs
+// only for n < 2^30): c, p, ce, cend and w as in step_geom.
+struct GGeom {
+    int c, p, ce, cend, w;
+};
+__device__ __forceinline__ GGeom gstep(const PassArgs& P, int r, int k) {
+    GGeom g;
+    const int n1 = (int)P.n - 1;
+    g.c = r + P.bp + k * P.b;
+    g.p = (k == 0) ? r : g.c - P.b;
+    g.ce = min(g.c + P.t, n1);
+    g.cend = min(g.ce + P.b, n1);
+    g.w = g.ce - g.c + 1;
+    return g;
+}
+
+// Right half-step (rows p..ce of columns c..ce) on the buffered band, by one
+// warp: reflector from row p, then lane i applies it to rows p+1+i, +32, ...
+// The half-step's columns span fewer than nslot slots, so a slot index past
+// the end wraps with one subtraction.
 template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_right(const PassArgs& P, const ColBuf<T>& cb, int r, int k, T* vb,
-                                            T* taub) {
+__device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
-    const StepGeom g = step_geom(P, r, k);
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    const int off = cb.off;
+    const int s0 = cb.slot(g.c);
+    // A(i, c+m) = cb.cols[idx[m] + (i - p)] with idx[m] = slot(c+m) lds + off + p - (c+m)
+    int idx[WMAX];
+    {
+        int sl = s0;
+#pragma unroll
+        for (int m = 0; m < WMAX; ++m) {
+            if (m < W) idx[m] = sl * cb.lds + cb.off + (g.p - g.c - m);
+            sl = (sl + 1 == cb.nslot) ? 0 : sl + 1;
+        }
+    }
     T xp[NPL];
+    int xo[NPL];
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        xp[q] = (m < W) ? cb.col(g.c + m)[g.p - (g.c + m) + off] : T(0);
+        int sl = s0 + m;
+        if (sl >= cb.nslot) sl -= cb.nslot;
+        xo[q] = sl * cb.lds + cb.off + (g.p - g.c - m);
+        xp[q] = (m < W) ? cb.cols[xo[q]] : T(0);
     }
     T beta = warp_larfg<T, NPL>(xp, W, lane, vb, taub);
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        if (m < W) cb.col(g.c + m)[g.p - (g.c + m) + off] = (m == 0) ? beta : T(0);
+        if (m < W) cb.cols[xo[q]] = (m == 0) ? beta : T(0);
     }
     __syncwarp();
     const T tau = *taub;
     if (tau == T(0)) return;
-    // A(i, c+m) = cb.cols[idx[m] + (i - p)] with idx[m] = slot(c+m) lds + off + p - (c+m)
-    int idx[WMAX];
-    {
-        int s = cb.slot(g.c);
-#pragma unroll
-        for (int m = 0; m < WMAX; ++m) {
-            if (m < W) idx[m] = s * cb.lds + off + (int)(g.p - (g.c + m));
-            s = (s + 1 == cb.nslot) ? 0 : s + 1;
-        }
-    }
-    const int nrows = (int)(g.ce - g.p);
+    const T* v = vb;
+    const int nrows = g.ce - g.p;
     for (int i = 1 + lane; i <= nrows; i += 32) {
         T x[WMAX];
         T y = 0;
@@ -99,25 +123,25 @@ __device__ __forceinline__ void group_right(const PassArgs& P, const ColBuf<T>& 
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
                 x[m] = cb.cols[idx[m] + i];
-                y = fma(x[m], vb[m], y);
+                y = fma(x[m], v[m], y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) cb.cols[idx[m] + i] = fma(-s, vb[m], x[m]);
+            if (m < W) cb.cols[idx[m] + i] = fma(-s, v[m], x[m]);
     }
 }
 
-// Left half-step of sweep r, step k on the buffered band, by one warp.
+// Left half-step (rows c..ce of columns c..cend) on the buffered band, by
+// one warp: reflector from column c, then lane i applies it to columns
+// c+1+i, +32, ...
 template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_left(const PassArgs& P, const ColBuf<T>& cb, int r, int k, T* vb,
-                                           T* taub) {
+__device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
-    const StepGeom g = step_geom(P, r, k);
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    const int off = cb.off;
-    T* colc = cb.col(g.c) + off;  // colc[m] = A(c + m, c)
+    const int s0 = cb.slot(g.c);
+    T* colc = cb.cols + s0 * cb.lds + cb.off;  // colc[m] = A(c + m, c)
     T xc[NPL];
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
@@ -133,37 +157,41 @@ __device__ __forceinline__ void group_left(const PassArgs& P, const ColBuf<T>& c
     __syncwarp();
     const T tau = *taub;
     if (tau == T(0)) return;
-    for (long long j = g.c + 1 + lane; j <= g.cend; j += 32) {
-        T* cj = cb.col(j) + off + (g.c - j);  // cj[m] = A(c + m, j)
+    const T* v = vb;
+    for (int dj = 1 + lane; dj <= g.cend - g.c; dj += 32) {
+        int sl = s0 + dj;
+        if (sl >= cb.nslot) sl -= cb.nslot;
+        T* cj = cb.cols + sl * cb.lds + cb.off - dj;  // cj[m] = A(c + m, c + dj)
         T x[WMAX];
         T y = 0;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
                 x[m] = cj[m];
-                y = fma(vb[m], x[m], y);
+                y = fma(v[m], x[m], y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) cj[m] = fma(-s, vb[m], x[m]);
+            if (m < W) cj[m] = fma(-s, v[m], x[m]);
     }
 }
 
 template <typename T, int WMAX>
 __device__ __forceinline__ void group_half(const PassArgs& P, const ColBuf<T>& cb, int r, int h, T* vb, T* taub) {
-    const int k = h >> 1;
-    const bool full = step_geom(P, r, k).w == WMAX;
+    const GGeom g = gstep(P, r, h >> 1);
+    const bool full = g.w == WMAX;
     if ((h & 1) == 0) {
-        if (full) group_right<T, WMAX, true>(P, cb, r, k, vb, taub);
-        else group_right<T, WMAX, false>(P, cb, r, k, vb, taub);
+        if (full) group_right<T, WMAX, true>(cb, g, vb, taub);
+        else group_right<T, WMAX, false>(cb, g, vb, taub);
     } else {
-        if (full) group_left<T, WMAX, true>(P, cb, r, k, vb, taub);
-        else group_left<T, WMAX, false>(P, cb, r, k, vb, taub);
+        if (full) group_left<T, WMAX, true>(cb, g, vb, taub);
+        else group_left<T, WMAX, false>(cb, g, vb, taub);
     }
 }
 
-// Warps a group CTA may have (its sweeps plus the loader and the storer): a
+// Warps a group CTA may have (its sweeps plus the loader, the storer and the
+// publisher): a
 // lane holds one row or column of WMAX entries plus WMAX buffer offsets.
 template <typename T, int WMAX>
 struct GroupMaxWarps {
@@ -196,15 +224,15 @@ __device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned pari
     return ok != 0;
 }
 // Bounded wait for the phase of parity `parity` of *bar; false on giving up
-// (after `budget` SM clock cycles, or when *abort_tick <= tick).
+// (after `budget` SM clock cycles, when *abort_tick <= tick or when *dead).
 __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned long long budget,
-                                          const volatile int* abort_tick, int tick) {
+                                          const volatile int* abort_tick, int tick, const volatile int* dead) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     for (unsigned it = 1;; ++it) {
         if (mbar_test(bar, parity)) return true;
         if ((it & 63u) == 0u) {
-            if (*abort_tick <= tick) return false;
+            if (*abort_tick <= tick || *dead) return false;
             if ((unsigned long long)(clock64() - t0) > budget) return false;
         }
     }
@@ -217,6 +245,36 @@ __device__ __forceinline__ int ld_acquire_cta_shared(const int* p) {
 __device__ __forceinline__ void st_release_cta_shared(int* p, int v) {
     asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
+// Bulk (TMA) copies of one buffered column, 16-byte aligned on both sides.
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, unsigned bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, unsigned bytes, unsigned long long* bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(smem_src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have read their shared-memory source
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// this thread's bulk stores but those of the most recent group are complete
+__device__ __forceinline__ void bulk_wait_prev() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
+// order this thread's generic-proxy accesses with later async-proxy (bulk
+// copy) accesses of shared or global memory, and vice versa
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -257,26 +315,6 @@ __device__ __forceinline__ bool warp_wait(const int* flag, int target, int* stat
     return ok != 0;
 }
 
-// Columns [j0, j1] between memory and the buffer, by one warp.
-template <typename T, bool LOAD>
-__device__ __forceinline__ void warp_move_cols(T* __restrict__ band, const PassArgs& P, const ColBuf<T>& cb,
-                                               long long j0, long long j1) {
-    if (j1 < j0) return;
-    const int ld = P.b + 2 * P.t + 1;
-    const long long top = (long long)P.ku - P.b - P.t;
-    const int lane = threadIdx.x & 31;
-    int sl = cb.slot(j0);
-    for (long long j = j0; j <= j1; ++j) {
-        T* sm = cb.cols + (size_t)sl * cb.lds;
-        T* gm = band + j * P.ldab + top;
-        for (int row = lane; row < ld; row += 32) {
-            if (LOAD) cp_async_elem<T>(sm + row, gm + row);
-            else gm[row] = sm[row];
-        }
-        sl = (sl + 1 == cb.nslot) ? 0 : sl + 1;
-    }
-}
-
 // Last column ticks <= ... touch, one sweep per lane: max over the group's
 // sweeps active at tick u of the last column of their half-step.
 __device__ __forceinline__ long long tick_max_col(const PassArgs& P, int r0, int ng, int L, const int* nsteps,
@@ -305,20 +343,32 @@ __device__ __forceinline__ long long tick_min_col(const PassArgs& P, int r0, int
 
 constexpr int kMaxStages = 8;
 
+// Shared memory of the group kernel: per-sweep reflectors and scalars, then
+// (16-byte aligned) the circular column buffer.
+__host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem) {
+    const size_t head = elem * ((size_t)g * wmax + (size_t)((g + 1) & ~1));
+    return (head + 15) & ~(size_t)15;
+}
+
 // Persistent group kernel: CTAs take groups G = blockIdx.x, + gridDim.x, ...
-// in order; blockDim.x = 32 * (g + 2).  Warp jj < g runs sweep r0 + jj, one
+// in order; blockDim.x = 32 * (g + 3).  Warp jj < g runs sweep r0 + jj, one
 // half-step per tick, the g warps meeting at a named barrier after each
-// tick.  Warp g (the loader) copies in the columns tick u first needs, once
-// group G - 1's watermark is beyond them and the storer has freed their
-// slots, and signals full[u mod S] when the copies have landed.  Warp g + 1
-// (the storer) waits for done[v mod S] (tick v computed), writes back the
-// columns no later tick touches, frees their slots and, every few ticks,
-// publishes the group's watermark (the first column the group may still
-// touch) with a gpu-scope fence.  The loader runs at most `ahead` ticks
-// ahead of the storer, S = ahead + 2 stages, so no mbarrier phase is
-// overtaken.  Copies, write-backs and fences thus overlap the computation.
-// Every wait is bounded; on giving up the CTA latches an error and all its
-// warps leave at the same tick.
+// tick.  Warp g (the loader) copies in the columns tick u first needs, one
+// bulk (TMA) copy per column, once group G - 1's watermark is beyond them and
+// the storer has freed their slots; full[u mod S] completes when the bytes
+// have landed.  Warp g + 1 (the storer) waits for done[v mod S] (tick v
+// computed), writes back with bulk copies the columns no later tick touches,
+// frees their slots and, one tick later (so that the wait rarely stalls),
+// reports them complete in shared memory; warp g + 2 (the publisher) turns
+// that report into the group's watermark (the first column the group may
+// still touch) with a gpu-scope fence and a release store, so the fence
+// delays neither the storer nor the loader.  The loader runs at most `ahead` ticks ahead of the storer and S = ahead + 2
+// stages, so no mbarrier phase is overtaken.  Copies, write-backs and fences
+// thus overlap the computation.  Every wait is bounded; on giving up the CTA
+// latches an error, the compute warps leave their loop at the same tick, the
+// other roles leave theirs, and the CTA returns after one last barrier.
+// Requires band, ldab * sizeof(T) and top * sizeof(T) 16-byte aligned and
+// n < 2^30 (32-bit geometry).
 template <typename T, int WMAX>
 __global__ void __launch_bounds__(32 * GroupMaxWarps<T, WMAX>::value)
 pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restrict__ wm,
@@ -329,24 +379,26 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     __shared__ __align__(8) unsigned long long s_full[kMaxStages], s_done[kMaxStages];
     __shared__ int s_freed;       // storer: columns < s_freed are written back
     __shared__ int s_retired;     // storer: last tick whose columns it retired
+    __shared__ int s_written;     // storer: columns < s_written are written back and complete
     __shared__ volatile int s_abort_tick;  // first tick the CTA does not run
-    __shared__ int s_dead;        // a compute warp gave up waiting
+    __shared__ volatile int s_dead;  // a warp gave up waiting on a signal that never came
     T* vbuf = reinterpret_cast<T*>(smem_raw);  // [g][WMAX]
     T* taubuf = vbuf + (size_t)GA.g * WMAX;    // [g]
     ColBuf<T> cb;
-    cb.cols = taubuf + ((GA.g + 1) & ~1);
+    cb.cols = reinterpret_cast<T*>(smem_raw + group_cols_offset(GA.g, WMAX, sizeof(T)));
     cb.nslot = GA.nslot;
     cb.lds = GA.lds;
-    cb.off = P.b + P.t;
+    cb.off = P.ku - GA.top;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int L = P.lagh;
     const int S = GA.ahead + 2;
+    const unsigned col_bytes = (unsigned)(GA.lds * sizeof(T));
     const unsigned long long inner_budget = 2 * P.wait_budget + (1ull << 24);
     if (threadIdx.x == 0) {
         s_flag = ld_relaxed_gpu(status);
         for (int s = 0; s < S; ++s) {
-            mbar_init(&s_full[s], 32);
+            mbar_init(&s_full[s], 1);
             mbar_init(&s_done[s], 1);
         }
         s_abort_tick = 0x7fffffff;
@@ -363,6 +415,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
         if (threadIdx.x == 0) {
             s_freed = r0 + P.bp;
             s_retired = -1;
+            s_written = -1;
         }
         __syncthreads();
         int tend = 0;
@@ -370,28 +423,35 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
         if (warp < GA.g) {
             // ---- compute warps ----
             const int my_h_end = (warp < ng) ? 2 * s_nsteps[warp] : 0;
+            int stage = (int)(T0 % (unsigned)S);
+            unsigned phase = (T0 / (unsigned)S) & 1u;
             for (int tau = 0; tau < tend; ++tau) {
-                const unsigned q = T0 + (unsigned)tau;
-                if (!mbar_wait(&s_full[q % S], (q / S) & 1u, inner_budget, &s_abort_tick, tau)) {
+                if (!mbar_wait(&s_full[stage], phase, inner_budget, &s_abort_tick, tau, &s_dead)) {
                     if (s_abort_tick > tau) {  // no abort announced: a lost signal
                         atomicCAS(status, kStatusOk, kStatusInternal);
                         s_dead = 1;
                     }
                 }
-                if (s_abort_tick <= tau) return;  // same tick for every compute warp
+                if (s_abort_tick <= tau) break;  // same tick for every compute warp
                 const int h = tau - L * warp;
-                if (!s_dead && h >= 0 && h < my_h_end)
+                if (!s_dead && h >= 0 && h < my_h_end) {
                     group_half<T, WMAX>(P, cb, r0 + warp, h, vbuf + (size_t)warp * WMAX, taubuf + warp);
+                    fence_proxy_async_smem();  // the storer's bulk copies read these columns
+                }
                 named_bar_sync(1, 32 * GA.g);
-                if (s_dead) return;
-                if (threadIdx.x == 0) mbar_arrive(&s_done[q % S]);
+                if (s_dead) break;  // read after the barrier: same tick for every compute warp
+                if (threadIdx.x == 0) mbar_arrive(&s_done[stage]);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         } else if (warp == GA.g) {
             // ---- loader ----
             long long B = (long long)r0 + P.bp - 1;  // last column copied in
             int seen = (G == 0) ? 0x7fffffff : -1;
+            int stage = (int)(T0 % (unsigned)S);
             for (int u = 0; u < tend; ++u) {
-                const unsigned q = T0 + (unsigned)u;
                 bool ok = true;
                 // stay within `ahead` ticks of the storer (mbarrier phases)
                 if (u - GA.ahead - 1 >= 0) {
@@ -408,62 +468,115 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                         if ((unsigned long long)(clock64() - t0) > inner_budget || s_dead) { ok = false; break; }
                     }
                     if (ok && G > 0) ok = warp_wait(wm + G - 1, (int)(xn + 1), status, P, seen);
-                    if (ok) {
-                        warp_move_cols<T, true>(band, P, cb, B + 1, xn);
-                        B = xn;
-                    }
                 }
                 if (!ok) {
                     if (lane == 0) {
                         atomicCAS(status, kStatusOk, kStatusTimeout);
                         s_abort_tick = u;
+                        mbar_arrive(&s_full[stage]);  // completes the phase: no bytes expected
                     }
-                    cp_async_wait_all();
-                    __syncwarp();
-                    mbar_arrive(&s_full[q % S]);  // every lane: completes the phase
-                    return;
+                    // let the copies already issued land before the CTA leaves
+                    const int never = 0;
+                    for (int v = max(0, u - S + 1); v < u; ++v) {
+                        const unsigned qv = T0 + (unsigned)v;
+                        (void)mbar_wait(&s_full[qv % S], (qv / S) & 1u, inner_budget, &s_abort_tick, 0x7fffffff,
+                                        &never);
+                    }
+                    break;
                 }
-                mbar_arrive_cp_async(&s_full[q % S]);
+                if (xn > B) {
+                    if (lane == 0) mbar_arrive_expect_tx(&s_full[stage], (unsigned)(xn - B) * col_bytes);
+                    __syncwarp();
+                    // the copies read what group G - 1 wrote (acquired above)
+                    fence_proxy_async_global();
+                    for (int j = (int)B + 1 + lane; j <= (int)xn; j += 32)
+                        bulk_load(cb.col(j), band + (long long)j * P.ldab + GA.top, col_bytes, &s_full[stage]);
+                    B = xn;
+                } else if (lane == 0) {
+                    mbar_arrive(&s_full[stage]);
+                }
+                if (++stage == S) stage = 0;
             }
-            cp_async_wait_all();
-        } else {
+        } else if (warp == GA.g + 1) {
             // ---- storer ----
             long long A = (long long)r0 + P.bp;  // first column not yet written back
             long long xr = -1;                   // last column ticks <= v touch
-            int published = -1;
+            int a_prev = (int)A;                 // A before this iteration's write-backs
+            bool stopped = false;
+            int stage = (int)(T0 % (unsigned)S);
+            unsigned phase = (T0 / (unsigned)S) & 1u;
             for (int v = 0; v < tend; ++v) {
-                const unsigned q = T0 + (unsigned)v;
-                if (!mbar_wait(&s_done[q % S], (q / S) & 1u, inner_budget, &s_abort_tick, v)) {
-                    if (lane == 0 && s_abort_tick > v) {  // no abort announced: a lost signal
+                if (!mbar_wait(&s_done[stage], phase, inner_budget, &s_abort_tick, v, &s_dead)) {
+                    if (lane == 0 && s_abort_tick > v && !s_dead) {  // no abort announced: a lost signal
                         atomicCAS(status, kStatusOk, kStatusInternal);
                         s_dead = 1;
                     }
-                    return;
+                    stopped = true;
+                    break;
+                }
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
                 xr = max(xr, tick_max_col(P, r0, ng, L, s_nsteps, v));
                 long long an = (v == tend - 1) ? (long long)P.n : tick_min_col(P, r0, ng, L, s_nsteps, v + 1);
                 an = min(an, xr + 1);
                 if (an > A) {
-                    warp_move_cols<T, false>(band, P, cb, A, an - 1);
+                    for (int j = (int)A + lane; j < (int)an; j += 32)
+                        bulk_store(band + (long long)j * P.ldab + GA.top, cb.col(j), col_bytes);
                     A = an;
                 }
+                bulk_commit();
+                bulk_wait_read();  // sources read: the slots may be refilled
+                // columns written back in earlier iterations are complete once
+                // only this iteration's group may still be pending: publish them
+                // (one iteration late, so the wait rarely stalls)
+                bulk_wait_prev();
+                fence_proxy_async_global();
                 __syncwarp();
                 if (lane == 0) {
                     st_release_cta_shared(&s_freed, (int)A);
                     st_release_cta_shared(&s_retired, v);
-                    const bool last = v == tend - 1;
-                    if ((last || (v % kPublishEvery) == kPublishEvery - 1) && (int)A > published) {
-                        published = (int)min(A, (long long)P.n);
-                        if (P.stall_sweep < r0 || P.stall_sweep >= r0 + ng) {
+                    st_release_cta_shared(&s_written, a_prev);
+                }
+                a_prev = (int)A;
+            }
+            bulk_wait_all();
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0 && !stopped) st_release_cta_shared(&s_written, (int)P.n);
+        } else if (warp == GA.g + 2) {
+            // ---- publisher: the gpu-scope fence stays off the storer's path ----
+            if (lane == 0) {
+                const bool publish = P.stall_sweep < r0 || P.stall_sweep >= r0 + ng;  // fault injection
+                int published = -1;
+                long long t0 = clock64();
+                for (;;) {
+                    const int a = ld_acquire_cta_shared(&s_written);
+                    if (a > published) {
+                        if (publish) {
                             __threadfence();
-                            st_release_gpu(wm + G, published);
+                            st_release_gpu(wm + G, a);
                         }
+                        published = a;
+                        if (a >= P.n) break;
+                        t0 = clock64();
+                    } else {
+                        if (s_abort_tick != 0x7fffffff || s_dead) break;
+                        if ((unsigned long long)(clock64() - t0) > inner_budget) {
+                            atomicCAS(status, kStatusOk, kStatusInternal);
+                            s_dead = 1;
+                            break;
+                        }
+                        __nanosleep(64);
                     }
                 }
             }
         }
         T0 += (unsigned)tend;
         __syncthreads();
+        // every warp has left its loop; the flags are final and read alike
+        if (s_dead || s_abort_tick != 0x7fffffff) return;
     }
 }
 

@@ -13,6 +13,15 @@ namespace bb {
 // Largest reflector length the kernels are instantiated for (tw <= 64).
 constexpr int kMaxW = 65;
 
+// Reflector lengths the kernels are compiled for: the exact t + 1 of common
+// tile widths (interior steps then run without predicates) and buckets for
+// the rest (predicated on the run-time length).
+inline int wmax_bucket(int w) {
+    for (int c : {8, 9, 16, 17, 32, 33, 65})
+        if (w <= c) return c;
+    return 0;
+}
+
 struct LaunchCfg {
     int tpb = 0;         // threads per block (flag and per-cycle kernels)
     int max_ctas = 0;    // cap on the persistent grid (0: co-resident maximum)
@@ -31,16 +40,45 @@ struct LaunchStats {
 // Shared memory of the group kernel: per-sweep reflectors and scalars, then
 // the circular column buffer.
 inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem) {
-    return elem * ((size_t)GA.g * wmax + (size_t)((GA.g + 1) & ~1) + (size_t)GA.nslot * GA.lds);
+    return group_cols_offset(GA.g, wmax, elem) + elem * (size_t)GA.nslot * GA.lds;
 }
 
-// Largest group (<= requested, or <= 16 when requested == 0) whose column
-// buffer fits in shared memory; false if not even one sweep fits.
+// Largest group (<= requested, or the most the kernel is compiled for when
+// requested == 0) whose column buffer fits in shared memory; false if not
+// even one sweep fits.  The kernel then needs the band and ldab * elem
+// 16-byte aligned (group_layout_ok).
 bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out);
 
+// Whether the group kernel's bulk copies can address this band storage.
+inline bool group_layout_ok(const void* band, long long ldab, size_t elem) {
+    return ((uintptr_t)band & 15) == 0 && ((size_t)ldab * elem) % 16 == 0;
+}
+
+// Orders the group kernel handles (its step geometry is 32-bit).
+constexpr long long kGroupMaxN = 1LL << 30;
+
 // Largest group size the group kernel is compiled for (GroupMaxWarps, minus
-// the loader and the storer warps).
-inline int group_max_warps(int wmax, size_t elem) { return ((wmax * (int)elem <= 17 * 4) ? 16 : 8) - 2; }
+// the loader, storer and publisher warps).
+inline int group_max_warps(int wmax, size_t elem) { return ((wmax * (int)elem <= 17 * 4) ? 16 : 8) - 3; }
+
+// Fewest sweeps per group for which the automatic scheduler prefers the
+// group kernel: with fewer, the per-group hand-over (a few ticks) is shared
+// by too few sweeps and the flag kernel is faster (measured on the
+// workloads' passes: the group kernel wins from 5 sweeps per group on).
+constexpr int kAutoGroupMin = 5;
+
+// Whether a pass goes to the group kernel, and its group plan: scheduler 3
+// always when a group fits, scheduler 0 (automatic) when at least
+// kAutoGroupMin sweeps fit (given a storage that suits bulk copies).
+inline bool choose_group(const PassArgs& P, int scheduler, int group_size, size_t elem, GroupArgs* out) {
+    if (scheduler != 0 && scheduler != 3) return false;
+    if (P.nsweeps <= 0 || P.n >= kGroupMaxN) return false;
+    GroupArgs ga;
+    if (!plan_group(P, wmax_bucket(P.t + 1), elem, group_size, &ga)) return false;
+    if (scheduler == 0 && ga.g < kAutoGroupMin) return false;
+    if (out) *out = ga;
+    return true;
+}
 
 // Ticks the group kernel's loader runs ahead of its storer.
 constexpr int kGroupAhead = 3;

@@ -8,15 +8,6 @@
 
 namespace bb {
 
-// Reflector lengths the kernels are compiled for: the exact t + 1 of common
-// tile widths (interior steps then run without predicates) and buckets for
-// the rest (predicated on the run-time length).
-inline int wmax_bucket(int w) {
-    for (int c : {8, 9, 16, 17, 32, 33, 65})
-        if (w <= c) return c;
-    return 0;
-}
-
 template <typename T, int WMAX>
 size_t smem_bytes(const PassArgs& P) {
     const int wp = WMAX | 1;
@@ -39,7 +30,7 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
         if (err != cudaSuccess) return err;
         int per_sm = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 2), gsmem);
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 3), gsmem);
         if (err != cudaSuccess) return err;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         long long grid = std::min<long long>((long long)per_sm * cfg.num_sms, GA.ngroups);
@@ -52,7 +43,7 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
         int* prog_arg = progress;
         int* stat_arg = status;
         void* args[] = {&band_arg, &p_arg, &g_arg, &prog_arg, &stat_arg};
-        err = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 2)), args,
+        err = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 3)), args,
                                           gsmem, stream);
         if (stats) {
             stats->launches += 1;
@@ -124,15 +115,11 @@ cudaError_t run_pass(T* band, const PassArgs& P, int scheduler, const LaunchCfg&
                      int* progress, int* status, cudaStream_t stream, LaunchStats* stats) {
     LaunchCfg cfg = cfg_in;
     const int wmax = wmax_bucket(P.t + 1);
-    if (scheduler == 0) {
-        // automatic: the flag kernel, which measures faster than the group
-        // kernel on every workload so far (per-tick column hand-over and
-        // bookkeeping of the group kernel still cost more than the flag
-        // hand-offs they replace)
-        scheduler = 2;
-    } else if (scheduler == 3) {
-        // group kernel where one group's columns fit shared memory
-        const bool ok = plan_group(P, wmax, sizeof(T), cfg.group_size, &cfg.group);
+    if (scheduler == 0 || scheduler == 3) {
+        // group kernel where enough sweeps' columns fit shared memory and the
+        // storage suits bulk copies; the flag kernel otherwise
+        const bool ok = group_layout_ok(band, P.ldab, sizeof(T)) &&
+                        choose_group(P, scheduler, cfg.group_size, sizeof(T), &cfg.group);
         scheduler = ok ? 3 : 2;
     }
     switch (wmax) {

@@ -1,7 +1,7 @@
 """Benchmark of the band -> bidiagonal reduction on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--scheduler 0|1] [--no-sweep]
+                    [--workload NAME] [--scheduler 0|1|2|3] [--no-sweep]
 
 One step is one whole reduction (every pass down to bidiagonal form, plus the
 fill-row zeroing and the d/e extraction) of one synthetic band.  Before each
@@ -270,6 +270,29 @@ def _model_bytes_py(w):
     return tot
 
 
+KERNEL_NAMES = {1: "pass_cycle_kernel", 2: "pass_persistent_kernel", 3: "pass_group_kernel"}
+SCHEDULER_NAMES = {0: "auto", 1: "per-cycle", 2: "flags", 3: "group"}
+
+
+def dominant_kernel(res):
+    """(name, achieved GB/s, launches, bytes, ms) of the pass kernel with the
+    largest share of the step's pass time."""
+    tot = {}
+    for (kind, _g), ms, by in zip(res["kernels"], res["pass_ms_mean"], res["pass_bytes"]):
+        t = tot.setdefault(kind, [0.0, 0.0, 0])
+        t[0] += ms
+        t[1] += by
+        t[2] += 1
+    if not tot:
+        return None, None, 0, 0.0, 0.0
+    kind = max(tot, key=lambda k: tot[k][0])
+    ms, by, nl = tot[kind]
+    if kind == 1:
+        nl = None  # one launch per cycle: many launches per pass
+    ach = by / (ms * 1e-3) / 1e9 if ms > 0 else None
+    return KERNEL_NAMES.get(kind, str(kind)), ach, nl if nl else 0, by, ms
+
+
 def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
     summary, if that summary was taken on the current kernel sources."""
@@ -354,16 +377,17 @@ def main():
     ms_step = sum(res["ms"]) / len(res["ms"])
     ms_max, bytes_all = aggregate(ms_step, res["model_bytes"])
     value = bytes_all / (ms_max * 1e-3) / 1e9
-    # roofline of the dominant kernel (the per-pass kernel: one launch a pass)
-    tot_pass_ms = sum(res["pass_ms_mean"])
-    achieved = sum(res["pass_bytes"]) / (tot_pass_ms * 1e-3) / 1e9 if tot_pass_ms > 0 else None
-    kname = "pass_persistent_kernel" if args.scheduler == 0 else "pass_cycle_kernel"
+    # roofline of the dominant kernel: the pass kernel (one launch a pass for
+    # the flag and group kernels) that takes the most time in a step
+    kname, achieved, nl, kbytes, kms = dominant_kernel(res)
     traffic = traffic_for(kname, w.name)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
-            "kernel": kname, "peak_source": peak_src,
-            "launches_per_step": len(res["pass_ms_mean"]) if args.scheduler == 0 else None,
-            "achieved_def": "sum over passes of algorithmic bytes / sum of per-pass CUDA-event time"}
+            "kernel": kname, "peak_source": peak_src, "launches_per_step": nl,
+            "algorithmic_bytes_per_launch": kbytes / nl if nl else None,
+            "ms_per_launch": kms / nl if nl else None,
+            "achieved_def": "algorithmic bytes of the kernel's passes / their CUDA-event time "
+                            "(events on the launching stream around each pass launch)"}
 
     sweep = []
     if rank == 0 and world == 1 and not args.no_sweep:
@@ -387,7 +411,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "n": w.n, "bw": w.bw, "tw": w.tw, "dist": w.dist,
-                       "graded": w.graded, "scheduler": "persistent" if args.scheduler == 0 else "per-cycle",
+                       "graded": w.graded, "scheduler": SCHEDULER_NAMES.get(args.scheduler, str(args.scheduler)),
                        "l2": "flushed between steps (256 MiB write); band restored before each step",
                        "parallelism": f"replicas x{world}"},
             "frac_of_hbm": value / hbm,

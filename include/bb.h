@@ -100,13 +100,20 @@ bb_status bb_status_sync(bb_handle* h, bb_stream_t stream);
 
 /* Tuning and test parameters (bb_set_param / bb_get_param). */
 enum {
-    BB_PARAM_SCHEDULER = 0,     /* 0: automatic (default): currently the flag kernel
-                                      for every pass (fastest measured);
+    BB_PARAM_SCHEDULER = 0,     /* 0: automatic (default): per pass, the group kernel
+                                      where at least 5 sweeps' columns fit shared
+                                      memory, else the flag kernel;
                                    1: one kernel launch per cycle;
                                    2: persistent flag kernel (one CTA per sweep, per-
                                       sweep progress counters) for every pass;
                                    3: group kernel (CTA per group of sweeps, columns in
-                                      shared memory) wherever one sweep fits, else 2  */
+                                      shared memory) wherever one sweep fits, else 2.
+                                   The group kernel moves columns with 16-byte bulk
+                                   copies: on a band whose base or column stride
+                                   (ldab * element size) is not a multiple of 16
+                                   bytes, bb_reduce runs it on a working copy
+                                   (allocated by the handle on first use, n x ldab
+                                   rounded up; copied in and back on the stream)   */
     BB_PARAM_TPB = 1,           /* threads per block, multiple of 32 in [32, 1024];
                                    0 = automatic (default)                              */
     BB_PARAM_MAX_CTAS = 2,      /* cap on the persistent grid; 0 = co-resident maximum  */
@@ -118,7 +125,9 @@ enum {
     BB_PARAM_TIMING = 7,        /* 1: record CUDA events around every pass launch, read
                                    back with bb_last_pass_ms (default 0)                */
     BB_PARAM_GROUP_SIZE = 8     /* sweeps per group of the group kernel: 0 = largest
-                                   that fits shared memory, at most 16 (default)        */
+                                   that fits shared memory, at most 13, or 5 when a
+                                   reflector of tw + 1 elements takes more than 68
+                                   bytes (default)                                      */
 };
 bb_status bb_set_param(bb_handle* h, int param, int64_t value);
 int64_t bb_get_param(const bb_handle* h, int param);

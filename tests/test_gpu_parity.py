@@ -10,6 +10,7 @@ Acceptance (the oracle runs in the same precision as the GPU path):
 """
 import numpy as np
 import pytest
+import torch
 
 import band_inputs as bi
 import banded_svd_stage_gb300 as bb
@@ -183,23 +184,86 @@ def test_reduce_host_matches_device():
     assert np.array_equal(d, d0) and np.array_equal(e, e0)
 
 
-def test_larger_ldab_and_untouched_rows():
+@pytest.mark.parametrize("sched", [bb.SCHED_AUTO, bb.SCHED_GROUP])
+@pytest.mark.parametrize("extra", [5, 3])
+def test_larger_ldab_and_untouched_rows(sched, extra):
+    # extra = 3: ldab = 68, a 16-byte column stride (group kernel in place);
+    # extra = 5: ldab = 70, not one (group kernel on an aligned working copy)
     n, bw, tw = 500, 40, 12
-    band = bi.make_band(n, bw, tw, "f64", "normal", seed=3, ldab=bw + 2 * tw + 1 + 5)
+    band = bi.make_band(n, bw, tw, "f64", "normal", seed=3, ldab=bw + 2 * tw + 1 + extra)
     band[:, bw + 2 * tw + 1:] = 7.0  # rows beyond ku + tw must not be touched
-    d, e, after = gpu_reduce(band, n, bw, tw, "f64", 0, return_band=True)
+    d, e, after = gpu_reduce(band, n, bw, tw, "f64", sched, return_band=True)
     assert np.all(after[:, bw + 2 * tw + 1:] == 7.0)
     inner = np.ascontiguousarray(band[:, : bw + 2 * tw + 1])
     d_ref, e_ref = oracle.bidiagonal(inner, n, bw, tw)
     assert_parity(d, e, d_ref, e_ref, inner, n, bw, tw, "f64")
 
 
-def test_garbage_in_fill_rows_is_cleared():
+@pytest.mark.parametrize("sched", [bb.SCHED_AUTO, bb.SCHED_GROUP])
+def test_garbage_in_fill_rows_is_cleared(sched):
     n, bw, tw = 400, 30, 9
     band = bi.make_band(n, bw, tw, "f32", "normal", seed=8)
     clean = band.copy()
     band[:, :tw] = 123.0
     band[:, bw + tw + 1:] = -55.0
     d_ref, e_ref = oracle.bidiagonal(clean, n, bw, tw)
-    d, e = gpu_reduce(band, n, bw, tw, "f32", 0)
+    d, e = gpu_reduce(band, n, bw, tw, "f32", sched)
     assert_parity(d, e, d_ref, e_ref, clean, n, bw, tw, "f32")
+
+
+@pytest.mark.parametrize("dt", ["f32", "f64"])
+def test_group_kernel_on_unaligned_band_pointer(dt):
+    # a band that starts 4 bytes past a 16-byte boundary with a 16-byte
+    # aligned column stride: the group kernel must not take it in place
+    n, bw, tw = 600, 24, 8
+    q = 4 if dt == "f32" else 2
+    ld = (bw + 2 * tw + 1 + q - 1) // q * q
+    band = bi.make_band(n, bw, tw, dt, "normal", seed=12, ldab=ld)
+    d_ref, e_ref = oracle.bidiagonal(np.ascontiguousarray(band[:, : bw + 2 * tw + 1]), n, bw, tw)
+    dev = torch.device("cuda:0")
+    flat = torch.zeros(n * ld + 1, dtype=torch.float32 if dt == "f32" else torch.float64, device=dev)
+    x = flat[1:].view(n, ld)
+    x.copy_(torch.from_numpy(band))
+    assert x.data_ptr() % 16 != 0
+    d = torch.empty(n, dtype=x.dtype, device=dev)
+    e = torch.empty(n - 1, dtype=x.dtype, device=dev)
+    h = bb.bb_create(n, bw, bb.dtype_code(dt))
+    try:
+        bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, bb.SCHED_GROUP)
+        s = torch.cuda.current_stream(dev)
+        bb.bb_reduce(h, x, ld, tw, d, e, s)
+        assert bb.bb_status_sync(h, s) == bb.BB_OK
+        assert 3 in [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))]
+    finally:
+        bb.bb_destroy(h)
+    assert flat[0].item() == 0.0  # nothing written before the band
+    inner = np.ascontiguousarray(band[:, : bw + 2 * tw + 1])
+    assert_parity(d.cpu().numpy(), e.cpu().numpy(), d_ref, e_ref, inner, n, bw, tw, dt)
+
+
+def test_automatic_scheduler_choice():
+    # automatic: the group kernel for passes where >= 5 sweeps' columns fit
+    # shared memory (every pass of the n = 4096, bw = 16 workload), the flag
+    # kernel for the wide passes of the n = 16384, bw = 128 f64 workload
+    for idx, want in ((1, [3, 3]), (3, None)):
+        w = bi.WORKLOADS[idx]
+        n = w.n if idx == 1 else 2048
+        band = bi.make_band(n, w.bw, w.tw, w.dtype, w.dist, w.graded, w.seed)
+        dev = torch.device("cuda:0")
+        x = torch.from_numpy(band).to(dev)
+        d = torch.empty(n, dtype=x.dtype, device=dev)
+        e = torch.empty(n - 1, dtype=x.dtype, device=dev)
+        h = bb.bb_create(n, w.bw, bb.dtype_code(w.dtype))
+        try:
+            s = torch.cuda.current_stream(dev)
+            bb.bb_reduce(h, x, band.shape[1], w.tw, d, e, s)
+            assert bb.bb_status_sync(h, s) == bb.BB_OK
+            kernels = [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))]
+            groups = [bb.bb_last_pass_group(h, i) for i in range(bb.bb_last_num_passes(h))]
+        finally:
+            bb.bb_destroy(h)
+        if want is not None:
+            assert kernels == want
+        for k, g in zip(kernels, groups):
+            assert (k == 3 and g >= 5) or k == 2, (kernels, groups)
+        assert kernels[0] == 2 if idx == 3 else True
