@@ -395,16 +395,19 @@ __device__ __forceinline__ void copy_columns(const T* __restrict__ base, long lo
     }
 }
 
+// after_barrier: a block barrier has followed right_post (the publication
+// of the right half-step), so the square is in the tile already; the threads
+// not busy with the fence start the column copies at once.
 template <typename T, int WMAX, bool FULL>
 __device__ __forceinline__ void left_pre(T* __restrict__ band, const PassArgs& P, int r, int k,
-                                         const Smem<T>& sm) {
+                                         const Smem<T>& sm, bool after_barrier = false) {
     constexpr int NPL = (WMAX + 31) / 32;
     const StepGeom g = step_geom(P, r, k);
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
     const long long stride = P.ldab - 1;
     T* __restrict__ base = band + P.ku;
-    __syncthreads();  // the right half-step's rows are in the tile
+    if (!after_barrier) __syncthreads();  // the right half-step's rows are in the tile
     const int jlate = (int)min((long long)g.ncol, max((long long)W, late_col(P, g.c) - g.c));
     copy_columns<T, WMAX, FULL>(base, stride, g, W, jlate, sm);
     cp_async_commit();
@@ -528,9 +531,11 @@ __device__ __forceinline__ bool block_wait(const int* flag, int target, int* sta
 
 // Publish "this sweep has completed `value` half-steps": every thread's
 // stores are ordered before the flag by the barrier and a gpu-scope fence.
+// The first thread of the last warp fences, so warp 0 (which builds the next
+// reflector) goes on at once.
 __device__ __forceinline__ void block_publish(int* flag, int value) {
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == blockDim.x - 32) {
         __threadfence();
         st_release_gpu(flag, value);
     }
@@ -563,8 +568,8 @@ __device__ __forceinline__ bool persistent_step(T* __restrict__ band, const Pass
     const bool pre = right_pre<T, WMAX, FULL>(band, P, r, k, sm);
     if (r > 0 && !block_wait(progress + r - 1, min(2 * k + P.lagh, Hprev), status, P, s_flag)) return false;
     right_post<T, WMAX, FULL>(band, P, r, k, sm, pre);
-    if (publish) block_publish(progress + r, 2 * k + 1);
-    left_pre<T, WMAX, FULL>(band, P, r, k, sm);
+    block_publish_if(progress + r, 2 * k + 1, publish);
+    left_pre<T, WMAX, FULL>(band, P, r, k, sm, true);
     if (r > 0 && !block_wait(progress + r - 1, min(2 * k + 1 + P.lagh, Hprev), status, P, s_flag))
         return false;
     left_post<T, WMAX, FULL>(band, P, r, k, sm);

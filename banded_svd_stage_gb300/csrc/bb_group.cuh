@@ -85,24 +85,18 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
     const int s0 = cb.slot(g.c);
-    // A(i, c+m) = cb.cols[idx[m] + (i - p)] with idx[m] = slot(c+m) lds + off + p - (c+m)
-    int idx[WMAX];
-    {
-        int sl = s0;
-#pragma unroll
-        for (int m = 0; m < WMAX; ++m) {
-            if (m < W) idx[m] = sl * cb.lds + cb.off + (g.p - g.c - m);
-            sl = (sl + 1 == cb.nslot) ? 0 : sl + 1;
-        }
-    }
+    // A(p + i, c + m) = cb.cols[a0 + i + m (lds - 1) - (m >= mwrap ? nslot lds : 0)]:
+    // column c + m sits in slot s0 + m, wrapped once past the end
+    const int a0 = s0 * cb.lds + cb.off + (g.p - g.c);
+    const int dm = cb.lds - 1;
+    const int mwrap = cb.nslot - s0;
+    const int wrap = cb.nslot * cb.lds;
     T xp[NPL];
     int xo[NPL];
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        int sl = s0 + m;
-        if (sl >= cb.nslot) sl -= cb.nslot;
-        xo[q] = sl * cb.lds + cb.off + (g.p - g.c - m);
+        xo[q] = a0 + m * dm - ((m >= mwrap) ? wrap : 0);
         xp[q] = (m < W) ? cb.cols[xo[q]] : T(0);
     }
     T beta = warp_larfg<T, NPL>(xp, W, lane, vb, taub);
@@ -117,18 +111,19 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
     const T* v = vb;
     const int nrows = g.ce - g.p;
     for (int i = 1 + lane; i <= nrows; i += 32) {
+        const int a = a0 + i;
         T x[WMAX];
         T y = 0;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
-                x[m] = cb.cols[idx[m] + i];
+                x[m] = cb.cols[a + m * dm - ((m >= mwrap) ? wrap : 0)];
                 y = fma(x[m], v[m], y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) cb.cols[idx[m] + i] = fma(-s, v[m], x[m]);
+            if (m < W) cb.cols[a + m * dm - ((m >= mwrap) ? wrap : 0)] = fma(-s, v[m], x[m]);
     }
 }
 

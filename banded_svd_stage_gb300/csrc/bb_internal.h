@@ -59,7 +59,10 @@ constexpr long long kGroupMaxN = 1LL << 30;
 
 // Largest group size the group kernel is compiled for (GroupMaxWarps, minus
 // the loader, storer and publisher warps).
-inline int group_max_warps(int wmax, size_t elem) { return ((wmax * (int)elem <= 17 * 4) ? 16 : 8) - 3; }
+inline int group_max_warps(int wmax, size_t elem) {
+    const int b = wmax * (int)elem;
+    return (b <= 17 * 4 ? 16 : 8) - 3;
+}
 
 // Fewest sweeps per group for which the automatic scheduler prefers the
 // group kernel: with fewer, the per-group hand-over (a few ticks) is shared
