@@ -517,6 +517,10 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
         ga.top = (P.ku - P.b - P.t) / q * q;
         ga.lds = (P.ku + P.t + 1 - ga.top + q - 1) / q * q;
         ga.ahead = kGroupAhead;
+        // wide columns go back with bulk copies (one instruction a column);
+        // narrow ones with plain copies, which spare the compute warps a
+        // proxy fence every tick
+        ga.bulk_store = ((size_t)ga.lds * elem >= 256) ? 1 : 0;
         ga.nslot = std::max(1, group_footprint(P, g, ga.ahead));
         if (group_smem_bytes(ga, wmax, elem) > budget) break;
         best = ga;

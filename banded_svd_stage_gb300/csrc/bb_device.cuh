@@ -119,6 +119,32 @@ __device__ __forceinline__ T warp_tail_norm(const T (&x)[NPL], int w, int lane) 
 template <typename T, int NPL>
 __device__ __forceinline__ T warp_larfg(T (&x)[NPL], int w, int lane, T* s_v, T* s_tau) {
     T alpha = __shfl_sync(0xffffffffu, x[0], 0);
+    // Fast path: the plain sum of squares is in range, so
+    // beta = -sign(alpha) sqrt(alpha^2 + ||x||^2) with one square root (the
+    // same norm as below up to rounding; beta then exceeds safmin).
+    {
+        T ss = 0;
+#pragma unroll
+        for (int q = 0; q < NPL; ++q) {
+            const int m = lane + 32 * q;
+            if (m >= 1 && m < w) ss = fma(x[q], x[q], ss);
+        }
+        ss = warp_sum(ss);
+        const T s2 = fma(alpha, alpha, ss);
+        if (w > 1 && isfinite(s2) && ss >= Lim<T>::min_normal()) {
+            const T nrm = dev_sqrt(s2);
+            const T beta = (alpha >= T(0)) ? -nrm : nrm;
+            const T tau = (beta - alpha) / beta;
+            const T scal = T(1) / (alpha - beta);
+#pragma unroll
+            for (int q = 0; q < NPL; ++q) {
+                const int m = lane + 32 * q;
+                if (m < w) s_v[m] = (m == 0) ? T(1) : x[q] * scal;
+            }
+            if (lane == 0) *s_tau = tau;
+            return beta;
+        }
+    }
     T xnorm = (w > 1) ? warp_tail_norm<T, NPL>(x, w, lane) : T(0);
     if (xnorm == T(0)) {
 #pragma unroll

@@ -36,6 +36,8 @@ struct GroupArgs {
     int lds;      // rows a buffered column holds = stride between buffered columns
                   // (a multiple of 16 bytes / element, so lds - 1 is odd)
     int ahead;    // ticks the loader may run ahead of the storer (1 .. kMaxStages - 2)
+    int bulk_store;  // 1: the storer writes columns back with bulk copies (wide
+                     // columns); 0: with plain 16-byte copies (narrow columns)
 };
 
 // Last column touched by half-step h (right: 2k, left: 2k+1) of sweep r.
@@ -431,7 +433,8 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 const int h = tau - L * warp;
                 if (!s_dead && h >= 0 && h < my_h_end) {
                     group_half<T, WMAX>(P, cb, r0 + warp, h, vbuf + (size_t)warp * WMAX, taubuf + warp);
-                    fence_proxy_async_smem();  // the storer's bulk copies read these columns
+                    // the storer's bulk copies read these columns through the async proxy
+                    if (GA.bulk_store) fence_proxy_async_smem();
                 }
                 named_bar_sync(1, 32 * GA.g);
                 if (s_dead) break;  // read after the barrier: same tick for every compute warp
@@ -500,6 +503,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
             bool stopped = false;
             int stage = (int)(T0 % (unsigned)S);
             unsigned phase = (T0 / (unsigned)S) & 1u;
+            const int nv = (int)(col_bytes / 16);
             for (int v = 0; v < tend; ++v) {
                 if (!mbar_wait(&s_done[stage], phase, inner_budget, &s_abort_tick, v, &s_dead)) {
                     if (lane == 0 && s_abort_tick > v && !s_dead) {  // no abort announced: a lost signal
@@ -516,18 +520,44 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 xr = max(xr, tick_max_col(P, r0, ng, L, s_nsteps, v));
                 long long an = (v == tend - 1) ? (long long)P.n : tick_min_col(P, r0, ng, L, s_nsteps, v + 1);
                 an = min(an, xr + 1);
-                if (an > A) {
-                    for (int j = (int)A + lane; j < (int)an; j += 32)
-                        bulk_store(band + (long long)j * P.ldab + GA.top, cb.col(j), col_bytes);
-                    A = an;
+                if (GA.bulk_store) {
+                    if (an > A) {
+                        for (int j = (int)A + lane; j < (int)an; j += 32)
+                            bulk_store(band + (long long)j * P.ldab + GA.top, cb.col(j), col_bytes);
+                        A = an;
+                    }
+                    bulk_commit();
+                    bulk_wait_read();  // sources read: the slots may be refilled
+                    // columns written back in earlier iterations are complete once
+                    // only this iteration's group may still be pending: report
+                    // them (one iteration late, so the wait rarely stalls)
+                    bulk_wait_prev();
+                    fence_proxy_async_global();
+                } else {
+                    if (an > A) {
+                        // element e of the range: vector e mod nv of column A + e / nv
+                        const int total = (int)(an - A) * nv;
+                        const int dq = 32 / nv, dr = 32 % nv;
+                        int jc = lane / nv, vq = lane % nv;
+                        for (int e = lane; e < total; e += 32) {
+                            const int j = (int)A + jc;
+                            const int4* src = reinterpret_cast<const int4*>(cb.col(j));
+                            int4* dst = reinterpret_cast<int4*>(band + (long long)j * P.ldab + GA.top);
+                            dst[vq] = src[vq];
+                            jc += dq;
+                            vq += dr;
+                            if (vq >= nv) {
+                                vq -= nv;
+                                ++jc;
+                            }
+                        }
+                        A = an;
+                    }
+                    a_prev = (int)A;  // plain stores: reported at once (the publisher fences)
+                    // these reads of the freed slots come before the loader's bulk
+                    // writes into them
+                    fence_proxy_async_smem();
                 }
-                bulk_commit();
-                bulk_wait_read();  // sources read: the slots may be refilled
-                // columns written back in earlier iterations are complete once
-                // only this iteration's group may still be pending: publish them
-                // (one iteration late, so the wait rarely stalls)
-                bulk_wait_prev();
-                fence_proxy_async_global();
                 __syncwarp();
                 if (lane == 0) {
                     st_release_cta_shared(&s_freed, (int)A);
@@ -536,8 +566,10 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 }
                 a_prev = (int)A;
             }
-            bulk_wait_all();
-            fence_proxy_async_global();
+            if (GA.bulk_store) {
+                bulk_wait_all();
+                fence_proxy_async_global();
+            }
             __syncwarp();
             if (lane == 0 && !stopped) st_release_cta_shared(&s_written, (int)P.n);
         } else if (warp == GA.g + 2) {
