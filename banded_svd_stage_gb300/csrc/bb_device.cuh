@@ -556,15 +556,13 @@ __device__ __forceinline__ bool block_wait(const int* flag, int target, int* sta
 }
 
 // Publish "this sweep has completed `value` half-steps": every thread's
-// stores are ordered before the flag by the barrier and a gpu-scope fence.
-// The first thread of the last warp fences, so warp 0 (which builds the next
+// stores are ordered before the flag by the barrier and the release store,
+// which is cumulative over what the barrier ordered before it.  The first
+// thread of the last warp releases, so warp 0 (which builds the next
 // reflector) goes on at once.
 __device__ __forceinline__ void block_publish(int* flag, int value) {
     __syncthreads();
-    if (threadIdx.x == blockDim.x - 32) {
-        __threadfence();
-        st_release_gpu(flag, value);
-    }
+    if (threadIdx.x == blockDim.x - 32) st_release_gpu(flag, value);
 }
 
 __device__ __forceinline__ void block_publish_if(int* flag, int value, bool publish) {

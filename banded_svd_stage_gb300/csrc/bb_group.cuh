@@ -438,7 +438,8 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 }
                 named_bar_sync(1, 32 * GA.g);
                 if (s_dead) break;  // read after the barrier: same tick for every compute warp
-                if (threadIdx.x == 0) mbar_arrive(&s_done[stage]);
+                // the last compute warp signals, so warp 0 (the front sweep) goes on at once
+                if (threadIdx.x == 32 * (GA.g - 1)) mbar_arrive(&s_done[stage]);
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
@@ -581,10 +582,9 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 for (;;) {
                     const int a = ld_acquire_cta_shared(&s_written);
                     if (a > published) {
-                        if (publish) {
-                            __threadfence();
-                            st_release_gpu(wm + G, a);
-                        }
+                        // release: cumulative over the storer's writes, which the
+                        // acquire of s_written ordered before it
+                        if (publish) st_release_gpu(wm + G, a);
                         published = a;
                         if (a >= P.n) break;
                         t0 = clock64();
