@@ -275,11 +275,15 @@ __device__ __forceinline__ long long late_col(const PassArgs& P, long long c) {
 // ---------------------------------------------------------------------------
 
 // Copy rows [i0, i1) (local: row p + 1 + i) of the right block into rtile.
+// Row i is always copied by thread i mod blockDim.x, the thread that applies
+// the reflector to it, so a thread needs only its own copies to be complete.
 template <typename T, int WMAX, bool FULL>
 __device__ __forceinline__ void copy_rows(const T* __restrict__ base, long long stride, const StepGeom& g,
                                           int i0, int i1, const Smem<T>& sm) {
     const int W = FULL ? WMAX : g.w;
-    for (int i = i0 + (int)threadIdx.x; i < i1; i += blockDim.x) {
+    const int nthr = blockDim.x;
+    const int first = i0 + (((int)threadIdx.x - i0 % nthr) + nthr) % nthr;
+    for (int i = first; i < i1; i += nthr) {
         const T* src = base + (g.p + 1 + i) + g.c * stride;
         T* dst = sm.rtile + i * sm.wp;
 #pragma unroll
@@ -351,7 +355,10 @@ __device__ __forceinline__ void right_post(T* __restrict__ band, const PassArgs&
     }
     cp_async_commit();
     cp_async_wait_all();
-    __syncthreads();
+    // With the reflector built before the wait (pre), every thread applies it
+    // to the rows it copied itself: no barrier.  Otherwise warp 0 has just
+    // built it.
+    if (!pre) __syncthreads();
     const T tau = *sm.tau;
     const int row_c = (int)(g.c - g.p - 1);  // local index of row c
     for (int i = tid; i < g.nrows; i += nthr) {
@@ -590,7 +597,12 @@ __device__ __forceinline__ bool persistent_step(T* __restrict__ band, const Pass
                                                 int K, int Hprev, bool publish, int* __restrict__ progress,
                                                 int* __restrict__ status, const Smem<T>& sm, int* s_flag) {
     const bool pre = right_pre<T, WMAX, FULL>(band, P, r, k, sm);
-    if (r > 0 && !block_wait(progress + r - 1, min(2 * k + P.lagh, Hprev), status, P, s_flag)) return false;
+    // the wait's barrier (or this one for sweep 0) publishes warp 0's reflector
+    if (r > 0) {
+        if (!block_wait(progress + r - 1, min(2 * k + P.lagh, Hprev), status, P, s_flag)) return false;
+    } else {
+        __syncthreads();
+    }
     right_post<T, WMAX, FULL>(band, P, r, k, sm, pre);
     block_publish_if(progress + r, 2 * k + 1, publish);
     left_pre<T, WMAX, FULL>(band, P, r, k, sm, true);
