@@ -587,7 +587,7 @@ __device__ __forceinline__ void block_publish_if(int* flag, int value, bool publ
 // addressing state, so the block size is capped to leave it the registers.
 template <typename T, int WMAX>
 struct MaxThreads {
-    static constexpr int value = (WMAX * sizeof(T) <= 17 * 4) ? 512 : ((WMAX * sizeof(T) <= 33 * 4) ? 384 : 256);
+    static constexpr int value = (WMAX * sizeof(T) <= 17 * 4) ? 512 : 256;
 };
 
 // One step (right then left half-step) of sweep r under the persistent
