@@ -5,13 +5,15 @@
 // tau, L being the same half-step lag as the progress protocol of the
 // persistent scheduler (2, 3 or 4).  Half-steps of one tick touch disjoint
 // windows and overlapping half-steps of different sweeps run in sweep order
-// (exhaustive check of the lockstep schedule), so a tick is one CTA barrier.
+// (exhaustive check of the lockstep schedule; for b - t = 1 a lag of 4 is
+// also the least that works), so a tick is one barrier of the compute warps.
 // Each sweep of the group is run by one warp.
 //
 // Between groups, whole columns change hands.  A group keeps the columns
 // [A, B] of the band in a circular buffer of shared memory: a column is
-// copied in (all b + 2t + 1 rows of the pass) the first time the group needs
-// it, and written back once no sweep of the group will touch it again.  A
+// copied in (rows ku-b-t .. ku+t of the pass, rounded out to 16 bytes) the
+// first time the group needs it, and written back once no sweep of the group
+// will touch it again.  A
 // group publishes its watermark A, the first column it may still touch; the
 // next group copies a column in only when the previous group's watermark is
 // beyond it, so at any time each column belongs to at most one group, and
@@ -205,10 +207,6 @@ __device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned coun
 __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
                  : "memory");
-}
-// Arrives once every cp.async this thread issued so far has landed.
-__device__ __forceinline__ void mbar_arrive_cp_async(unsigned long long* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned parity) {
     unsigned ok;
