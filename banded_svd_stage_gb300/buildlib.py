@@ -82,11 +82,13 @@ if __name__ == "__main__":
 
 
 def source_digest() -> str:
-    """sha256 of the CUDA sources and the C header (identifies a kernel build)."""
+    """sha256 of the library's CUDA sources under csrc/ (identifies a kernel
+    build; the public header's documentation does not change the kernels)."""
     import hashlib
     h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
     for f in sorted(_deps()):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f.endswith((".cu", ".cuh", ".h")) and os.path.abspath(f).startswith(csrc + os.sep):
             h.update(os.path.basename(f).encode())
             with open(f, "rb") as fh:
                 h.update(fh.read())

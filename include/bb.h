@@ -58,8 +58,10 @@ typedef enum {
 /* A cudaStream_t, passed as a plain pointer (NULL = the legacy default stream). */
 typedef void* bb_stream_t;
 
-/* Opaque handle: owns the per-sweep progress counters (n int32), a device
- * status word, and (only after bb_reduce_host) staging buffers. */
+/* Opaque handle: owns the per-sweep progress counters (n int32; the group
+ * kernel keeps one watermark per group there), a device status word, and,
+ * once needed, staging buffers (bb_reduce_host) and a working copy of the
+ * band (see BB_PARAM_SCHEDULER). */
 typedef struct bb_handle bb_handle;
 
 /* Create a handle for n x n matrices of upper bandwidth bw (0 <= bw < n) and
@@ -73,8 +75,12 @@ bb_handle* bb_create(int64_t n, int64_t bw, bb_dtype dtype);
  * tw: entries annihilated per reflector, 1 <= tw <= max(1, bw - 1), tw <= 64.
  * Stream-ordered and asynchronous: the return code covers argument checks and
  * launch errors only.  A device-side failure (a progress wait that ran out of
- * its budget) is latched in the handle's status word and reported by
- * bb_status_sync.  Covers the paper's Algorithms 1 and 2 (Section III). */
+ * its budget, or BB_ERR_INTERNAL from a consistency check) is latched in the
+ * handle's status word and reported by bb_status_sync.  When a pass runs on
+ * the group kernel and the band's base or column stride is not a multiple of
+ * 16 bytes, the first such call allocates the handle's working copy (n x ldab
+ * rounded up to 16 bytes; BB_ERR_NOMEM if that fails).  Covers the paper's
+ * Algorithms 1 and 2 (Section III). */
 bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
                     void* e_out, bb_stream_t stream);
 
