@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "BB_OK", 1: "BB_ERR_INVALID_ARG", 2: "BB_ERR_LDAB", 3: "BB_ER
 BB_ERR_INTERNAL = 7
 STATUS_NAMES[7] = "BB_ERR_INTERNAL"
 # scheduler values
-SCHED_AUTO, SCHED_CYCLE, SCHED_FLAGS, SCHED_GROUP = 0, 1, 2, 3
+SCHED_AUTO, SCHED_CYCLE, SCHED_FLAGS, SCHED_GROUP, SCHED_CYCLE_GRAPH = 0, 1, 2, 3, 4
 
 
 class BBError(RuntimeError):

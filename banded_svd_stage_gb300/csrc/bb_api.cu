@@ -89,6 +89,17 @@ struct bb_handle {
     // kernel on a caller layout its bulk copies cannot address)
     void* work = nullptr;
     size_t work_bytes = 0;
+    // scheduler 4: per-cycle launches of each pass captured once in a CUDA
+    // graph (on a stream of the handle) and replayed on the caller's stream
+    struct PassGraph {
+        const void* band = nullptr;
+        int64_t ldab = 0, n = 0;
+        int b = 0, t = 0, tpb = 0;
+        int64_t launches = 0;
+        cudaGraphExec_t exec = nullptr;
+    };
+    std::vector<PassGraph> graphs;  // by pass index
+    cudaStream_t capture_stream = nullptr;
     // statistics of the last reduction
     int64_t last_launches = 0;
     std::vector<cudaEvent_t> ev;  // 2 per pass
@@ -180,6 +191,9 @@ void bb_destroy(bb_handle* h) {
     if (h->s_band) cudaFree(h->s_band);
     if (h->s_de) cudaFree(h->s_de);
     if (h->work) cudaFree(h->work);
+    for (auto& pg : h->graphs)
+        if (pg.exec) cudaGraphExecDestroy(pg.exec);
+    if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
     for (auto ev : h->ev) cudaEventDestroy(ev);
     delete h;
 }
@@ -188,7 +202,7 @@ bb_status bb_set_param(bb_handle* h, int param, int64_t value) {
     if (!h) return fail(BB_ERR_INVALID_ARG, "bb_set_param: null handle");
     switch (param) {
         case BB_PARAM_SCHEDULER:
-            if (value < 0 || value > 3) return fail(BB_ERR_INVALID_ARG, "scheduler must be 0, 1, 2 or 3");
+            if (value < 0 || value > 4) return fail(BB_ERR_INVALID_ARG, "scheduler must be 0, 1, 2, 3 or 4");
             h->scheduler = (int)value;
             return BB_OK;
         case BB_PARAM_TPB:
@@ -306,6 +320,59 @@ static bb_status check_reduce_args(bb_handle* h, int64_t ldab, int64_t tw) {
     return BB_OK;
 }
 
+// Scheduler 4: the per-cycle launches of pass pi, captured into a CUDA graph
+// the first time (and again whenever the band, ldab or the pass changes),
+// then replayed on stream s with one graph launch.  Capture runs on a stream
+// of the handle, since the caller's stream may be the legacy default stream.
+template <typename T>
+static cudaError_t run_pass_graph(bb_handle* h, int64_t pi, T* band, int64_t ldab, const bb::PassArgs& P,
+                                  const bb::LaunchCfg& cfg, cudaStream_t s, bb::LaunchStats* st) {
+    cudaError_t err;
+    if ((int64_t)h->graphs.size() <= pi) h->graphs.resize((size_t)pi + 1);
+    bb_handle::PassGraph& pg = h->graphs[(size_t)pi];
+    const bool hit = pg.exec && pg.band == band && pg.ldab == ldab && pg.n == P.n && pg.b == P.b &&
+                     pg.t == P.t && pg.tpb == cfg.tpb;
+    if (!hit) {
+        if (pg.exec) {
+            cudaGraphExecDestroy(pg.exec);
+            pg.exec = nullptr;
+        }
+        if (!h->capture_stream) {
+            err = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking);
+            if (err != cudaSuccess) return err;
+        }
+        bb::LaunchStats cs;
+        err = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeRelaxed);
+        if (err != cudaSuccess) return err;
+        cudaError_t lerr = bb::run_pass<T>(band, P, 1, cfg, h->d_progress, h->d_status, h->capture_stream, &cs);
+        cudaGraph_t graph = nullptr;
+        err = cudaStreamEndCapture(h->capture_stream, &graph);
+        if (lerr != cudaSuccess || err != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            return lerr != cudaSuccess ? lerr : err;
+        }
+        err = cudaGraphInstantiate(&pg.exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (err != cudaSuccess) {
+            pg.exec = nullptr;
+            return err;
+        }
+        pg.band = band;
+        pg.ldab = ldab;
+        pg.n = P.n;
+        pg.b = P.b;
+        pg.t = P.t;
+        pg.tpb = cfg.tpb;
+        pg.launches = cs.launches;
+    }
+    err = cudaGraphLaunch(pg.exec, s);
+    if (st) {
+        st->launches += pg.launches;  // kernels the graph runs
+        st->kernel = 4;
+    }
+    return err;
+}
+
 template <typename T>
 static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T* d, T* e,
                              cudaStream_t s) {
@@ -383,7 +450,11 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         cfg.group_size = h->group_size;
         bb::LaunchStats st;
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo)], s);
-        err = bb::run_pass<T>(wb, P, h->scheduler, cfg, h->d_progress, h->d_status, s, &st);
+        if (h->scheduler == 4) {
+            err = run_pass_graph<T>(h, pi, wb, ldw, P, cfg, s, &st);
+        } else {
+            err = bb::run_pass<T>(wb, P, h->scheduler, cfg, h->d_progress, h->d_status, s, &st);
+        }
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo) + 1], s);
         h->last_launches += st.launches;
         if (err != cudaSuccess) return cuda_fail(err, "pass launch");

@@ -33,7 +33,7 @@ struct LaunchCfg {
 struct LaunchStats {
     int64_t launches = 0;  // kernel launches issued
     int grid = 0;          // persistent grid of the last pass
-    int kernel = 0;        // 1 per-cycle, 2 flag kernel, 3 group kernel
+    int kernel = 0;        // 1 per-cycle, 2 flag kernel, 3 group kernel, 4 per-cycle graph
     int group = 0;         // sweeps per group (group kernel)
 };
 

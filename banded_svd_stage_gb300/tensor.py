@@ -61,7 +61,8 @@ class Reducer:
         return [bb_last_pass_ms(self.h, i) for i in range(bb_last_num_passes(self.h))]
 
     def pass_kernels(self):
-        """[(kernel, group size), ...] of the last reduction: 1 per-cycle, 2 flags, 3 group."""
+        """[(kernel, group size), ...] of the last reduction: 1 per-cycle, 2 flags, 3 group,
+        4 per-cycle launches replayed from a CUDA graph."""
         from . import bb_last_pass_group, bb_last_pass_kernel
         return [(bb_last_pass_kernel(self.h, i), bb_last_pass_group(self.h, i))
                 for i in range(bb_last_num_passes(self.h))]

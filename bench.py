@@ -1,7 +1,7 @@
 """Benchmark of the band -> bidiagonal reduction on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--scheduler 0|1|2|3] [--no-sweep]
+                    [--workload NAME] [--scheduler 0|1|2|3|4] [--no-sweep]
 
 One step is one whole reduction (every pass down to bidiagonal form, plus the
 fill-row zeroing and the d/e extraction) of one synthetic band.  Before each
@@ -270,8 +270,9 @@ def _model_bytes_py(w):
     return tot
 
 
-KERNEL_NAMES = {1: "pass_cycle_kernel", 2: "pass_persistent_kernel", 3: "pass_group_kernel"}
-SCHEDULER_NAMES = {0: "auto", 1: "per-cycle", 2: "flags", 3: "group"}
+KERNEL_NAMES = {1: "pass_cycle_kernel", 2: "pass_persistent_kernel", 3: "pass_group_kernel",
+                4: "pass_cycle_kernel"}
+SCHEDULER_NAMES = {0: "auto", 1: "per-cycle", 2: "flags", 3: "group", 4: "per-cycle-graph"}
 
 
 def dominant_kernel(res):
@@ -287,7 +288,7 @@ def dominant_kernel(res):
         return None, None, 0, 0.0, 0.0
     kind = max(tot, key=lambda k: tot[k][0])
     ms, by, nl = tot[kind]
-    if kind == 1:
+    if kind in (1, 4):
         nl = None  # one launch per cycle: many launches per pass
     ach = by / (ms * 1e-3) / 1e9 if ms > 0 else None
     return KERNEL_NAMES.get(kind, str(kind)), ach, nl if nl else 0, by, ms

@@ -113,7 +113,12 @@ enum {
                                    2: persistent flag kernel (one CTA per sweep, per-
                                       sweep progress counters) for every pass;
                                    3: group kernel (CTA per group of sweeps, columns in
-                                      shared memory) wherever one sweep fits, else 2.
+                                      shared memory) wherever one sweep fits, else 2;
+                                   4: as 1, with each pass's launches captured once in
+                                      a CUDA graph (on a stream of the handle) and
+                                      replayed on the caller's stream; the graph is
+                                      kept by the handle and captured again when the
+                                      band pointer, ldab or the pass changes.
                                    The group kernel moves columns with 16-byte bulk
                                    copies: on a band whose base or column stride
                                    (ldab * element size) is not a multiple of 16
@@ -158,8 +163,10 @@ int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass);
 int64_t bb_last_launches(const bb_handle* h);
 
 /* Kernel that ran pass i of the last reduction: 1 per-cycle, 2 flag kernel,
- * 3 group kernel (-1 if out of range), and, for the group kernel, its group
- * size (sweeps per CTA; 0 otherwise). */
+ * 3 group kernel, 4 per-cycle launches replayed from a CUDA graph (-1 if out
+ * of range), and, for the group kernel, its group size (sweeps per CTA; 0
+ * otherwise).  With scheduler 4, bb_last_launches counts the kernels the
+ * graphs ran. */
 int64_t bb_last_pass_kernel(const bb_handle* h, int64_t i);
 int64_t bb_last_pass_group(const bb_handle* h, int64_t i);
 

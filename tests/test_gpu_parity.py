@@ -53,7 +53,7 @@ def assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler=0):
     return err
 
 
-SCHEDULERS = [bb.SCHED_AUTO, bb.SCHED_CYCLE, bb.SCHED_FLAGS, bb.SCHED_GROUP]
+SCHEDULERS = [bb.SCHED_AUTO, bb.SCHED_CYCLE, bb.SCHED_FLAGS, bb.SCHED_GROUP, bb.SCHED_CYCLE_GRAPH]
 
 
 @pytest.mark.parametrize("scheduler", SCHEDULERS)
@@ -267,3 +267,36 @@ def test_automatic_scheduler_choice():
         for k, g in zip(kernels, groups):
             assert (k == 3 and g >= 5) or k == 2, (kernels, groups)
         assert kernels[0] == 2 if idx == 3 else True
+
+
+def test_cycle_graph_reused_and_recaptured():
+    """Scheduler 4 replays the captured graph on a second call with the same
+    buffers, and captures again for another band buffer: all results equal
+    the plain per-cycle scheduler's bitwise."""
+    w = bi.WORKLOADS[1]
+    n = 1500
+    band = bi.make_band(n, w.bw, w.tw, w.dtype, w.dist, w.graded, w.seed)
+    ref = gpu_reduce(band, n, w.bw, w.tw, w.dtype, bb.SCHED_CYCLE)
+    dev = torch.device("cuda:0")
+    h = bb.bb_create(n, w.bw, bb.dtype_code(w.dtype))
+    try:
+        bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, bb.SCHED_CYCLE_GRAPH)
+        s = torch.cuda.current_stream(dev)
+        outs, launches = [], []
+        src = torch.from_numpy(band).to(dev)
+        x1 = torch.empty_like(src)
+        x2 = torch.empty_like(src)
+        for x in (x1, x1, x2):
+            x.copy_(src)
+            d = torch.empty(n, dtype=x.dtype, device=dev)
+            e = torch.empty(n - 1, dtype=x.dtype, device=dev)
+            bb.bb_reduce(h, x, band.shape[1], w.tw, d, e, s)
+            assert bb.bb_status_sync(h, s) == bb.BB_OK
+            outs.append((d.cpu().numpy(), e.cpu().numpy()))
+            launches.append(bb.bb_last_launches(h))
+            assert [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))] == [4, 4]
+    finally:
+        bb.bb_destroy(h)
+    for d, e in outs:
+        assert np.array_equal(d, ref[0]) and np.array_equal(e, ref[1])
+    assert launches[0] == launches[1] == launches[2] > 100
