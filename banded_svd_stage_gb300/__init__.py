@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             "bb_reduce_noalloc": ([p, i64, i64, i64, i64, ci, p, p, p], ci),
             "bb_last_pass_kernel": ([p, i64], i64),
             "bb_last_pass_group": ([p, i64], i64),
+            "bb_singular_values": ([ci, i64, p, p, p, p], ci),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -194,6 +195,12 @@ def bb_reduce_noalloc(band, n: int, bw: int, ldab: int, tw: int, dtype: int, d_o
     synchronizes the stream before returning."""
     _check(lib().bb_reduce_noalloc(_addr(band), n, bw, ldab, tw, dtype, _addr(d_out), _addr(e_out),
                                    _stream(stream)))
+
+
+def bb_singular_values(dtype: int, n: int, d, e, sigma_out, stream=None) -> None:
+    """Singular values of the bidiagonal (d, e), descending, into sigma_out
+    (device buffers; asynchronous on `stream`)."""
+    _check(lib().bb_singular_values(dtype, n, _addr(d), _addr(e), _addr(sigma_out), _stream(stream)))
 
 
 def dtype_code(dtype) -> int:

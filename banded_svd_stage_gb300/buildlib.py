@@ -17,7 +17,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
 LIB_PATH = os.path.join(HERE, "libbb.so")
 SOURCES = ["bb_api.cu", "bb_kernels_f32.cu", "bb_kernels_f64.cu", "bb_kernels_f32_narrow.cu",
-           "bb_kernels_f32_wide.cu", "bb_kernels_f64_narrow.cu", "bb_kernels_f64_wide.cu", "bb_noalloc.cu"]
+           "bb_kernels_f32_wide.cu", "bb_kernels_f64_narrow.cu", "bb_kernels_f64_wide.cu", "bb_noalloc.cu",
+           "bb_svals.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,136 @@
+// Singular values of an upper bidiagonal matrix (d, e) on the GPU: bisection
+// on Sturm counts of the 2n x 2n Golub-Kahan tridiagonal, one thread per
+// singular value.
+//
+// The Golub-Kahan matrix T has a zero diagonal and off-diagonal
+// a = (d_0, e_0, d_1, e_1, ..., e_{n-2}, d_{n-1}); its eigenvalues are the
+// +- sigma_i.  The number of eigenvalues of T below x is the number of
+// negative pivots of T - x I: q_0 = -x, q_i = -x - a_{i-1}^2 / q_{i-1}
+// (LAPACK xSTEBZ's count, with its pivmin guard: |q_i| < pivmin becomes
+// -pivmin).  For x > 0, #{sigma < x} = count(x) - n.  This is the step the
+// two-stage SVD takes right after the band -> bidiagonal reduction ("A
+// two-stage reduction on an Apple M5 Pro", Section 7, bisection for the
+// bidiagonal singular values); the GPU layout is this library's.
+//
+// Every thread runs the same number of bisection steps, so a block walks the
+// squared off-diagonal in shared-memory chunks in lockstep.  The entries are
+// first scaled by a power of two that brings the largest near 1.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "../../include/bb.h"
+
+namespace bb {
+
+void set_last_error(const char* msg);  // bb_api.cu
+
+template <typename T> struct SvLim;
+template <> struct SvLim<float> {
+    static __device__ __forceinline__ float safmin() { return 1.17549435e-38f; }
+    static constexpr int iters = 27;  // 2^-27 of the Gershgorin bound < eps/2 of it
+};
+template <> struct SvLim<double> {
+    static __device__ __forceinline__ double safmin() { return 2.2250738585072014e-308; }
+    static constexpr int iters = 56;
+};
+
+constexpr int kSvThreads = 128;
+constexpr int kSvChunk = 2048;  // squared off-diagonal entries per shared-memory chunk
+
+// sigma[k] = the k-th largest singular value (k = 0 .. n-1).
+template <typename T>
+__global__ void __launch_bounds__(kSvThreads)
+bidiag_svals_kernel(const T* __restrict__ d, const T* __restrict__ e, int n, T* __restrict__ sigma) {
+    __shared__ T s_a2[kSvChunk];
+    __shared__ T s_red[kSvThreads / 32];
+    const int m = 2 * n - 1;  // off-diagonal entries of T
+    // The largest |a_i|, each block on its own (one pass; the bisection
+    // makes tens of them).  The counts run on a * sc, sc the power of two
+    // that brings it near 1, so that the squares neither under- nor overflow
+    // (as LAPACK scales before bisecting); sigma = result / sc exactly.
+    T amax = 0;
+    for (int i = threadIdx.x; i < m; i += blockDim.x) amax = fmax(amax, fabs(i & 1 ? e[i >> 1] : d[i >> 1]));
+    for (int o = 16; o > 0; o >>= 1) amax = fmax(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0;
+    for (int w = 0; w < kSvThreads / 32; ++w) amax = fmax(amax, s_red[w]);
+    const T sc = (amax > T(0) && isfinite(amax)) ? ldexp(T(1), -ilogb(amax)) : T(1);
+    // Gershgorin bound of the scaled T: max over rows of |a_{i-1}| + |a_i|
+    T bound = 0;
+    for (int i = threadIdx.x; i <= m; i += blockDim.x) {
+        const T left = (i > 0) ? fabs((i - 1) & 1 ? e[(i - 1) >> 1] : d[(i - 1) >> 1]) : T(0);
+        const T right = (i < m) ? fabs(i & 1 ? e[i >> 1] : d[i >> 1]) : T(0);
+        bound = fmax(bound, (left + right) * sc);
+    }
+    for (int o = 16; o > 0; o >>= 1) bound = fmax(bound, __shfl_xor_sync(0xffffffffu, bound, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = bound;
+    __syncthreads();
+    bound = 0;
+    for (int w = 0; w < kSvThreads / 32; ++w) bound = fmax(bound, s_red[w]);
+    const T amax_s = amax * sc;
+    const T pivmin = SvLim<T>::safmin() * fmax(T(1), amax_s * amax_s);
+
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;  // k-th largest
+    const int j = n - 1 - k;                               // j-th smallest
+    T lo = 0, hi = bound * T(1.0000001) + pivmin;
+    for (int it = 0; it < SvLim<T>::iters; ++it) {
+        const T x = T(0.5) * (lo + hi);
+        T q = -x;
+        int cnt = (q < T(0)) ? 1 : 0;
+        for (int c0 = 0; c0 < m; c0 += kSvChunk) {
+            const int len = min(kSvChunk, m - c0);
+            __syncthreads();
+            for (int i = threadIdx.x; i < len; i += blockDim.x) {
+                const int g = c0 + i;
+                const T a = ((g & 1) ? e[g >> 1] : d[g >> 1]) * sc;
+                s_a2[i] = a * a;
+            }
+            __syncthreads();
+            for (int i = 0; i < len; ++i) {
+                q = -x - s_a2[i] / q;
+                if (fabs(q) < pivmin) q = -pivmin;
+                cnt += (q < T(0)) ? 1 : 0;
+            }
+        }
+        if (cnt - n > j) hi = x;
+        else lo = x;
+    }
+    if (k < n) sigma[k] = T(0.5) * (lo + hi) / sc;
+}
+
+}  // namespace bb
+
+extern "C" bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d, const void* e, void* sigma_out,
+                                        bb_stream_t stream) {
+    if (n < 1 || n > (int64_t)1 << 29) {
+        bb::set_last_error("bb_singular_values: n must be in [1, 2^29]");
+        return BB_ERR_INVALID_ARG;
+    }
+    if (!d || !sigma_out || (n > 1 && !e)) {
+        bb::set_last_error("bb_singular_values: null d, e or sigma_out");
+        return BB_ERR_INVALID_ARG;
+    }
+    if (dtype != BB_F32 && dtype != BB_F64) {
+        bb::set_last_error("bb_singular_values: unknown dtype");
+        return BB_ERR_DTYPE;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const unsigned grid = (unsigned)((n + bb::kSvThreads - 1) / bb::kSvThreads);
+    // e may be null for n == 1: the kernel never reads it then (m = 1)
+    if (dtype == BB_F32)
+        bb::bidiag_svals_kernel<float><<<grid, bb::kSvThreads, 0, s>>>(
+            (const float*)d, (const float*)e, (int)n, (float*)sigma_out);
+    else
+        bb::bidiag_svals_kernel<double><<<grid, bb::kSvThreads, 0, s>>>(
+            (const double*)d, (const double*)e, (int)n, (double*)sigma_out);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) {
+        bb::set_last_error(cudaGetErrorString(err));
+        return BB_ERR_CUDA;
+    }
+    return BB_OK;
+}

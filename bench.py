@@ -193,6 +193,45 @@ def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int,
     }
 
 
+def run_svals(w: bi.Workload, steps: int, warmup: int):
+    """Device time of bb_singular_values on the bidiagonal the library
+    produces for workload w (the step after the reduction), CUDA events on
+    the launching stream."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    dev = torch.device("cuda", torch.cuda.current_device())
+    band = torch.from_numpy(bi.make_workload(w)).to(dev)
+    d = torch.empty(w.n, dtype=band.dtype, device=dev)
+    e = torch.empty(max(w.n - 1, 1), dtype=band.dtype, device=dev)
+    sig = torch.empty(w.n, dtype=band.dtype, device=dev)
+    h = bb.bb_create(w.n, w.bw, bb.dtype_code(w.dtype))
+    stream = torch.cuda.current_stream(dev)
+    try:
+        bb.bb_reduce(h, band, band.shape[1], w.tw, d, e, stream)
+        if bb.bb_status_sync(h, stream) != bb.BB_OK:
+            raise RuntimeError("reduction failed")
+    finally:
+        bb.bb_destroy(h)
+    code = bb.dtype_code(w.dtype)
+    for _ in range(warmup):
+        bb.bb_singular_values(code, w.n, d, e, sig, stream)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        bb.bb_singular_values(code, w.n, d, e, sig, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+    ms = statistics.median(times)
+    return {"ms": ms, "n": w.n, "values_per_s": w.n / (ms * 1e-3), "kernel": "bidiag_svals_kernel",
+            "launches": 1, "method": "bisection on Sturm counts of the 2n Golub-Kahan tridiagonal, "
+                                     "one thread per singular value"}
+
+
 def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
     """bb_reduce_host from pinned host memory: H2D of the band, reduction, D2H
     of d and e, inside the timed region (host wall clock around the call,
@@ -403,6 +442,10 @@ def main():
                           "effective_gbs": g2, "frac_of_hbm": g2 / hbm,
                           "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"]})
 
+    svals = None
+    if rank == 0 and world == 1 and not args.no_sweep:
+        svals = run_svals(w, args.steps, args.warmup)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_oracle_rate(w)
@@ -425,6 +468,7 @@ def main():
             "pass_kernels": res["kernels"],
             "pass_ms": res["pass_ms_mean"],
             "per_workload": sweep,
+            "singular_values": svals,
         }
         print(json.dumps(line))
     if world > 1:

@@ -137,3 +137,32 @@ def bidiagonal(band: np.ndarray, n: int, bw: int, tw: int):
     work = np.ascontiguousarray(band.copy())
     reduce_band(work, n, bw, tw)
     return extract(work, n, bw + tw)
+
+
+def bidiagonal_singular_values(d: np.ndarray, e: np.ndarray) -> np.ndarray:
+    """Singular values of the upper bidiagonal matrix (d, e), descending, in
+    float64: by definition the non-negative eigenvalues of the 2n x 2n
+    Golub-Kahan tridiagonal with zero diagonal and off-diagonal
+    (d_0, e_0, d_1, ..., d_{n-1}), taken with LAPACK's symmetric tridiagonal
+    eigensolver (scipy.linalg.eigvalsh_tridiagonal).  The oracle of
+    bb_singular_values ("A two-stage reduction on an Apple M5 Pro",
+    Section 7: bidiagonal singular values by bisection on this matrix)."""
+    import scipy.linalg as sla
+    d = np.asarray(d, dtype=np.float64)
+    e = np.asarray(e, dtype=np.float64)
+    n = d.size
+    if n == 0:
+        return np.zeros(0)
+    if n == 1:
+        return np.abs(d)
+    off = np.empty(2 * n - 1)
+    off[0::2] = d
+    off[1::2] = e[: n - 1]
+    # sigma(s B) = |s| sigma(B): scale by the power of two that brings the
+    # largest entry near 1 (exact), so that the eigensolver's internal
+    # squares neither under- nor overflow, and scale the result back
+    amax = float(np.abs(off).max())
+    k = int(np.floor(np.log2(amax))) if amax > 0 and np.isfinite(amax) else 0
+    ev = sla.eigvalsh_tridiagonal(np.zeros(2 * n), np.ldexp(off, -k))
+    return np.ldexp(np.sort(ev)[::-1][:n].clip(min=0.0), k)
+

@@ -430,3 +430,70 @@ def test_a_too_short_lag_is_detected():
 
     alt = _run_order(band, n, bw, tw, bad)
     assert not np.array_equal(alt, serial)
+
+
+# ---------------------------------------------------------------------------
+# Bidiagonal singular values (oracle of bb_singular_values)
+# ---------------------------------------------------------------------------
+
+def _dense_bidiag(d, e):
+    n = d.size
+    B = np.diag(d.astype(np.float64))
+    if n > 1:
+        B += np.diag(e.astype(np.float64), 1)
+    return B
+
+
+def test_svals_one_by_one():
+    assert oracle.bidiagonal_singular_values(np.array([-2.5]), np.zeros(0))[0] == 2.5
+
+
+def test_svals_two_by_two_closed_form():
+    # B = [[a, b], [0, c]]: s1 s2 = |a c|, s1^2 + s2^2 = a^2 + b^2 + c^2
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        a, b, c = rng.normal(size=3)
+        S = a * a + b * b + c * c
+        disc = np.sqrt(S * S - 4 * (a * c) ** 2)
+        want = np.sqrt(np.array([(S + disc) / 2, max((S - disc) / 2, 0.0)]))
+        got = oracle.bidiagonal_singular_values(np.array([a, c]), np.array([b]))
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def test_svals_diagonal_is_sorted_abs():
+    d = np.array([0.5, -3.0, 2.0, 0.0, -1.0])
+    got = oracle.bidiagonal_singular_values(d, np.zeros(4))
+    assert np.array_equal(got, np.array([3.0, 2.0, 1.0, 0.5, 0.0]))
+
+
+def test_svals_all_ones_path_graph():
+    # all d = e = 1: the Golub-Kahan matrix is the path graph on 2n nodes,
+    # eigenvalues 2 cos(k pi / (2n + 1)); the positive half are the sigma
+    n = 37
+    got = oracle.bidiagonal_singular_values(np.ones(n), np.ones(n - 1))
+    want = 2 * np.cos(np.arange(1, n + 1) * np.pi / (2 * n + 1))
+    assert np.allclose(got, want, rtol=0, atol=1e-13)
+
+
+def test_svals_match_dense_svd_and_scale():
+    rng = np.random.default_rng(6)
+    d = rng.normal(size=60)
+    e = rng.normal(size=59)
+    got = oracle.bidiagonal_singular_values(d, e)
+    want = np.linalg.svd(_dense_bidiag(d, e), compute_uv=False)
+    assert np.allclose(got, want, rtol=0, atol=1e-13 * want[0])
+    got3 = oracle.bidiagonal_singular_values(-3 * d, 3 * e)
+    assert np.allclose(got3, 3 * got, rtol=0, atol=1e-13 * got3[0])
+    assert np.all(np.diff(got) <= 0)
+
+
+def test_svals_power_of_two_scaling_exact():
+    # sigma(2^k B) = 2^k sigma(B) exactly (the oracle scales internally), from
+    # near underflow to near overflow
+    rng = np.random.default_rng(7)
+    d = rng.normal(size=40)
+    e = rng.normal(size=39)
+    base = oracle.bidiagonal_singular_values(d, e)
+    for k in (-1000, -500, -60, 60, 500, 1000):
+        got = oracle.bidiagonal_singular_values(np.ldexp(d, k), np.ldexp(e, k))
+        assert np.array_equal(got, np.ldexp(base, k)), k
