@@ -1,6 +1,6 @@
-// Singular values of an upper bidiagonal matrix (d, e) on the GPU: bisection
-// on Sturm counts of the 2n x 2n Golub-Kahan tridiagonal, one thread per
-// singular value.
+// Singular values of an upper bidiagonal matrix (d, e) on the GPU:
+// multisection on Sturm counts of the 2n x 2n Golub-Kahan tridiagonal, a
+// group of lanes per singular value.
 //
 // The Golub-Kahan matrix T has a zero diagonal and off-diagonal
 // a = (d_0, e_0, d_1, e_1, ..., e_{n-2}, d_{n-1}); its eigenvalues are the
@@ -12,8 +12,8 @@
 // two-stage reduction on an Apple M5 Pro", Section 7, bisection for the
 // bidiagonal singular values); the GPU layout is this library's.
 //
-// Every thread runs the same number of bisection steps, so a block walks the
-// squared off-diagonal in shared-memory chunks in lockstep.  The entries are
+// Every thread runs the same number of steps, so a block walks the squared
+// off-diagonal in shared-memory chunks in lockstep.  The entries are
 // first scaled by a power of two that brings the largest near 1.
 #include <cuda_runtime.h>
 
@@ -29,20 +29,24 @@ void set_last_error(const char* msg);  // bb_api.cu
 template <typename T> struct SvLim;
 template <> struct SvLim<float> {
     static __device__ __forceinline__ float safmin() { return 1.17549435e-38f; }
-    static constexpr int iters = 27;  // 2^-27 of the Gershgorin bound < eps/2 of it
 };
 template <> struct SvLim<double> {
     static __device__ __forceinline__ double safmin() { return 2.2250738585072014e-308; }
-    static constexpr int iters = 56;
 };
 
 constexpr int kSvThreads = 128;
 constexpr int kSvChunk = 2048;  // squared off-diagonal entries per shared-memory chunk
 
-// sigma[k] = the k-th largest singular value (k = 0 .. n-1).
+// sigma[k] = the k-th largest singular value (k = 0 .. n-1).  A group of P
+// consecutive lanes of a warp (P a power of two, 1 .. 32) works on one value:
+// each step, lane l of the group counts at lo + (hi - lo) (l + 1) / (P + 1)
+// and the group keeps the subinterval where the count passes j (the counts
+// grow with l, so the lanes at or below j form a prefix: a ballot finds it).
+// P = 1 is plain bisection; larger P trades more counts for fewer steps.
 template <typename T>
 __global__ void __launch_bounds__(kSvThreads)
-bidiag_svals_kernel(const T* __restrict__ d, const T* __restrict__ e, int n, T* __restrict__ sigma) {
+bidiag_svals_kernel(const T* __restrict__ d, const T* __restrict__ e, int n, int P, int steps,
+                    T* __restrict__ sigma) {
     __shared__ T s_a2[kSvChunk];
     __shared__ T s_red[kSvThreads / 32];
     const int m = 2 * n - 1;  // off-diagonal entries of T
@@ -74,11 +78,15 @@ bidiag_svals_kernel(const T* __restrict__ d, const T* __restrict__ e, int n, T* 
     const T amax_s = amax * sc;
     const T pivmin = SvLim<T>::safmin() * fmax(T(1), amax_s * amax_s);
 
-    const int k = blockIdx.x * blockDim.x + threadIdx.x;  // k-th largest
-    const int j = n - 1 - k;                               // j-th smallest
+    const int lane = threadIdx.x & 31;
+    const int l = lane & (P - 1);                     // lane within the group
+    const int gbase = lane & ~(P - 1);                // first lane of the group
+    const unsigned gmask = (P == 32) ? 0xffffffffu : (((1u << P) - 1u) << gbase);
+    const int k = (blockIdx.x * blockDim.x + threadIdx.x) / P;  // k-th largest
+    const int j = n - 1 - k;                                     // j-th smallest
     T lo = 0, hi = bound * T(1.0000001) + pivmin;
-    for (int it = 0; it < SvLim<T>::iters; ++it) {
-        const T x = T(0.5) * (lo + hi);
+    for (int it = 0; it < steps; ++it) {
+        const T x = lo + (hi - lo) * T(l + 1) / T(P + 1);
         T q = -x;
         int cnt = (q < T(0)) ? 1 : 0;
         for (int c0 = 0; c0 < m; c0 += kSvChunk) {
@@ -96,10 +104,15 @@ bidiag_svals_kernel(const T* __restrict__ d, const T* __restrict__ e, int n, T* 
                 cnt += (q < T(0)) ? 1 : 0;
             }
         }
-        if (cnt - n > j) hi = x;
-        else lo = x;
+        // lanes whose point has at most j singular values below it: a prefix
+        const unsigned below = __ballot_sync(0xffffffffu, cnt - n <= j) & gmask;
+        const int lstar = __popc(below) - 1;  // last such lane of the group, or -1
+        const T xlo = __shfl_sync(0xffffffffu, x, gbase + max(lstar, 0));
+        const T xhi = __shfl_sync(0xffffffffu, x, gbase + min(lstar + 1, P - 1));
+        if (lstar >= 0) lo = xlo;
+        if (lstar < P - 1) hi = xhi;
     }
-    if (k < n) sigma[k] = T(0.5) * (lo + hi) / sc;
+    if (l == 0 && k < n) sigma[k] = T(0.5) * (lo + hi) / sc;
 }
 
 }  // namespace bb
@@ -119,14 +132,24 @@ extern "C" bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d
         return BB_ERR_DTYPE;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    const unsigned grid = (unsigned)((n + bb::kSvThreads - 1) / bb::kSvThreads);
+    // lanes per value: about enough threads to fill the GPU (152 SMs x 2048),
+    // a power of two from 1 to 32
+    int P = 1;
+    while (P < 32 && (int64_t)P * 2 * n <= (int64_t)152 * 2048) P *= 2;
+    // steps: the interval shrinks by P + 1 per step, down to 2^-27 (float)
+    // or 2^-56 (double) of the bound
+    const int bits = (dtype == BB_F32) ? 27 : 56;
+    int lg = 0;  // floor(log2(P + 1))
+    while ((2 << lg) <= P + 1) ++lg;
+    const int steps = (bits + lg - 1) / lg;
+    const unsigned grid = (unsigned)((n * P + bb::kSvThreads - 1) / bb::kSvThreads);
     // e may be null for n == 1: the kernel never reads it then (m = 1)
     if (dtype == BB_F32)
         bb::bidiag_svals_kernel<float><<<grid, bb::kSvThreads, 0, s>>>(
-            (const float*)d, (const float*)e, (int)n, (float*)sigma_out);
+            (const float*)d, (const float*)e, (int)n, P, steps, (float*)sigma_out);
     else
         bb::bidiag_svals_kernel<double><<<grid, bb::kSvThreads, 0, s>>>(
-            (const double*)d, (const double*)e, (int)n, (double*)sigma_out);
+            (const double*)d, (const double*)e, (int)n, P, steps, (double*)sigma_out);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) {
         bb::set_last_error(cudaGetErrorString(err));

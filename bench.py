@@ -228,8 +228,8 @@ def run_svals(w: bi.Workload, steps: int, warmup: int):
         times.append(ev0.elapsed_time(ev1))
     ms = statistics.median(times)
     return {"ms": ms, "n": w.n, "values_per_s": w.n / (ms * 1e-3), "kernel": "bidiag_svals_kernel",
-            "launches": 1, "method": "bisection on Sturm counts of the 2n Golub-Kahan tridiagonal, "
-                                     "one thread per singular value"}
+            "launches": 1, "method": "multisection on Sturm counts of the 2n Golub-Kahan tridiagonal, "
+                                     "a group of lanes per singular value"}
 
 
 def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):

@@ -95,10 +95,12 @@ def test_after_the_reduction(idx):
     assert err <= TOL[w.dtype], err
 
 
-def test_full_size_properties():
-    """n = 32768 (the largest workload's order), float32: descending,
-    bounded by the Gershgorin bound, and sum sigma^2 = ||B||_F^2."""
-    n = 32768
+@pytest.mark.parametrize("n", [32768, 40000, 80000])
+def test_full_size_properties(n):
+    """n = 32768 (the largest workload's order) and beyond, float32 (the lane
+    group per value shrinks with n: 4, 2 and 1 lanes here): descending,
+    bounded by the Gershgorin bound, and sum sigma^2 = ||B||_F^2; against the
+    oracle at n = 32768."""
     rng = np.random.default_rng(4)
     d = rng.normal(size=n).astype(np.float32)
     e = rng.normal(size=n - 1).astype(np.float32)
@@ -108,9 +110,9 @@ def test_full_size_properties():
     assert got[0] <= bound
     fro2 = float((d.astype(np.float64) ** 2).sum() + (e.astype(np.float64) ** 2).sum())
     assert abs((got ** 2).sum() - fro2) / fro2 < 1e-5
-    # sampled values against the oracle
-    want = oracle.bidiagonal_singular_values(d, e)
-    assert float(np.abs(got - want).max()) / np.sqrt(fro2) <= TOL["f32"]
+    if n == 32768:
+        want = oracle.bidiagonal_singular_values(d, e)
+        assert float(np.abs(got - want).max()) / np.sqrt(fro2) <= TOL["f32"]
 
 
 def test_argument_errors():
