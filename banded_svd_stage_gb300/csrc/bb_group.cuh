@@ -346,24 +346,28 @@ __host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem
 }
 
 // Persistent group kernel: CTAs take groups G = blockIdx.x, + gridDim.x, ...
-// in order; blockDim.x = 32 * (g + 3).  Warp jj < g runs sweep r0 + jj, one
-// half-step per tick, the g warps meeting at a named barrier after each
-// tick.  Warp g (the loader) copies in the columns tick u first needs, one
-// bulk (TMA) copy per column, once group G - 1's watermark is beyond them and
-// the storer has freed their slots; full[u mod S] completes when the bytes
-// have landed.  Warp g + 1 (the storer) waits for done[v mod S] (tick v
-// computed), writes back with bulk copies the columns no later tick touches,
-// frees their slots and, one tick later (so that the wait rarely stalls),
-// reports them complete in shared memory; warp g + 2 (the publisher) turns
-// that report into the group's watermark (the first column the group may
-// still touch) with a gpu-scope fence and a release store, so the fence
-// delays neither the storer nor the loader.  The loader runs at most `ahead` ticks ahead of the storer and S = ahead + 2
-// stages, so no mbarrier phase is overtaken.  Copies, write-backs and fences
-// thus overlap the computation.  Every wait is bounded; on giving up the CTA
-// latches an error, the compute warps leave their loop at the same tick, the
-// other roles leave theirs, and the CTA returns after one last barrier.
-// Requires band, ldab * sizeof(T) and top * sizeof(T) 16-byte aligned and
-// n < 2^30 (32-bit geometry).
+// in order; blockDim.x = 32 * (g + 3).
+//   Warps jj < g run sweep r0 + jj, one half-step per tick, and meet at a
+//   named barrier after each tick.
+//   Warp g (the loader) copies in the columns tick u first needs, one bulk
+//   (TMA) copy per column, once group G - 1's watermark is beyond them and
+//   the storer has freed their slots; full[u mod S] completes when the bytes
+//   have landed.
+//   Warp g + 1 (the storer) waits for done[v mod S] (tick v computed), writes
+//   back the columns no later tick touches (bulk copies for wide columns,
+//   plain 16-byte copies for narrow ones), frees their slots and reports the
+//   written-back range in shared memory (bulk copies one tick later, once
+//   they are complete).
+//   Warp g + 2 (the publisher) turns that report into the group's watermark
+//   (the first column the group may still touch) with a release store, so
+//   its latency delays neither the storer nor the loader.
+// The loader runs at most `ahead` ticks ahead of the storer and S = ahead + 2
+// stages, so no mbarrier phase is overtaken.  Copies, write-backs and
+// publication thus overlap the computation.  Every wait is bounded; on
+// giving up the CTA latches an error, the compute warps leave their loop at
+// the same tick, the other roles leave theirs, and the CTA returns after one
+// last barrier.  Requires band, ldab * sizeof(T) and top * sizeof(T) 16-byte
+// aligned and n < 2^30 (32-bit geometry).
 template <typename T, int WMAX>
 __global__ void __launch_bounds__(32 * GroupMaxWarps<T, WMAX>::value)
 pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restrict__ wm,
@@ -572,7 +576,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
             __syncwarp();
             if (lane == 0 && !stopped) st_release_cta_shared(&s_written, (int)P.n);
         } else if (warp == GA.g + 2) {
-            // ---- publisher: the gpu-scope fence stays off the storer's path ----
+            // ---- publisher: the release's latency stays off the storer's path ----
             if (lane == 0) {
                 const bool publish = P.stall_sweep < r0 || P.stall_sweep >= r0 + ng;  // fault injection
                 int published = -1;
