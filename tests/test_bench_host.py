@@ -1,0 +1,60 @@
+"""Host-side logic of bench.py (no GPU): the dominant-kernel roofline
+bookkeeping and the staleness guard of the committed DRAM traffic."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_dominant_kernel_picks_the_largest_time_share():
+    res = {"kernels": [(2, 0), (2, 0), (3, 5), (3, 5)],
+           "pass_ms_mean": [10.0, 10.0, 30.0, 5.0],
+           "pass_bytes": [100e9, 100e9, 50e9, 10e9]}
+    name, ach, nl, by, ms = bench.dominant_kernel(res)
+    assert name == "pass_group_kernel" and nl == 2
+    assert by == 60e9 and ms == 35.0
+    assert ach == pytest.approx(60e9 / 35e-3 / 1e9)
+
+
+def test_dominant_kernel_per_cycle_has_no_launch_count():
+    res = {"kernels": [(1, 0)], "pass_ms_mean": [5.0], "pass_bytes": [1e9]}
+    name, ach, nl, _, _ = bench.dominant_kernel(res)
+    assert name == "pass_cycle_kernel" and nl == 0
+    res = {"kernels": [(4, 0)], "pass_ms_mean": [5.0], "pass_bytes": [1e9]}
+    assert bench.dominant_kernel(res)[0] == "pass_cycle_kernel"
+
+
+def test_dominant_kernel_empty():
+    assert bench.dominant_kernel({"kernels": [], "pass_ms_mean": [], "pass_bytes": []})[0] is None
+
+
+def test_committed_traffic_is_reported_only_for_its_sources():
+    """bench reports the DRAM bytes of profiles/traffic.json only while the
+    kernel sources are the ones they were taken on."""
+    from banded_svd_stage_gb300.buildlib import source_digest
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        data = json.load(f)
+    got = bench.traffic_for("pass_group_kernel", "n4096_bw16_tw8_f32")
+    if data["source_digest"] == source_digest():
+        assert got == data["per_launch"]["pass_group_kernel"]["n4096_bw16_tw8_f32"] > 0
+    else:
+        assert got is None
+    assert bench.traffic_for("pass_group_kernel", "no_such_workload") is None
+
+
+def test_traffic_is_dropped_when_sources_change(monkeypatch):
+    import banded_svd_stage_gb300.buildlib as bl
+    monkeypatch.setattr(bl, "source_digest", lambda: "0000000000000000")
+    assert bench.traffic_for("pass_group_kernel", "n4096_bw16_tw8_f32") is None
+
+
+def test_measured_peak_is_read():
+    peak, src = bench.measured_peaks()
+    assert peak > 1000 and src in ("measured", "fallback")
