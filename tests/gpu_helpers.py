@@ -70,12 +70,13 @@ def oracle_sensitivity(band: np.ndarray, n: int, bw: int, tw: int, seeds=(101, 2
 
 
 def record(kind: str, **kw) -> None:
-    """Append a parity record to gpurun_out/parity_records.jsonl when that folder exists."""
+    """Append a parity record (JSON line) to the file named by the environment
+    variable BB_PARITY_RECORDS, when it is set."""
     import json
     import os
-    out = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
-    if os.path.isdir(out):
-        with open(os.path.join(out, "parity_records.jsonl"), "a") as f:
+    path = os.environ.get("BB_PARITY_RECORDS")
+    if path:
+        with open(path, "a") as f:
             f.write(json.dumps({"kind": kind, **kw}) + "\n")
 
 
