@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "bb_last_pass_kernel": ([p, i64], i64),
             "bb_last_pass_group": ([p, i64], i64),
             "bb_singular_values": ([ci, i64, p, p, p, p], ci),
+            "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -195,6 +196,14 @@ def bb_reduce_noalloc(band, n: int, bw: int, ldab: int, tw: int, dtype: int, d_o
     synchronizes the stream before returning."""
     _check(lib().bb_reduce_noalloc(_addr(band), n, bw, ldab, tw, dtype, _addr(d_out), _addr(e_out),
                                    _stream(stream)))
+
+
+def bb_group_plan(n: int, bw: int, tw: int, elem_bytes: int, pass_index: int, group_size: int = 0):
+    """(g, nslot, ahead, lds) of the group kernel's plan for one pass; g = 0
+    when the group kernel cannot take it.  Host-only."""
+    vals = [ctypes.c_int64() for _ in range(4)]
+    _check(lib().bb_group_plan(n, bw, tw, elem_bytes, pass_index, group_size, *[ctypes.byref(v) for v in vals]))
+    return tuple(v.value for v in vals)
 
 
 def bb_singular_values(dtype: int, n: int, d, e, sigma_out, stream=None) -> None:

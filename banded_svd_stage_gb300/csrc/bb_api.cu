@@ -124,6 +124,30 @@ bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t
     return BB_OK;
 }
 
+bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
+                        int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds) {
+    auto plan = plan_passes(bw, tw);
+    if (pass < 0 || pass >= (int64_t)plan.size() || !g || !nslot || !ahead || !lds || n < 1 ||
+        n >= bb::kGroupMaxN || (elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
+        return fail(BB_ERR_INVALID_ARG, "bb_group_plan: argument out of range");
+    bb::PassArgs P{};
+    P.n = n;
+    P.b = plan[pass].b;
+    P.t = plan[pass].t;
+    P.bp = P.b - P.t;
+    P.ku = (int)(bw + tw);
+    P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
+    P.lagh = pass_lag_half(P.b, P.t);
+    bb::GroupArgs ga{};
+    const bool ok = P.nsweeps > 0 &&
+                    bb::plan_group(P, bb::wmax_bucket(P.t + 1), (size_t)elem_bytes, (int)group_size, &ga);
+    *g = ok ? ga.g : 0;
+    *nslot = ok ? ga.nslot : 0;
+    *ahead = ok ? ga.ahead : 0;
+    *lds = ok ? ga.lds : 0;
+    return BB_OK;
+}
+
 double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass) {
     auto plan = plan_passes(bw, tw);
     double total = 0;

@@ -147,6 +147,15 @@ int64_t bb_get_param(const bb_handle* h, int param);
 int64_t bb_num_passes(int64_t bw, int64_t tw);
 bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t);
 
+/* Group-kernel plan of pass `pass` of an n x n reduction (element size
+ * elem_bytes, 4 or 8): the sweeps per group g (0 when the group kernel
+ * cannot take the pass), the columns of its shared-memory buffer (nslot),
+ * the loader's run-ahead in ticks, and the rows a buffered column holds
+ * (lds).  group_size as BB_PARAM_GROUP_SIZE (0 = the largest that fits).
+ * Host-only, for inspection and tests. */
+bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
+                        int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds);
+
 /* Algorithmic bytes of pass i (or of all passes when i < 0) of an n x n
  * reduction with element size elem_bytes: every element of each step's right
  * block (rows p..ce x cols c..ce) and left block (rows c..ce x cols c..cend)
