@@ -3,7 +3,9 @@
 This module only draws random numbers and lays them out; it holds none of the
 reduction's arithmetic.  Both the CUDA library's tests/benchmark and the CPU
 oracle's tests take their inputs from here, so the two sides see the same
-arrays.
+arrays.  The one construction beyond that, the band with prescribed singular
+values, runs the *first* stage of the two-stage SVD (dense -> band) with
+numpy's QR; the band -> bidiagonal reduction itself appears nowhere here.
 
 Storage is compact column-major band storage with fill rows (LAPACK "gb"
 layout with ku = bw + tw upper and kl = tw lower diagonals):
@@ -127,3 +129,112 @@ def dense_to_band(a: np.ndarray, ku: int, ldab: int) -> np.ndarray:
             if 0 <= i < n:
                 band[j, d] = a[i, j]
     return band
+
+
+# ------------------------------------------------ prescribed singular values ---
+#
+# Accuracy protocol of "Accelerating Bidiagonalization of Banded Matrices
+# through Memory-Aware Bulge-Chasing on GPUs" (Section V, accuracy study):
+# A = U diag(sigma) V^T with random orthogonal U, V and sigma in [0, 1] from
+# one of three profiles (uniform spacing, logarithmic decay, quarter-circle),
+# reduced to band form in double precision by block Householder; the
+# band -> bidiagonal reduction then runs in the precision under test and the
+# singular values of its result are compared with sigma.
+
+SPECTRA = ("arithmetic", "logarithmic", "quarter_circle")
+
+
+def spectrum(kind: str, n: int, seed: int = 0, decades: float = 8.0) -> np.ndarray:
+    """n singular values in [0, 1], descending, float64.
+
+    arithmetic      k / n, k = n .. 1 (uniform spacing);
+    logarithmic     10 ** (-decades * k / (n - 1)), k = 0 .. n-1;
+    quarter_circle  n seeded draws from the density (4 / pi) sqrt(1 - x^2) on
+                    [0, 1] (the limit law of the singular values of a scaled
+                    square Gaussian matrix): |sqrt(u1) cos(2 pi u2)| is the
+                    |abscissa| of a point uniform in the unit disc;
+    rank_deficient  the arithmetic profile of n - n // 2 values, then n // 2
+                    exact zeros.
+    """
+    if n == 0:
+        return np.zeros(0)
+    if kind == "arithmetic":
+        s = np.arange(n, 0, -1, dtype=np.float64) / n
+    elif kind == "logarithmic":
+        s = 10.0 ** (-decades * np.arange(n, dtype=np.float64) / max(n - 1, 1))
+    elif kind == "quarter_circle":
+        rng = np.random.default_rng(seed)
+        u1 = rng.random(n)
+        u2 = rng.random(n)
+        s = np.sort(np.abs(np.sqrt(u1) * np.cos(2.0 * np.pi * u2)))[::-1]
+    elif kind == "rank_deficient":
+        m = n - n // 2
+        s = np.concatenate([np.arange(m, 0, -1, dtype=np.float64) / m, np.zeros(n // 2)])
+    else:
+        raise ValueError(kind)
+    return np.ascontiguousarray(s)
+
+
+def _haar_orthogonal(n: int, rng) -> np.ndarray:
+    """Haar-distributed orthogonal matrix: QR of a Gaussian matrix with the
+    signs of R's diagonal moved into Q."""
+    q, r = np.linalg.qr(rng.standard_normal((n, n)))
+    sg = np.sign(np.diag(r))
+    sg[sg == 0] = 1.0
+    return q * sg
+
+
+def dense_to_upper_band(a: np.ndarray, bw: int) -> np.ndarray:
+    """Orthogonally equivalent upper band of bandwidth bw (float64), by block
+    Householder: for each panel of bw columns, the QR factorisation of the
+    panel (rows below) zeroes it under the diagonal; the LQ factorisation of
+    the bw rows to the right of the panel (as QR of their transpose) leaves
+    them lower triangular, so row i ends at column i + bw.  LAPACK's compact
+    reflectors (geqrf through scipy's raw QR) are applied with ormqr.  The
+    rounding residue left outside the band (a few eps * ||a||) is set to
+    zero."""
+    import scipy.linalg as sla
+    from scipy.linalg import lapack
+
+    a = np.array(a, dtype=np.float64, copy=True, order="F")
+    n = a.shape[0]
+    if bw < 1:
+        raise ValueError("bw must be at least 1")
+    for k in range(0, n, bw):
+        kb = min(k + bw, n)
+        (qr, tau), _ = sla.qr(a[k:, k:kb], mode="raw")
+        c = np.asfortranarray(a[k:, k:])
+        c, _, info = lapack.dormqr("L", "T", qr[:, :tau.size], tau, c, max(1, c.shape[1] * 64))
+        assert info == 0
+        a[k:, k:] = c
+        if kb < n:
+            (qr, tau), _ = sla.qr(a[k:kb, kb:].T, mode="raw")
+            # rows above k are already zero in columns kb..
+            c = np.asfortranarray(a[k:, kb:])
+            c, _, info = lapack.dormqr("R", "N", qr[:, :tau.size], tau, c, max(1, c.shape[0] * 64))
+            assert info == 0
+            a[k:, kb:] = c
+    i, j = np.indices(a.shape)
+    a[(j < i) | (j - i > bw)] = 0.0
+    return np.ascontiguousarray(a)
+
+
+def make_band_with_spectrum(n: int, bw: int, tw: int, sigma: np.ndarray, dtype="f64", seed=0,
+                            ldab: int | None = None) -> np.ndarray:
+    """Band storage (shape (n, ldab)) of an upper band of bandwidth bw whose
+    singular values are sigma up to the float64 rounding of the construction:
+    A = U diag(sigma) V^T with U, V Haar-random (seeded), reduced to band form
+    by dense_to_upper_band.  float32 rounds the float64 band."""
+    if ldab is None:
+        ldab = bw + 2 * tw + 1
+    if ldab < bw + 2 * tw + 1:
+        raise ValueError("ldab too small")
+    sigma = np.asarray(sigma, dtype=np.float64)
+    if sigma.shape != (n,):
+        raise ValueError("sigma must have n entries")
+    rng = np.random.default_rng(seed)
+    u = _haar_orthogonal(n, rng)
+    v = _haar_orthogonal(n, rng)
+    a = dense_to_upper_band((u * sigma) @ v.T, max(bw, 1))
+    npd = np.float32 if dtype == "f32" else np.float64
+    return dense_to_band(a, bw + tw, ldab).astype(npd)

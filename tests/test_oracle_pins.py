@@ -295,6 +295,60 @@ def test_invalid_arguments_rejected():
         oracle.reduce_band(bi.make_band(4, 3, 1, "f64"), 4, 4, 1)  # bw >= n
 
 
+# ---------------------------------------------- prescribed singular values ---
+#
+# The paper's accuracy protocol (Section V): a band built from A = U diag(sigma)
+# V^T in float64 must reduce to a bidiagonal whose singular values are sigma.
+# Unlike the Jacobi pin above, the expected values here are the prescribed
+# ones, not computed from the input.  The pages report no numbers, only
+# float64 errors "near machine epsilon"; the bars are the acceptance bars of
+# the parity tests (max |dsigma| <= 1e-12 sigma_1 in float64, 2e-5 sigma_1 in
+# float32), and the paper's measure ||dsigma||_2 / ||sigma||_2 is held to
+# 1e-13 (float64) and 1e-5 (float32).
+
+KNOWN_SIGMA_CASES = [(200, 16, 8), (384, 24, 7), (300, 40, 12), (512, 32, 8)]
+KNOWN_SIGMA_BARS = {"f64": (1e-12, 1e-13), "f32": (2e-5, 1e-5)}
+
+
+@pytest.mark.parametrize("kind", bi.SPECTRA + ("rank_deficient",))
+def test_known_spectrum_generator(kind):
+    # the generator itself, against LAPACK's SVD of the dense band it returns
+    n, bw, tw = 160, 12, 5
+    sigma = bi.spectrum(kind, n, seed=4)
+    assert np.all(np.diff(sigma) <= 0) and sigma[0] <= 1.0 and sigma[-1] >= 0.0
+    band = bi.make_band_with_spectrum(n, bw, tw, sigma, seed=9)
+    a = dense_of(band, n, bw, tw)
+    i, j = np.indices(a.shape)
+    assert not a[(j < i) | (j - i > bw)].any()
+    assert np.abs(np.linalg.svd(a, compute_uv=False) - sigma).max() <= 50 * F64_EPS
+
+
+def test_spectrum_profiles():
+    n = 11
+    assert np.array_equal(bi.spectrum("arithmetic", n), np.arange(n, 0, -1) / n)
+    lg = bi.spectrum("logarithmic", n)
+    assert lg[0] == 1.0 and abs(lg[-1] - 1e-8) <= 1e-22
+    assert np.allclose(lg[1:] / lg[:-1], 10 ** -0.8, rtol=1e-14)
+    rd = bi.spectrum("rank_deficient", n)
+    assert np.count_nonzero(rd) == n - n // 2
+    # quarter-circle law: mean 4 / (3 pi), second moment 1 / 4
+    qc = bi.spectrum("quarter_circle", 200000, seed=1)
+    assert abs(qc.mean() - 4 / (3 * np.pi)) < 3e-3 and abs((qc * qc).mean() - 0.25) < 3e-3
+
+
+@pytest.mark.parametrize("dt", ["f64", "f32"])
+@pytest.mark.parametrize("kind", bi.SPECTRA + ("rank_deficient",))
+@pytest.mark.parametrize("n,bw,tw", KNOWN_SIGMA_CASES)
+def test_oracle_recovers_prescribed_singular_values(n, bw, tw, kind, dt):
+    sigma = bi.spectrum(kind, n, seed=n + bw)
+    band = bi.make_band_with_spectrum(n, bw, tw, sigma, dt, seed=3 * n + tw)
+    d, e = oracle.bidiagonal(band, n, bw, tw)
+    got = oracle.bidiagonal_singular_values(d.astype(np.float64), e.astype(np.float64))
+    max_bar, norm_bar = KNOWN_SIGMA_BARS[dt]
+    assert np.abs(got - sigma).max() <= max_bar * sigma[0]
+    assert np.linalg.norm(got - sigma) <= norm_bar * np.linalg.norm(sigma)
+
+
 def test_pass_plan_of_the_workloads():
     assert oracle.pass_plan(8, 7) == [(8, 7)]
     assert oracle.pass_plan(16, 8) == [(16, 8), (8, 7)]
