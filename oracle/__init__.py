@@ -30,33 +30,42 @@ def build(force: bool = False) -> str:
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(s) for s in srcs)):
         return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    return compile_library(_SRC, _LIB_PATH)
+
+
+def compile_library(src: str, out: str) -> str:
+    """gcc the oracle source src (bb_oracle.c, which includes its body from
+    the same folder) into the shared library out, atomically."""
+    tmp = out + f".tmp{os.getpid()}"
     subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
-                           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+                           "-fPIC", "-shared", "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the argument and result types of the oracle's C functions."""
+    i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    for sfx in ("_d", "_f"):
+        getattr(lib, "oracle_larfg" + sfx).argtypes = [i64, p, p, i64, p]
+        getattr(lib, "oracle_larfg" + sfx).restype = None
+        getattr(lib, "oracle_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64, i64, i64]
+        getattr(lib, "oracle_reduce_band" + sfx).restype = ci
+        getattr(lib, "oracle_reduce_dense" + sfx).argtypes = [i64, i64, i64, p]
+        getattr(lib, "oracle_reduce_dense" + sfx).restype = ci
+        getattr(lib, "oracle_halfstep_band" + sfx).argtypes = [i64, i64, i64, i64, p, i64, i64, i64, ci]
+        getattr(lib, "oracle_halfstep_band" + sfx).restype = None
+        getattr(lib, "oracle_sweep_steps" + sfx).argtypes = [i64, i64, i64, i64]
+        getattr(lib, "oracle_sweep_steps" + sfx).restype = i64
+        getattr(lib, "oracle_extract_band" + sfx).argtypes = [i64, i64, p, i64, p, p]
+        getattr(lib, "oracle_extract_band" + sfx).restype = None
+    return lib
 
 
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-        for sfx in ("_d", "_f"):
-            getattr(lib, "oracle_larfg" + sfx).argtypes = [i64, p, p, i64, p]
-            getattr(lib, "oracle_larfg" + sfx).restype = None
-            getattr(lib, "oracle_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64, i64, i64]
-            getattr(lib, "oracle_reduce_band" + sfx).restype = ci
-            getattr(lib, "oracle_reduce_dense" + sfx).argtypes = [i64, i64, i64, p]
-            getattr(lib, "oracle_reduce_dense" + sfx).restype = ci
-            getattr(lib, "oracle_halfstep_band" + sfx).argtypes = [i64, i64, i64, i64, p, i64, i64, i64, ci]
-            getattr(lib, "oracle_halfstep_band" + sfx).restype = None
-            getattr(lib, "oracle_sweep_steps" + sfx).argtypes = [i64, i64, i64, i64]
-            getattr(lib, "oracle_sweep_steps" + sfx).restype = i64
-            getattr(lib, "oracle_extract_band" + sfx).argtypes = [i64, i64, p, i64, p, p]
-            getattr(lib, "oracle_extract_band" + sfx).restype = None
-        _lib = lib
+        _lib = bind(ctypes.CDLL(build()))
     return _lib
 
 
