@@ -289,6 +289,35 @@ def cpu_oracle_rate(w: bi.Workload, budget_s: float = 12.0):
             "sample": f"{reps} whole serial reductions of {w.name} ({el:.1f} s)"}
 
 
+def cpu_pipelined_rate(w: bi.Workload, budget_s: float = 6.0):
+    """The oracle's pipelined driver on the host cores: sweep r on thread
+    r mod P, each sweep spinning on its predecessor's count of finished
+    half-steps (the multi-threaded chase of "A two-stage reduction on an Apple
+    M5 Pro", Section 6), bitwise equal to the serial oracle.  P follows that
+    section's limits: at most the usable cores, 2n / (3 bw) and n / 256."""
+    import oracle
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    P = max(1, min(cores, 2 * w.n // (3 * max(w.bw, 1)), w.n // 256))
+    band = bi.make_workload(w)
+    try:
+        import banded_svd_stage_gb300 as bb
+        model_bytes = bb.bb_model_bytes(w.n, w.bw, w.tw, 4 if w.dtype == "f32" else 8)
+    except Exception:
+        model_bytes = _model_bytes_py(w)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.bidiagonal_pipelined(band, w.n, w.bw, w.tw, P)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el / reps * (reps + 1) > 2.5 * budget_s:
+            break
+    sec = el / reps
+    return {"value": model_bytes / sec / 1e9, "unit": "GB/s", "cores": P, "kind": "oracle, pipelined sweeps",
+            "ms_per_reduction": sec * 1e3,
+            "sample": f"{reps} whole reductions of {w.name} on {P} threads ({el:.1f} s)"}
+
+
 def _model_bytes_py(w):
     s = 4 if w.dtype == "f32" else 8
     tot, b = 0, w.bw
@@ -447,9 +476,13 @@ def main():
     if rank == 0 and world == 1 and not args.no_sweep:
         svals = run_svals(w, args.steps, args.warmup)
 
-    cpu = None
+    cpu = cpu_pipe = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_oracle_rate(w)
+        try:
+            cpu_pipe = cpu_pipelined_rate(w)
+        except Exception as ex:  # context only: never lose the line for it
+            cpu_pipe = {"error": f"{type(ex).__name__}: {ex}"}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -462,6 +495,7 @@ def main():
             "frac_of_hbm": value / hbm,
             "roofline": roof,
             "cpu_baseline": cpu,
+            "cpu_pipelined": cpu_pipe,
             "e2e": res["e2e"],
             "gpu_launches": res["launches"] * world,
             "clocks": clocks,

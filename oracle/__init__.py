@@ -38,7 +38,7 @@ def compile_library(src: str, out: str) -> str:
     the same folder) into the shared library out, atomically."""
     tmp = out + f".tmp{os.getpid()}"
     subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
-                           "-fPIC", "-shared", "-o", tmp, src, "-lm"])
+                           "-fPIC", "-shared", "-pthread", "-o", tmp, src, "-lm"])
     os.replace(tmp, out)
     return out
 
@@ -59,6 +59,9 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, "oracle_sweep_steps" + sfx).restype = i64
         getattr(lib, "oracle_extract_band" + sfx).argtypes = [i64, i64, p, i64, p, p]
         getattr(lib, "oracle_extract_band" + sfx).restype = None
+        getattr(lib, "oracle_reduce_band_pipelined" + sfx).argtypes = [i64, i64, i64, p, i64, i64,
+                                                                       ctypes.c_double]
+        getattr(lib, "oracle_reduce_band_pipelined" + sfx).restype = ci
     return lib
 
 
@@ -113,6 +116,25 @@ def reduce_band(band: np.ndarray, n: int, bw: int, tw: int, pass_lo: int = 0,
     return band
 
 
+def reduce_band_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: int,
+                          time_limit: float = 600.0) -> np.ndarray:
+    """reduce_band on host threads: sweep r on thread r mod threads, each sweep
+    spinning on its predecessor's count of finished half-steps (the pipelined
+    chase of "A two-stage reduction on an Apple M5 Pro", Section 6, with the
+    half-step separation rule).  Bitwise equal to reduce_band.  Raises
+    TimeoutError after time_limit seconds of waiting."""
+    assert band.flags.c_contiguous and band.shape[0] == n
+    rc = getattr(_load(), "oracle_reduce_band_pipelined" + _sfx(band))(
+        n, bw, tw, _ptr(band), band.shape[1], threads, float(time_limit))
+    if rc == -1:
+        raise ValueError("oracle_reduce_band_pipelined: invalid arguments")
+    if rc == -2:
+        raise TimeoutError("oracle_reduce_band_pipelined: time limit reached")
+    if rc != 0:
+        raise RuntimeError("oracle_reduce_band_pipelined: could not start the threads")
+    return band
+
+
 def reduce_dense(a: np.ndarray, bw: int, tw: int) -> np.ndarray:
     """Reduce a dense row-major n x n array in place (reflectors on whole rows/cols)."""
     assert a.flags.c_contiguous and a.shape[0] == a.shape[1]
@@ -145,6 +167,13 @@ def bidiagonal(band: np.ndarray, n: int, bw: int, tw: int):
     """(d, e) of the reduction of a copy of band (serial oracle)."""
     work = np.ascontiguousarray(band.copy())
     reduce_band(work, n, bw, tw)
+    return extract(work, n, bw + tw)
+
+
+def bidiagonal_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: int):
+    """(d, e) of the pipelined reduction of a copy of band."""
+    work = np.ascontiguousarray(band.copy())
+    reduce_band_pipelined(work, n, bw, tw, threads)
     return extract(work, n, bw + tw)
 
 

@@ -34,13 +34,27 @@
  * brute-force Jacobi SVD) are preserved; |d|, |e| agree with a textbook dense
  * Golub-Kahan bidiagonalisation; larfg agrees with LAPACK's slarfg/dlarfg;
  * any schedule that respects the sweep dependencies gives the serial result
- * bitwise; power-of-two scaling commutes bitwise; diagonal and zero inputs.
+ * bitwise (also when run on host threads by oracle_reduce_band_pipelined);
+ * power-of-two scaling commutes bitwise; diagonal and zero inputs.
  */
+#define _POSIX_C_SOURCE 200809L
 #include <float.h>
 #include <math.h>
+#include <pthread.h>
+#include <sched.h>
+#include <stdatomic.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <time.h>
 
 #define ORACLE_WMAX 129 /* tw <= 128 */
+
+/* wall clock in seconds, for the pipelined driver's time limit */
+static double oracle_now_(void) {
+    struct timespec ts;
+    clock_gettime(CLOCK_MONOTONIC, &ts);
+    return (double)ts.tv_sec + 1e-9 * (double)ts.tv_nsec;
+}
 
 /* double instantiation */
 #define REAL double

@@ -182,6 +182,120 @@ int FN(oracle_reduce_band)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_
     return 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * Pipelined sweeps on P host threads ("A two-stage reduction on an Apple M5
+ * Pro", Section 6, the multi-threaded band chase): sweep r runs on thread
+ * r mod P, every sweep publishes how many of its half-steps are finished, and
+ * the next sweep spins on that count.  All P threads run at once (a sweep
+ * waits only on its predecessor, which belongs to another running thread, or
+ * to its own thread and is then finished), so nothing deadlocks.
+ *
+ * Dependency rule, the half-step form of the sweep separation: half-step h
+ * (right of step k = 2k, left = 2k+1) of sweep r starts once sweep r-1 has
+ * finished min(h + L, H_{r-1}) half-steps, with L = 2 when b - t >= 3, 3 when
+ * b - t == 2 and 4 when b - t == 1 (H_r = 2 x steps of sweep r); the last
+ * half-step of a sweep waits for all of sweep r-1.  Each half-step is
+ * oracle_halfstep_band, so the result is the serial one bitwise as long as
+ * the rule keeps every pair of overlapping half-steps in sweep order.  The
+ * passes are separated by joining the threads.
+ *
+ * Counters are C11 atomics, stored with release and loaded with acquire, so
+ * a sweep sees every write of the half-steps it waited for.  Every wait gives
+ * up after time_limit_s seconds of wall clock for the whole call (then all
+ * threads stop and -2 is returned).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int64_t n, b, t, ku, ldab, nthreads, thread;
+    REAL* band;
+    _Atomic int64_t* done;
+    _Atomic int* stop;
+    double deadline;
+} FN(pipe_arg_);
+
+static int FN(pipe_wait_)(_Atomic int64_t* count, int64_t need, const FN(pipe_arg_)* a) {
+    uint64_t spins = 0;
+    while (atomic_load_explicit(count, memory_order_acquire) < need) {
+        if (atomic_load_explicit(a->stop, memory_order_relaxed)) return 0;
+        if ((++spins & 0x3FF) == 0) {
+            if (oracle_now_() > a->deadline) {
+                atomic_store_explicit(a->stop, 1, memory_order_relaxed);
+                return 0;
+            }
+            sched_yield();
+        }
+    }
+    return 1;
+}
+
+static void* FN(pipe_worker_)(void* arg) {
+    const FN(pipe_arg_)* a = (const FN(pipe_arg_)*)arg;
+    const int64_t n = a->n, b = a->b, t = a->t;
+    const int64_t L = (b - t >= 3) ? 2 : ((b - t == 2) ? 3 : 4);
+    const int64_t nsweeps = n - (b - t) - 1;
+    for (int64_t r = a->thread; r < nsweeps; r += a->nthreads) {
+        const int64_t H = 2 * FN(oracle_sweep_steps)(n, b, t, r);
+        const int64_t Hp = (r > 0) ? 2 * FN(oracle_sweep_steps)(n, b, t, r - 1) : 0;
+        for (int64_t h = 0; h < H; ++h) {
+            if (r > 0) {
+                int64_t need = (h + L < Hp) ? h + L : Hp;
+                if (h == H - 1) need = Hp;
+                if (!FN(pipe_wait_)(&a->done[r - 1], need, a)) return NULL;
+            }
+            FN(oracle_halfstep_band)(n, b, t, a->ku, a->band, a->ldab, r, h >> 1, (int)(h & 1));
+            atomic_store_explicit(&a->done[r], h + 1, memory_order_release);
+        }
+    }
+    return NULL;
+}
+
+/* Same arguments and result as oracle_reduce_band over all passes, on
+ * nthreads (1 .. 1024) threads.  Returns 0; -1 on invalid arguments; -2 when
+ * time_limit_s ran out (the band is then partly reduced); -3 when the
+ * threads or the counters could not be created. */
+int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab,
+                                     int64_t nthreads, double time_limit_s) {
+    if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
+    if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
+    if (tw + 1 > ORACLE_WMAX) return -1;
+    if (nthreads < 1 || nthreads > 1024 || !(time_limit_s > 0)) return -1;
+    const int64_t ku = bw + tw;
+    for (int64_t j = 0; j < n; ++j) {
+        for (int64_t q = 0; q < tw; ++q) band[q + j * ldab] = 0;
+        for (int64_t q = ku + 1; q <= ku + tw; ++q) band[q + j * ldab] = 0;
+    }
+    _Atomic int64_t* done = (_Atomic int64_t*)malloc((size_t)n * sizeof(_Atomic int64_t));
+    pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
+    FN(pipe_arg_)* args = (FN(pipe_arg_)*)malloc((size_t)nthreads * sizeof(FN(pipe_arg_)));
+    _Atomic int stop;
+    atomic_init(&stop, 0);
+    int rc = 0;
+    if (!done || !th || !args) rc = -3;
+    const double deadline = oracle_now_() + time_limit_s;
+    int64_t b = bw;
+    while (rc == 0 && b > 1) {
+        const int64_t t = (tw < b - 1) ? tw : b - 1;
+        const int64_t nsweeps = n - (b - t) - 1;
+        for (int64_t r = 0; r < n; ++r) atomic_init(&done[r], 0);
+        int64_t P = nthreads < nsweeps ? nthreads : nsweeps, started = 0;
+        for (int64_t q = 0; q < P; ++q) {
+            args[q] = (FN(pipe_arg_)){n, b, t, ku, ldab, P, q, band, done, &stop, deadline};
+            if (pthread_create(&th[q], NULL, FN(pipe_worker_), &args[q]) != 0) {
+                atomic_store_explicit(&stop, 1, memory_order_relaxed);
+                rc = -3;
+                break;
+            }
+            ++started;
+        }
+        for (int64_t q = 0; q < started; ++q) pthread_join(th[q], NULL);
+        if (rc == 0 && atomic_load_explicit(&stop, memory_order_relaxed)) rc = -2;
+        b -= t;
+    }
+    free(done);
+    free(th);
+    free(args);
+    return rc;
+}
+
 /* d_i = A(i, i), e_i = A(i, i+1) from band storage. */
 void FN(oracle_extract_band)(int64_t n, int64_t ku, const REAL* band, int64_t ldab, REAL* d, REAL* e) {
     for (int64_t i = 0; i < n; ++i) d[i] = ELEM(i, i);

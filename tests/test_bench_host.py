@@ -58,3 +58,16 @@ def test_traffic_is_dropped_when_sources_change(monkeypatch):
 def test_measured_peak_is_read():
     peak, src = bench.measured_peaks()
     assert peak > 1000 and src in ("measured", "fallback")
+
+
+def test_cpu_legs_report_rates_and_threads():
+    import band_inputs as bi
+    w = bi.WORKLOADS[0]
+    serial = bench.cpu_oracle_rate(w, budget_s=0.3)
+    pipe = bench.cpu_pipelined_rate(w, budget_s=0.3)
+    assert serial["cores"] == 1 and serial["value"] > 0
+    assert pipe["value"] > 0 and 1 <= pipe["cores"] <= max(1, w.n // 256)
+    # the thread count follows the limits of the pipelined chase
+    big = bi.by_name("n4096_bw16_tw8_f32")
+    cores = len(os.sched_getaffinity(0))
+    assert min(cores, 16) == max(1, min(cores, 2 * big.n // (3 * big.bw), big.n // 256))

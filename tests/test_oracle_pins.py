@@ -463,6 +463,45 @@ def test_halfstep_protocol_reproduces_serial_bitwise(n, bw, tw, seed):
     assert np.array_equal(alt, serial)
 
 
+PIPELINE_CASES = [(40, 8, 3), (40, 8, 7), (48, 6, 4), (48, 6, 5), (60, 16, 14), (33, 5, 2), (64, 16, 8),
+                  (50, 3, 2), (50, 3, 1), (70, 24, 7), (2, 1, 1), (3, 2, 1), (5, 3, 2), (300, 40, 12)]
+
+
+@pytest.mark.parametrize("n,bw,tw", PIPELINE_CASES)
+@pytest.mark.parametrize("dt", ["f64", "f32"])
+def test_pipelined_threads_reproduce_serial_bitwise(n, bw, tw, dt):
+    # the multi-threaded chase (sweep r on thread r mod P, spinning on the
+    # predecessor's half-step count) runs the half-step rule concurrently
+    band = bi.make_band(n, bw, tw, dt, "normal", seed=n + bw + 5)
+    serial = band.copy()
+    oracle.reduce_band(serial, n, bw, tw)
+    for threads in (1, 2, 3, 8, 16):
+        work = band.copy()
+        oracle.reduce_band_pipelined(work, n, bw, tw, threads)
+        assert np.array_equal(work, serial), threads
+
+
+@pytest.mark.parametrize("n,bw,tw", [(1000, 32, 8), (600, 9, 8), (800, 12, 10), (512, 64, 16)])
+def test_pipelined_threads_larger_bands(n, bw, tw):
+    # enough sweeps in flight for real overlap between threads; repeated
+    band = bi.make_band(n, bw, tw, "f32", "uniform", seed=n)
+    serial = band.copy()
+    oracle.reduce_band(serial, n, bw, tw)
+    for _ in range(3):
+        work = band.copy()
+        oracle.reduce_band_pipelined(work, n, bw, tw, 8)
+        assert np.array_equal(work, serial)
+
+
+def test_pipelined_invalid_arguments():
+    band = bi.make_band(20, 4, 2, "f64", seed=1)
+    for threads, limit in ((0, 10.0), (2000, 10.0), (2, 0.0), (2, -1.0)):
+        with pytest.raises(ValueError):
+            oracle.reduce_band_pipelined(band.copy(), 20, 4, 2, threads, limit)
+    with pytest.raises(ValueError):
+        oracle.reduce_band_pipelined(band.copy(), 20, 4, 4, 2)   # tw > bw - 1
+
+
 def test_a_too_short_lag_is_detected():
     # Sanity of the schedule tests above: running the last pass with a
     # one-cycle lag (steps of consecutive sweeps in the same cycle, taken in
