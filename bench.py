@@ -307,7 +307,7 @@ def cpu_pipelined_rate(w: bi.Workload, budget_s: float = 6.0):
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle.bidiagonal_pipelined(band, w.n, w.bw, w.tw, P)
+        oracle.bidiagonal_pipelined(band, w.n, w.bw, w.tw, P, time_limit=60.0)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or el / reps * (reps + 1) > 2.5 * budget_s:

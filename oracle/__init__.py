@@ -170,10 +170,11 @@ def bidiagonal(band: np.ndarray, n: int, bw: int, tw: int):
     return extract(work, n, bw + tw)
 
 
-def bidiagonal_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: int):
+def bidiagonal_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: int,
+                         time_limit: float = 600.0):
     """(d, e) of the pipelined reduction of a copy of band."""
     work = np.ascontiguousarray(band.copy())
-    reduce_band_pipelined(work, n, bw, tw, threads)
+    reduce_band_pipelined(work, n, bw, tw, threads, time_limit)
     return extract(work, n, bw + tw)
 
 
