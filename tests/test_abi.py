@@ -99,3 +99,16 @@ def test_planner_and_traffic_model(lib, n, bw, tw):
 def test_required_ldab(lib):
     assert bb.bb_required_ldab(256, 32) == 321
     assert bb.bb_required_ldab(8, 7) == 23
+
+
+def test_singular_values_argument_errors_need_no_gpu(lib):
+    # the entry point validates its arguments before any CUDA call
+    fake = 0x1000  # never dereferenced: every call below is rejected first
+    assert lib.bb_singular_values(bb.BB_F32, 0, fake, fake, fake, None) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_singular_values(bb.BB_F32, -5, fake, fake, fake, None) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_singular_values(bb.BB_F64, (1 << 29) + 1, fake, fake, fake, None) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_singular_values(bb.BB_F32, 4, None, fake, fake, None) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_singular_values(bb.BB_F32, 4, fake, None, fake, None) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_singular_values(bb.BB_F32, 4, fake, fake, None, None) == bb.BB_ERR_INVALID_ARG
+    assert lib.bb_singular_values(7, 4, fake, fake, fake, None) == bb.BB_ERR_DTYPE
+    assert "bb_singular_values" in bb.bb_last_error()
