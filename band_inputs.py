@@ -238,3 +238,112 @@ def make_band_with_spectrum(n: int, bw: int, tw: int, sigma: np.ndarray, dtype="
     a = dense_to_upper_band((u * sigma) @ v.T, max(bw, 1))
     npd = np.float32 if dtype == "f32" else np.float64
     return dense_to_band(a, bw + tw, ldab).astype(npd)
+
+
+# ------------------------------------------------------ symmetric variant ---
+#
+# Symmetric band matrices in LAPACK's lower band layout with fill rows:
+# A(i, j), 0 <= i - j < ldab, at sband[j, i - j] (numpy array of shape
+# (n, ldab)); an input of bandwidth bw occupies rows 0 .. bw, the fill rows
+# bw+1 .. bw+tw start at zero, ldab >= bw + tw + 1.
+
+
+def make_sym_band(n: int, bw: int, tw: int, dtype="f64", dist="normal", seed=0,
+                  ldab: int | None = None) -> np.ndarray:
+    """Lower band storage of a random symmetric band matrix: Z = rng.<dist>(
+    size=(n, bw+1)) in float64, sband[j, q] = Z[j, q] (entry A(j+q, j)),
+    draws that would fall below row n - 1 discarded."""
+    if ldab is None:
+        ldab = bw + tw + 1
+    if ldab < bw + tw + 1:
+        raise ValueError("ldab too small")
+    rng = np.random.default_rng(seed)
+    if dist == "normal":
+        z = rng.standard_normal(size=(n, bw + 1))
+    elif dist == "uniform":
+        z = rng.uniform(-1.0, 1.0, size=(n, bw + 1))
+    elif dist == "zeros":
+        z = np.zeros((n, bw + 1))
+    else:
+        raise ValueError(dist)
+    npd = np.float32 if dtype == "f32" else np.float64
+    sband = np.zeros((n, ldab), dtype=npd)
+    keep = (np.arange(n)[:, None] + np.arange(bw + 1)[None, :]) < n
+    sband[:, :bw + 1] = np.where(keep, z, 0.0).astype(npd)
+    return sband
+
+
+def sym_band_to_dense(sband: np.ndarray, n: int) -> np.ndarray:
+    """Dense symmetric n x n matrix of the lower band storage."""
+    a = np.zeros((n, n), dtype=sband.dtype)
+    for j in range(n):
+        for q in range(sband.shape[1]):
+            if j + q < n:
+                a[j + q, j] = sband[j, q]
+                a[j, j + q] = sband[j, q]
+    return a
+
+
+def dense_to_sym_band(a: np.ndarray, ldab: int) -> np.ndarray:
+    """Lower band storage of the entries of a with 0 <= i - j < ldab."""
+    n = a.shape[0]
+    sband = np.zeros((n, ldab), dtype=a.dtype)
+    for j in range(n):
+        for q in range(ldab):
+            if j + q < n:
+                sband[j, q] = a[j + q, j]
+    return sband
+
+
+def dense_to_sym_band_form(a: np.ndarray, bw: int) -> np.ndarray:
+    """Orthogonally similar symmetric band of bandwidth bw (float64), by block
+    Householder: for each panel of bw columns, the QR factorisation of the
+    panel's rows below the band, applied from both sides, leaves it upper
+    triangular there.  The rounding residue outside the band is set to zero
+    and the result symmetrised exactly from its lower triangle."""
+    import scipy.linalg as sla
+    from scipy.linalg import lapack
+
+    a = np.array(a, dtype=np.float64, copy=True, order="F")
+    n = a.shape[0]
+    if bw < 1:
+        raise ValueError("bw must be at least 1")
+    for k in range(0, n, bw):
+        r0 = k + bw
+        if r0 >= n:
+            break
+        kb = min(k + bw, n)
+        (qr, tau), _ = sla.qr(a[r0:, k:kb], mode="raw")
+        c = np.asfortranarray(a[r0:, :])
+        c, _, info = lapack.dormqr("L", "T", qr[:, :tau.size], tau, c, max(1, c.shape[1] * 64))
+        assert info == 0
+        a[r0:, :] = c
+        c = np.asfortranarray(a[:, r0:])
+        c, _, info = lapack.dormqr("R", "N", qr[:, :tau.size], tau, c, max(1, c.shape[0] * 64))
+        assert info == 0
+        a[:, r0:] = c
+    i, j = np.indices(a.shape)
+    a[np.abs(i - j) > bw] = 0.0
+    low = np.tril(a)
+    return np.ascontiguousarray(low + np.tril(low, -1).T)
+
+
+def make_sym_band_with_spectrum(n: int, bw: int, tw: int, lam: np.ndarray, dtype="f64", seed=0,
+                                ldab: int | None = None) -> np.ndarray:
+    """Lower band storage of a symmetric band of bandwidth bw whose
+    eigenvalues are lam up to the float64 rounding of the construction:
+    A = Q diag(lam) Q^T with Q Haar-random (seeded), reduced to band form by
+    dense_to_sym_band_form.  float32 rounds the float64 band."""
+    if ldab is None:
+        ldab = bw + tw + 1
+    if ldab < bw + tw + 1:
+        raise ValueError("ldab too small")
+    lam = np.asarray(lam, dtype=np.float64)
+    if lam.shape != (n,):
+        raise ValueError("lam must have n entries")
+    rng = np.random.default_rng(seed)
+    q = _haar_orthogonal(n, rng)
+    a = (q * lam) @ q.T
+    a = dense_to_sym_band_form(0.5 * (a + a.T), max(bw, 1))
+    npd = np.float32 if dtype == "f32" else np.float64
+    return dense_to_sym_band(a, ldab).astype(npd)

@@ -26,7 +26,7 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile bb_oracle.c with gcc (no contraction of multiply-adds)."""
-    srcs = [_SRC, os.path.join(_HERE, "bb_oracle_body.h")]
+    srcs = [_SRC, os.path.join(_HERE, "bb_oracle_body.h"), os.path.join(_HERE, "sb_oracle_body.h")]
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(s) for s in srcs)):
         return _LIB_PATH
@@ -62,6 +62,14 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).argtypes = [i64, i64, i64, p, i64, i64,
                                                                        ctypes.c_double]
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).restype = ci
+        getattr(lib, "oracle_sym_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64]
+        getattr(lib, "oracle_sym_reduce_band" + sfx).restype = ci
+        getattr(lib, "oracle_sym_reduce_dense" + sfx).argtypes = [i64, i64, i64, p]
+        getattr(lib, "oracle_sym_reduce_dense" + sfx).restype = ci
+        getattr(lib, "oracle_sym_extract_band" + sfx).argtypes = [i64, p, i64, p, p]
+        getattr(lib, "oracle_sym_extract_band" + sfx).restype = None
+        getattr(lib, "oracle_sym_step_band" + sfx).argtypes = [i64, i64, i64, p, i64, i64, i64]
+        getattr(lib, "oracle_sym_step_band" + sfx).restype = None
     return lib
 
 
@@ -176,6 +184,48 @@ def bidiagonal_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: in
     work = np.ascontiguousarray(band.copy())
     reduce_band_pipelined(work, n, bw, tw, threads, time_limit)
     return extract(work, n, bw + tw)
+
+
+# ------------------------------------------------ symmetric variant -------
+# Symmetric band -> tridiagonal (sb_oracle_body.h): lower band storage of shape
+# (n, ldab), A(i, j) = band[j, i - j] for 0 <= i - j < ldab, ldab >= bw + tw + 1.
+
+def sym_reduce_band(band: np.ndarray, n: int, bw: int, tw: int) -> np.ndarray:
+    """Reduce symmetric lower band storage to tridiagonal form in place."""
+    assert band.flags.c_contiguous and band.shape[0] == n
+    rc = getattr(_load(), "oracle_sym_reduce_band" + _sfx(band))(n, bw, tw, _ptr(band), band.shape[1])
+    if rc != 0:
+        raise ValueError("oracle_sym_reduce_band: invalid arguments")
+    return band
+
+
+def sym_reduce_dense(a: np.ndarray, bw: int, tw: int) -> np.ndarray:
+    """Reduce a dense symmetric row-major n x n array in place (both triangles)."""
+    assert a.flags.c_contiguous and a.shape[0] == a.shape[1]
+    rc = getattr(_load(), "oracle_sym_reduce_dense" + _sfx(a))(a.shape[0], bw, tw, _ptr(a))
+    if rc != 0:
+        raise ValueError("oracle_sym_reduce_dense: invalid arguments")
+    return a
+
+
+def sym_extract(band: np.ndarray, n: int):
+    """(d, e): diagonal and subdiagonal of the lower band storage."""
+    d = np.zeros(n, dtype=band.dtype)
+    e = np.zeros(max(n - 1, 0), dtype=band.dtype)
+    getattr(_load(), "oracle_sym_extract_band" + _sfx(band))(n, _ptr(band), band.shape[1], _ptr(d), _ptr(e))
+    return d, e
+
+
+def sym_step_band(band: np.ndarray, n: int, b: int, t: int, r: int, k: int) -> None:
+    """One step (sweep r, step k) of pass (b, t) in place (lower band storage)."""
+    getattr(_load(), "oracle_sym_step_band" + _sfx(band))(n, b, t, _ptr(band), band.shape[1], r, k)
+
+
+def tridiagonal(band: np.ndarray, n: int, bw: int, tw: int):
+    """(d, e) of the symmetric reduction of a copy of band (serial oracle)."""
+    work = np.ascontiguousarray(band.copy())
+    sym_reduce_band(work, n, bw, tw)
+    return sym_extract(work, n)
 
 
 def bidiagonal_singular_values(d: np.ndarray, e: np.ndarray) -> np.ndarray:

@@ -36,6 +36,10 @@
  * any schedule that respects the sweep dependencies gives the serial result
  * bitwise (also when run on host threads by oracle_reduce_band_pipelined);
  * power-of-two scaling commutes bitwise; diagonal and zero inputs.
+ *
+ * sb_oracle_body.h adds the symmetric variant (symmetric band -> tridiagonal
+ * by the same passes, one two-sided reflector per step), pinned the same way
+ * against LAPACK's dsytrd and eigenvalues.
  */
 #define _POSIX_C_SOURCE 200809L
 #include <float.h>
@@ -65,6 +69,7 @@ static double oracle_now_(void) {
 #define REAL_MIN_NORMAL DBL_MIN
 #define REAL_SAFMIN (DBL_MIN / (DBL_EPSILON * 0.5))
 #include "bb_oracle_body.h"
+#include "sb_oracle_body.h"
 #undef REAL
 #undef SFX
 #undef SQRT
@@ -83,4 +88,5 @@ static double oracle_now_(void) {
 #define REAL_MIN_NORMAL FLT_MIN
 #define REAL_SAFMIN (FLT_MIN / (FLT_EPSILON * 0.5f))
 #include "bb_oracle_body.h"
+#include "sb_oracle_body.h"
 #undef STEP_BODY

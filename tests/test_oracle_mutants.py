@@ -122,7 +122,9 @@ def bound_library(monkeypatch):
 
 
 def build_mutant(tmp_path, edits):
-    shutil.copy(os.path.join(ORACLE_DIR, "bb_oracle.c"), tmp_path / "bb_oracle.c")
+    for f in os.listdir(ORACLE_DIR):
+        if f.endswith((".c", ".h")) and f != "bb_oracle_body.h":
+            shutil.copy(os.path.join(ORACLE_DIR, f), tmp_path / f)
     with open(os.path.join(ORACLE_DIR, "bb_oracle_body.h")) as f:
         body = f.read()
     for old, new in edits:
