@@ -9,6 +9,16 @@ it.
 
 Functions take numpy arrays in the layout of ``band_inputs``: band storage of
 shape (n, ldab), A(i, j) = band[j, ku + i - j], ku = bw + tw.
+
+Also here:
+  * ``reduce_band_pipelined``: the same reduction on host threads (sweep r on
+    thread r mod P, "A two-stage reduction on an Apple M5 Pro", Section 6),
+    bitwise equal to the serial order;
+  * the symmetric variant (``sym_*``, ``tridiagonal``): symmetric band ->
+    tridiagonal by the same passes, lower band storage
+    A(i, j) = band[j, i - j];
+  * ``bidiagonal_singular_values``: singular values of a bidiagonal by the
+    Golub-Kahan tridiagonal's eigenvalues.
 """
 from __future__ import annotations
 
