@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -28,16 +29,36 @@ struct PassPlan {
     int b, t;
 };
 
-// b = bw; while b > 1: t = min(tw, b - 1); pass (b, t); b -= t.
+// Largest order (and so bandwidth) any entry point accepts.
+constexpr int64_t kMaxOrder = (int64_t)1 << 30;
+
+// The plan: b = bw; while b > 1: t = min(tw, b - 1); pass (b, t); b -= t.
+// Every pass but the last removes tw and the last ends at 1, so pass i is
+// b = bw - i tw, t = min(tw, b - 1), and there are ceil((bw - 1) / tw).
+int64_t count_passes(int64_t bw, int64_t tw) {
+    if (bw <= 1 || bw > kMaxOrder || tw < 1) return 0;
+    return (bw - 1 + tw - 1) / tw;
+}
+PassPlan pass_at(int64_t bw, int64_t tw, int64_t i) {
+    const int64_t b = bw - i * tw;
+    return {(int)b, (int)std::min(tw, b - 1)};
+}
+// The whole plan, for callers whose bandwidth is already bounded by the
+// shared-memory check of its widest pass (at most a few thousand passes).
 std::vector<PassPlan> plan_passes(int64_t bw, int64_t tw) {
     std::vector<PassPlan> out;
-    int64_t b = bw;
-    while (b > 1 && tw >= 1) {
-        int64_t t = std::min(tw, b - 1);
-        out.push_back({(int)b, (int)t});
-        b -= t;
-    }
+    const int64_t np = count_passes(bw, tw);
+    out.reserve((size_t)np);
+    for (int64_t i = 0; i < np; ++i) out.push_back(pass_at(bw, tw, i));
     return out;
+}
+
+// Shared memory of the flag kernel's tile for pass (b, t): the widest pass,
+// the first, decides whether a reduction fits.
+size_t flag_tile_bytes(int64_t b, int64_t t, size_t elem) {
+    const int64_t w = t + 1;
+    const int64_t wm = w <= 8 ? 8 : w <= 9 ? 9 : w <= 16 ? 16 : w <= 17 ? 17 : w <= 32 ? 32 : w <= 33 ? 33 : 65;
+    return elem * ((size_t)wm + 2 + (size_t)(2 * (b + t) + 1) * (size_t)(wm | 1));
 }
 
 // Half-step lag of the persistent scheduler: half-step h of sweep r waits for
@@ -113,27 +134,29 @@ const char* bb_last_error(void) { return g_last_error.c_str(); }
 
 int64_t bb_required_ldab(int64_t bw, int64_t tw) { return bw + 2 * tw + 1; }
 
-int64_t bb_num_passes(int64_t bw, int64_t tw) { return (int64_t)plan_passes(bw, tw).size(); }
+int64_t bb_num_passes(int64_t bw, int64_t tw) { return count_passes(bw, tw); }
 
 bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t) {
-    auto plan = plan_passes(bw, tw);
-    if (i < 0 || i >= (int64_t)plan.size() || !b || !t)
+    if (i < 0 || i >= count_passes(bw, tw) || !b || !t)
         return fail(BB_ERR_INVALID_ARG, "bb_pass_info: pass index out of range");
-    *b = plan[i].b;
-    *t = plan[i].t;
+    const PassPlan ps = pass_at(bw, tw, i);
+    *b = ps.b;
+    *t = ps.t;
     return BB_OK;
 }
 
 bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
                         int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds) {
-    auto plan = plan_passes(bw, tw);
-    if (pass < 0 || pass >= (int64_t)plan.size() || !g || !nslot || !ahead || !lds || n < 1 ||
-        n >= bb::kGroupMaxN || (elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
+    if (n < 1 || n >= bb::kGroupMaxN || bw < 0 || bw >= n || tw < 1 || tw > std::max<int64_t>(1, bw - 1) ||
+        pass < 0 || pass >= count_passes(bw, tw) || !g || !nslot || !ahead || !lds ||
+        (elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
         return fail(BB_ERR_INVALID_ARG, "bb_group_plan: argument out of range");
+    try {
+    const PassPlan ps = pass_at(bw, tw, pass);
     bb::PassArgs P{};
     P.n = n;
-    P.b = plan[pass].b;
-    P.t = plan[pass].t;
+    P.b = ps.b;
+    P.t = ps.t;
     P.bp = P.b - P.t;
     P.ku = (int)(bw + tw);
     P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
@@ -146,14 +169,19 @@ bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, i
     *ahead = ok ? ga.ahead : 0;
     *lds = ok ? ga.lds : 0;
     return BB_OK;
+    } catch (const std::bad_alloc&) {
+        return fail(BB_ERR_NOMEM, "bb_group_plan: host allocation failed");
+    } catch (...) {
+        return fail(BB_ERR_INTERNAL, "bb_group_plan: unexpected host exception");
+    }
 }
 
 double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass) {
-    auto plan = plan_passes(bw, tw);
     double total = 0;
-    for (int64_t pi = 0; pi < (int64_t)plan.size(); ++pi) {
+    const int64_t np = count_passes(bw, tw);
+    for (int64_t pi = 0; pi < np; ++pi) {
         if (pass >= 0 && pi != pass) continue;
-        const int b = plan[pi].b, t = plan[pi].t;
+        const int b = pass_at(bw, tw, pi).b, t = pass_at(bw, tw, pi).t;
         for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) {
             const int64_t K = steps_of_sweep(n, b, t, r);
             for (int64_t k = 0; k < K; ++k) {
@@ -170,11 +198,11 @@ double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int
 }
 
 int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass) {
-    auto plan = plan_passes(bw, tw);
     int64_t total = 0;
-    for (int64_t pi = 0; pi < (int64_t)plan.size(); ++pi) {
+    const int64_t np = count_passes(bw, tw);
+    for (int64_t pi = 0; pi < np; ++pi) {
         if (pass >= 0 && pi != pass) continue;
-        const int b = plan[pi].b, t = plan[pi].t;
+        const int b = pass_at(bw, tw, pi).b, t = pass_at(bw, tw, pi).t;
         for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) total += steps_of_sweep(n, b, t, r);
     }
     return total;
@@ -185,11 +213,15 @@ bb_handle* bb_create(int64_t n, int64_t bw, bb_dtype dtype) {
         fail(BB_ERR_DTYPE, "bb_create: unknown dtype");
         return nullptr;
     }
-    if (n < 1 || n > (int64_t)1 << 30 || bw < 0 || bw >= n) {
+    if (n < 1 || n > kMaxOrder || bw < 0 || bw >= n) {
         fail(BB_ERR_INVALID_ARG, "bb_create: need n >= 1 and 0 <= bw < n");
         return nullptr;
     }
-    bb_handle* h = new bb_handle();
+    bb_handle* h = new (std::nothrow) bb_handle();
+    if (!h) {
+        fail(BB_ERR_NOMEM, "bb_create: host allocation failed");
+        return nullptr;
+    }
     h->n = n;
     h->bw = bw;
     h->dtype = dtype;
@@ -332,15 +364,11 @@ static bb_status check_reduce_args(bb_handle* h, int64_t ldab, int64_t tw) {
     if (tw + 1 > bb::kMaxW) return fail(BB_ERR_INVALID_ARG, "tw > 64 is not supported");
     if (ldab < bb_required_ldab(h->bw, tw)) return fail(BB_ERR_LDAB, "ldab < bw + 2*tw + 1");
     if ((double)ldab * (double)h->n > 9.0e18 / 8) return fail(BB_ERR_INVALID_ARG, "band too large");
-    // shared memory of the widest pass (the first): tile of (b + t + 1) columns
-    auto plan = plan_passes(h->bw, tw);
-    for (auto& ps : plan) {
-        int w = ps.t + 1;
-        int wm = w <= 8 ? 8 : w <= 9 ? 9 : w <= 16 ? 16 : w <= 17 ? 17 : w <= 32 ? 32 : w <= 33 ? 33 : 65;
-        size_t smem = elem_size(h->dtype) * ((size_t)wm + 2 + (size_t)(2 * (ps.b + ps.t) + 1) * (wm | 1));
-        if (smem > 227 * 1024)
-            return fail(BB_ERR_INVALID_ARG, "bandwidth too large for the shared-memory tile");
-    }
+    // shared memory of the widest pass (the first): tile of (b + t + 1)
+    // columns; later passes have a smaller b and no larger t
+    if (count_passes(h->bw, tw) > 0 &&
+        flag_tile_bytes(h->bw, std::min<int64_t>(tw, h->bw - 1), elem_size(h->dtype)) > 227 * 1024)
+        return fail(BB_ERR_INVALID_ARG, "bandwidth too large for the shared-memory tile");
     return BB_OK;
 }
 
@@ -499,8 +527,8 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
 
 extern "C" {
 
-bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
-                    void* e_out, bb_stream_t stream) {
+static bb_status reduce_checked(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
+                                void* e_out, bb_stream_t stream) {
     bb_status st = check_reduce_args(h, ldab, tw);
     if (st != BB_OK) return st;
     if (!band_ptr || !d_out || (h->n > 1 && !e_out))
@@ -512,6 +540,19 @@ bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void
     if (h->dtype == BB_F32)
         return reduce_impl<float>(h, (float*)band_ptr, ldab, tw, (float*)d_out, (float*)e_out, s);
     return reduce_impl<double>(h, (double*)band_ptr, ldab, tw, (double*)d_out, (double*)e_out, s);
+}
+
+// No C++ exception crosses the C ABI: host allocation failures (the handle's
+// per-pass bookkeeping) come back as BB_ERR_NOMEM.
+bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
+                    void* e_out, bb_stream_t stream) {
+    try {
+        return reduce_checked(h, band_ptr, ldab, tw, d_out, e_out, stream);
+    } catch (const std::bad_alloc&) {
+        return fail(BB_ERR_NOMEM, "bb_reduce: host allocation failed");
+    } catch (...) {
+        return fail(BB_ERR_INTERNAL, "bb_reduce: unexpected host exception");
+    }
 }
 
 bb_status bb_reduce_host(bb_handle* h, const void* band_host, int64_t ldab, int64_t tw,

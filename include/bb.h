@@ -79,8 +79,9 @@ bb_handle* bb_create(int64_t n, int64_t bw, bb_dtype dtype);
  * handle's status word and reported by bb_status_sync.  When a pass runs on
  * the group kernel and the band's base or column stride is not a multiple of
  * 16 bytes, the first such call allocates the handle's working copy (n x ldab
- * rounded up to 16 bytes; BB_ERR_NOMEM if that fails).  Covers the paper's
- * Algorithms 1 and 2 (Section III). */
+ * rounded up to 16 bytes; BB_ERR_NOMEM if that fails).  No C++ exception
+ * leaves the library: a failed host allocation is BB_ERR_NOMEM.  Covers the
+ * paper's Algorithms 1 and 2 (Section III). */
 bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
                     void* e_out, bb_stream_t stream);
 
@@ -143,7 +144,11 @@ enum {
 bb_status bb_set_param(bb_handle* h, int param, int64_t value);
 int64_t bb_get_param(const bb_handle* h, int param);
 
-/* Pass plan of (bw, tw): number of passes, and the (b, t) of pass i. */
+/* Pass plan of (bw, tw) (b = bw; while b > 1: t = min(tw, b - 1); b -= t):
+ * the number of passes, ceil((bw - 1) / tw), and the (b, t) of pass i,
+ * b = bw - i tw, t = min(tw, b - 1).  Host-only and computed in closed form;
+ * bb_num_passes returns 0 when bw <= 1, tw < 1 or bw > 2^30, and
+ * bb_pass_info BB_ERR_INVALID_ARG for an index outside the plan. */
 int64_t bb_num_passes(int64_t bw, int64_t tw);
 bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t);
 
@@ -152,7 +157,9 @@ bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t
  * cannot take the pass), the columns of its shared-memory buffer (nslot),
  * the loader's run-ahead in ticks, and the rows a buffered column holds
  * (lds).  group_size as BB_PARAM_GROUP_SIZE (0 = the largest that fits).
- * Host-only, for inspection and tests. */
+ * Host-only, for inspection and tests.  BB_ERR_INVALID_ARG unless
+ * 1 <= n < 2^30, 0 <= bw < n, 1 <= tw <= max(1, bw - 1), the pass is in the
+ * plan, elem_bytes is 4 or 8 and group_size >= 0. */
 bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
                         int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds);
 

@@ -112,3 +112,21 @@ def test_singular_values_argument_errors_need_no_gpu(lib):
     assert lib.bb_singular_values(bb.BB_F32, 4, fake, fake, None, None) == bb.BB_ERR_INVALID_ARG
     assert lib.bb_singular_values(7, 4, fake, fake, fake, None) == bb.BB_ERR_DTYPE
     assert "bb_singular_values" in bb.bb_last_error()
+
+
+def test_pass_count_is_arithmetic_and_bounded(lib):
+    # the plan is never materialised for these: a huge bandwidth costs nothing
+    assert bb.bb_num_passes((1 << 30) - 1, 1) == (1 << 30) - 2
+    assert bb.bb_num_passes((1 << 30) + 1, 1) == 0          # beyond any accepted order
+    assert bb.bb_pass_info((1 << 30) - 1, 1, (1 << 30) - 3) == (2, 1)
+    for bw in range(0, 70):
+        for tw in range(1, 12):
+            assert bb.bb_num_passes(bw, tw) == len(_plan(bw, tw))
+    assert bb.bb_num_passes(16, 0) == 0 and bb.bb_num_passes(-3, 2) == 0
+
+
+def test_group_plan_rejects_inconsistent_shapes(lib):
+    for args in ((100, 100, 8, 4, 0), (100, 16, 0, 4, 0), (100, 16, 16, 4, 0), (100, 16, 8, 2, 0),
+                 (0, 0, 1, 4, 0), (100, 16, 8, 4, -1)):
+        with pytest.raises(bb.BBError):
+            bb.bb_group_plan(*args)
