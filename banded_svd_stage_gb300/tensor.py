@@ -35,8 +35,10 @@ class Reducer:
     def reduce_(self, band: torch.Tensor, tw: int, d: torch.Tensor | None = None,
                 e: torch.Tensor | None = None, stream=None):
         """Reduce band (CUDA, (n, ldab), contiguous) in place; returns (d, e)."""
-        assert band.is_cuda and band.is_contiguous() and band.dtype == self.dtype
-        assert band.shape[0] == self.n
+        if not (band.is_cuda and band.is_contiguous() and band.dtype == self.dtype):
+            raise ValueError("band must be a contiguous CUDA tensor of the reducer's dtype")
+        if band.dim() != 2 or band.shape[0] != self.n:
+            raise ValueError(f"band must have shape ({self.n}, ldab)")
         if d is None:
             d = torch.empty(self.n, dtype=self.dtype, device=band.device)
         if e is None:
