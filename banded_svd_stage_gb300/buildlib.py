@@ -18,7 +18,14 @@ BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
 LIB_PATH = os.path.join(HERE, "libbb.so")
 SOURCES = ["bb_api.cu", "bb_kernels_f32.cu", "bb_kernels_f64.cu", "bb_kernels_f32_narrow.cu",
            "bb_kernels_f32_wide.cu", "bb_kernels_f64_narrow.cu", "bb_kernels_f64_wide.cu", "bb_noalloc.cu",
-           "bb_svals.cu"]
+           "bb_svals.cu", "bb_plan.cu"]
+# The pass kernels: their device code and the host planner that fixes their
+# launch shape.  The C-ABI checks (bb_api.cu), the allocation-free entry
+# (bb_noalloc.cu) and the singular-value kernel (bb_svals.cu) are not part of
+# them.
+PASS_KERNEL_SOURCES = ["bb_device.cuh", "bb_group.cuh", "bb_launch.cuh", "bb_internal.h", "bb_plan.cu",
+                       "bb_kernels_f32.cu", "bb_kernels_f64.cu", "bb_kernels_f32_narrow.cu",
+                       "bb_kernels_f32_wide.cu", "bb_kernels_f64_narrow.cu", "bb_kernels_f64_wide.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -83,14 +90,13 @@ if __name__ == "__main__":
 
 
 def source_digest() -> str:
-    """sha256 of the library's CUDA sources under csrc/ (identifies a kernel
-    build; the public header's documentation does not change the kernels)."""
+    """sha256 of the pass kernels' sources (PASS_KERNEL_SOURCES): it changes
+    exactly when a pass kernel or its launch plan may have changed, so DRAM
+    counters taken under another digest no longer describe the kernel."""
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
-    for f in sorted(_deps()):
-        if f.endswith((".cu", ".cuh", ".h")) and os.path.abspath(f).startswith(csrc + os.sep):
-            h.update(os.path.basename(f).encode())
-            with open(f, "rb") as fh:
-                h.update(fh.read())
+    for f in PASS_KERNEL_SOURCES:
+        h.update(f.encode())
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]

@@ -12,7 +12,7 @@
 //     registers;
 //   - the three-cycle separation between consecutive sweeps is what makes
 //     concurrent sweeps safe; here it is refined to half-step granularity
-//     (see pass_lag_half in bb_api.cu).
+//     (see pass_lag_half in bb_plan.cu).
 // The Householder reflector uses the LAPACK xLARFG convention.
 //
 // Band storage: A(i, j) = band[(ku + i - j) + j * ldab], so with

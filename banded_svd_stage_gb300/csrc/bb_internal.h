@@ -106,6 +106,10 @@ cudaError_t run_extract(const T* band, long long n, long long ldab, int ku, T* d
 
 // Threads per block the launcher uses for a pass when none is requested.
 int auto_tpb(int b, int t);
+// Half-step lag of the persistent schedulers and cycle lag of the per-cycle
+// scheduler for pass (b, t) (bb_plan.cu).
+int pass_lag_half(int b, int t);
+int pass_lag_cycle(int b, int t);
 
 // Set the message bb_last_error() returns on the calling thread.
 void set_last_error(const char* msg);

@@ -97,8 +97,8 @@ bb_status run_all(T* band, int64_t n, int64_t bw, int64_t ldab, int64_t tw, T* d
         P.bp = (int)(b - t);
         P.ku = ku;
         P.nsweeps = (int)std::max<int64_t>(0, n - (b - t) - 1);
-        P.lag = (b > t + 1) ? 2 : 3;
-        P.lagh = (b - t >= 3) ? 2 : (b - t == 2 ? 3 : 4);
+        P.lag = bb::pass_lag_cycle((int)b, (int)t);
+        P.lagh = bb::pass_lag_half((int)b, (int)t);
         P.stall_sweep = -1;
         P.wait_budget = 4000ULL * (unsigned long long)slot.clock_khz;  // 4 s
         bb::LaunchCfg cfg;

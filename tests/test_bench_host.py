@@ -71,3 +71,19 @@ def test_cpu_legs_report_rates_and_threads():
     big = bi.by_name("n4096_bw16_tw8_f32")
     cores = len(os.sched_getaffinity(0))
     assert min(cores, 16) == max(1, min(cores, 2 * big.n // (3 * big.bw), big.n // 256))
+
+
+def test_traffic_digest_covers_the_pass_kernels_only():
+    import banded_svd_stage_gb300.buildlib as bl
+    srcs = set(bl.PASS_KERNEL_SOURCES)
+    for f in srcs:
+        assert os.path.exists(os.path.join(bl.CSRC, f)), f
+    # every file defining a pass kernel, and the planner that launches it
+    for f in os.listdir(bl.CSRC):
+        text = open(os.path.join(bl.CSRC, f)).read()
+        if "__global__" in text and "pass_" in text and f.endswith((".cu", ".cuh")):
+            assert f in srcs, f
+    assert "bb_plan.cu" in srcs and "bb_launch.cuh" in srcs
+    # the boundary and the other kernels are not part of it
+    assert not srcs & {"bb_api.cu", "bb_noalloc.cu", "bb_svals.cu"}
+    assert len(bl.source_digest()) == 16
