@@ -80,6 +80,9 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, "oracle_sym_extract_band" + sfx).restype = None
         getattr(lib, "oracle_sym_step_band" + sfx).argtypes = [i64, i64, i64, p, i64, i64, i64]
         getattr(lib, "oracle_sym_step_band" + sfx).restype = None
+        getattr(lib, "oracle_sym_reduce_band_pipelined" + sfx).argtypes = [i64, i64, i64, p, i64, i64,
+                                                                           ctypes.c_double]
+        getattr(lib, "oracle_sym_reduce_band_pipelined" + sfx).restype = ci
     return lib
 
 
@@ -224,6 +227,23 @@ def sym_extract(band: np.ndarray, n: int):
     e = np.zeros(max(n - 1, 0), dtype=band.dtype)
     getattr(_load(), "oracle_sym_extract_band" + _sfx(band))(n, _ptr(band), band.shape[1], _ptr(d), _ptr(e))
     return d, e
+
+
+def sym_reduce_band_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: int,
+                              time_limit: float = 600.0) -> np.ndarray:
+    """sym_reduce_band on host threads (sweep r on thread r mod threads, step k
+    of sweep r after sweep r-1 finished min(k + L, its steps), L = 2, or 3
+    when b - t = 1).  Bitwise equal to sym_reduce_band."""
+    assert band.flags.c_contiguous and band.shape[0] == n
+    rc = getattr(_load(), "oracle_sym_reduce_band_pipelined" + _sfx(band))(
+        n, bw, tw, _ptr(band), band.shape[1], threads, float(time_limit))
+    if rc == -1:
+        raise ValueError("oracle_sym_reduce_band_pipelined: invalid arguments")
+    if rc == -2:
+        raise TimeoutError("oracle_sym_reduce_band_pipelined: time limit reached")
+    if rc != 0:
+        raise RuntimeError("oracle_sym_reduce_band_pipelined: could not start the threads")
+    return band
 
 
 def sym_step_band(band: np.ndarray, n: int, b: int, t: int, r: int, k: int) -> None:

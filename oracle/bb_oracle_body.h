@@ -248,21 +248,13 @@ static void* FN(pipe_worker_)(void* arg) {
     return NULL;
 }
 
-/* Same arguments and result as oracle_reduce_band over all passes, on
- * nthreads (1 .. 1024) threads.  Returns 0; -1 on invalid arguments; -2 when
- * time_limit_s ran out (the band is then partly reduced); -3 when the
- * threads or the counters could not be created. */
-int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab,
-                                     int64_t nthreads, double time_limit_s) {
-    if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
-    if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
-    if (tw + 1 > ORACLE_WMAX) return -1;
-    if (nthreads < 1 || nthreads > 1024 || !(time_limit_s > 0)) return -1;
+/* Runs every pass of the plan on nthreads threads with `worker` (the
+ * bidiagonal or the symmetric one), joining the threads between passes.
+ * Returns 0, -2 when the time limit ran out, -3 when the threads or the
+ * counters could not be created. */
+static int FN(pipe_run_)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab, int64_t nthreads,
+                         double time_limit_s, void* (*worker)(void*)) {
     const int64_t ku = bw + tw;
-    for (int64_t j = 0; j < n; ++j) {
-        for (int64_t q = 0; q < tw; ++q) band[q + j * ldab] = 0;
-        for (int64_t q = ku + 1; q <= ku + tw; ++q) band[q + j * ldab] = 0;
-    }
     _Atomic int64_t* done = (_Atomic int64_t*)malloc((size_t)n * sizeof(_Atomic int64_t));
     pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
     FN(pipe_arg_)* args = (FN(pipe_arg_)*)malloc((size_t)nthreads * sizeof(FN(pipe_arg_)));
@@ -279,7 +271,7 @@ int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* ba
         int64_t P = nthreads < nsweeps ? nthreads : nsweeps, started = 0;
         for (int64_t q = 0; q < P; ++q) {
             args[q] = (FN(pipe_arg_)){n, b, t, ku, ldab, P, q, band, done, &stop, deadline};
-            if (pthread_create(&th[q], NULL, FN(pipe_worker_), &args[q]) != 0) {
+            if (pthread_create(&th[q], NULL, worker, &args[q]) != 0) {
                 atomic_store_explicit(&stop, 1, memory_order_relaxed);
                 rc = -3;
                 break;
@@ -294,6 +286,24 @@ int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* ba
     free(th);
     free(args);
     return rc;
+}
+
+/* Same arguments and result as oracle_reduce_band over all passes, on
+ * nthreads (1 .. 1024) threads.  Returns 0; -1 on invalid arguments; -2 when
+ * time_limit_s ran out (the band is then partly reduced); -3 when the
+ * threads or the counters could not be created. */
+int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab,
+                                     int64_t nthreads, double time_limit_s) {
+    if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
+    if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
+    if (tw + 1 > ORACLE_WMAX) return -1;
+    if (nthreads < 1 || nthreads > 1024 || !(time_limit_s > 0)) return -1;
+    const int64_t ku = bw + tw;
+    for (int64_t j = 0; j < n; ++j) {
+        for (int64_t q = 0; q < tw; ++q) band[q + j * ldab] = 0;
+        for (int64_t q = ku + 1; q <= ku + tw; ++q) band[q + j * ldab] = 0;
+    }
+    return FN(pipe_run_)(n, bw, tw, band, ldab, nthreads, time_limit_s, FN(pipe_worker_));
 }
 
 /* d_i = A(i, i), e_i = A(i, i+1) from band storage. */

@@ -121,6 +121,45 @@ void FN(oracle_sym_step_band)(int64_t n, int64_t b, int64_t t, REAL* band, int64
     SYM_STEP_BODY(p + 1, c - 1, ce + 1, cend);
 }
 
+/* Pipelined sweeps on host threads, as oracle_reduce_band_pipelined, one
+ * step per unit: step k of sweep r starts once sweep r-1 has finished
+ * min(k + L, K_{r-1}) steps, L = 2 when b - t >= 2 and 3 when b - t == 1 (the
+ * least lockstep lag of this variant); the last step of a sweep waits for all
+ * of sweep r-1. */
+static void* FN(sym_pipe_worker_)(void* arg) {
+    const FN(pipe_arg_)* a = (const FN(pipe_arg_)*)arg;
+    const int64_t n = a->n, b = a->b, t = a->t;
+    const int64_t L = (b - t >= 2) ? 2 : 3;
+    const int64_t nsweeps = n - (b - t) - 1;
+    for (int64_t r = a->thread; r < nsweeps; r += a->nthreads) {
+        const int64_t K = FN(oracle_sweep_steps)(n, b, t, r);
+        const int64_t Kp = (r > 0) ? FN(oracle_sweep_steps)(n, b, t, r - 1) : 0;
+        for (int64_t k = 0; k < K; ++k) {
+            if (r > 0) {
+                int64_t need = (k + L < Kp) ? k + L : Kp;
+                if (k == K - 1) need = Kp;
+                if (!FN(pipe_wait_)(&a->done[r - 1], need, a)) return NULL;
+            }
+            FN(oracle_sym_step_band)(n, b, t, a->band, a->ldab, r, k);
+            atomic_store_explicit(&a->done[r], k + 1, memory_order_release);
+        }
+    }
+    return NULL;
+}
+
+/* Same arguments and result as oracle_sym_reduce_band, on nthreads (1 ..
+ * 1024) threads; return codes as oracle_reduce_band_pipelined. */
+int FN(oracle_sym_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab,
+                                         int64_t nthreads, double time_limit_s) {
+    if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + tw + 1) return -1;
+    if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
+    if (tw + 1 > ORACLE_WMAX) return -1;
+    if (nthreads < 1 || nthreads > 1024 || !(time_limit_s > 0)) return -1;
+    for (int64_t j = 0; j < n; ++j)
+        for (int64_t q = bw + 1; q <= bw + tw; ++q) band[q + j * ldab] = 0;
+    return FN(pipe_run_)(n, bw, tw, band, ldab, nthreads, time_limit_s, FN(sym_pipe_worker_));
+}
+
 /* d_i = A(i, i), e_i = A(i+1, i) from the lower band storage. */
 void FN(oracle_sym_extract_band)(int64_t n, const REAL* band, int64_t ldab, REAL* d, REAL* e) {
     for (int64_t i = 0; i < n; ++i) d[i] = GET(i, i);

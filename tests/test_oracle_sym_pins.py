@@ -232,6 +232,73 @@ def test_symmetric_short_lag_is_detected():
     assert not np.array_equal(run_lockstep(sb, n, bw, tw, lambda b, t: sym_lag(b, t) - 1), serial)
 
 
+def async_order_run(sb, n, bw, tw, seed, lag_of):
+    """Random interleaving allowed by the progress-flag rule: step k of sweep
+    r starts once sweep r-1 has finished min(k + L, K_{r-1}) steps, and the
+    last step of a sweep once all of sweep r-1 is done."""
+    import random
+    work = sb.copy()
+    work[:, bw + 1:bw + tw + 1] = 0
+    rng = random.Random(seed)
+    for (b, t) in oracle.pass_plan(bw, tw):
+        L = lag_of(b, t)
+        K = {r: oracle.sweep_steps(n, b, t, r) for r in range(n)}
+        S = [r for r in K if K[r] > 0]
+        done = {r: 0 for r in S}
+        while True:
+            ready = []
+            for r in S:
+                k = done[r]
+                if k >= K[r]:
+                    continue
+                if r > 0:
+                    need = K[r - 1] if k == K[r] - 1 else min(k + L, K[r - 1])
+                    if done[r - 1] < need:
+                        continue
+                ready.append(r)
+            if not ready:
+                break
+            # prefer later sweeps, the order most likely to expose a race
+            r = max(ready) if rng.random() < 0.7 else rng.choice(ready)
+            oracle.sym_step_band(work, n, b, t, r, done[r])
+            done[r] += 1
+        assert all(done[r] == K[r] for r in S)
+    return work
+
+
+ASYNC_CASES = [(40, 8, 3), (40, 8, 7), (48, 6, 4), (48, 6, 5), (60, 16, 14), (33, 5, 2), (64, 16, 8),
+               (50, 3, 2), (50, 3, 1), (70, 24, 7), (30, 2, 1), (45, 12, 11)]
+
+
+@pytest.mark.parametrize("n,bw,tw", ASYNC_CASES)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_symmetric_progress_rule_reproduces_serial_bitwise(n, bw, tw, seed):
+    sb = bi.make_sym_band(n, bw, tw, "f64", seed=n + bw)
+    serial = sb.copy()
+    oracle.sym_reduce_band(serial, n, bw, tw)
+    assert np.array_equal(async_order_run(sb, n, bw, tw, seed, sym_lag), serial)
+
+
+def test_symmetric_progress_rule_with_short_lag_fails():
+    n, bw, tw = 40, 8, 3
+    sb = bi.make_sym_band(n, bw, tw, "f64", seed=n + bw)
+    serial = sb.copy()
+    oracle.sym_reduce_band(serial, n, bw, tw)
+    assert not np.array_equal(async_order_run(sb, n, bw, tw, 0, lambda b, t: sym_lag(b, t) - 1), serial)
+
+
+@pytest.mark.parametrize("n,bw,tw", ASYNC_CASES + [(2, 1, 1), (3, 2, 1), (700, 32, 8), (600, 9, 8)])
+@pytest.mark.parametrize("dt", ["f64", "f32"])
+def test_symmetric_pipelined_threads_reproduce_serial_bitwise(n, bw, tw, dt):
+    sb = bi.make_sym_band(n, bw, tw, dt, seed=n + tw)
+    serial = sb.copy()
+    oracle.sym_reduce_band(serial, n, bw, tw)
+    for threads in (1, 2, 3, 8):
+        work = sb.copy()
+        oracle.sym_reduce_band_pipelined(work, n, bw, tw, threads)
+        assert np.array_equal(work, serial), threads
+
+
 # ----------------------------------------------------------- planted mistakes
 
 SYM_MUTANTS = {
