@@ -133,7 +133,8 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
-def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int, with_e2e: bool):
+def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int, with_e2e: bool,
+             group_size: int = 0):
     import torch
 
     import banded_svd_stage_gb300 as bb
@@ -147,6 +148,8 @@ def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int,
     work = torch.empty_like(pristine)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     red = Reducer(w.n, w.bw, tdt, scheduler=scheduler)
+    if group_size:
+        bb.bb_set_param(red.h, bb.BB_PARAM_GROUP_SIZE, group_size)
     red.enable_timing(True)
     d = torch.empty(w.n, dtype=tdt, device=dev)
     e = torch.empty(w.n, dtype=tdt, device=dev)
@@ -388,6 +391,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=MAIN_WORKLOAD)
     ap.add_argument("--scheduler", type=int, default=0)
+    ap.add_argument("--group-size", type=int, default=0,
+                    help="sweeps per CTA of the group kernel (0: the planner's choice)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (e2e) leg")
@@ -438,7 +443,8 @@ def main():
     if sampler:
         sampler.start()
     t_wall0 = time.perf_counter()
-    res = run_ours(w, args.steps, args.warmup, args.scheduler, rank, with_e2e=(world == 1 and not args.no_e2e))
+    res = run_ours(w, args.steps, args.warmup, args.scheduler, rank, with_e2e=(world == 1 and not args.no_e2e),
+                   group_size=args.group_size)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -465,7 +471,8 @@ def main():
             if name == w.name:
                 continue
             ww = bi.by_name(name)
-            r2 = run_ours(ww, max(2, min(args.steps, 3)), 1, args.scheduler, rank, with_e2e=False)
+            r2 = run_ours(ww, max(2, min(args.steps, 3)), 1, args.scheduler, rank, with_e2e=False,
+                          group_size=args.group_size)
             m2 = statistics.median(r2["ms"])
             g2 = r2["model_bytes"] / (m2 * 1e-3) / 1e9
             sweep.append({"workload": name, "ms_per_reduction": m2, "min_ms": min(r2["ms"]),
@@ -490,6 +497,7 @@ def main():
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "n": w.n, "bw": w.bw, "tw": w.tw, "dist": w.dist,
                        "graded": w.graded, "scheduler": SCHEDULER_NAMES.get(args.scheduler, str(args.scheduler)),
+                       "group_size": args.group_size or "planner",
                        "l2": "flushed between steps (256 MiB write); band restored before each step",
                        "parallelism": f"replicas x{world}"},
             "frac_of_hbm": value / hbm,
