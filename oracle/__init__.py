@@ -20,7 +20,9 @@ Also here:
   * ``bidiagonal_singular_values``: singular values of a bidiagonal by the
     Golub-Kahan tridiagonal's eigenvalues;
   * ``bidiagonal_with_vectors``: the reduction with its reflectors kept and
-    applied to the identity, A = U B V^T (the back-transformation).
+    applied to the identity, A = U B V^T (the back-transformation);
+  * ``dense_to_band``: stage 1, a dense matrix to upper band form by block
+    Householder (numpy, with this oracle's larfg).
 """
 from __future__ import annotations
 
@@ -249,6 +251,50 @@ def bidiagonal_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: in
     work = np.ascontiguousarray(band.copy())
     reduce_band_pipelined(work, n, bw, tw, threads, time_limit)
     return extract(work, n, bw + tw)
+
+
+# ------------------------------------------------ stage 1: dense -> band ---
+
+def dense_to_band(a: np.ndarray, bw: int) -> np.ndarray:
+    """Stage 1 of the two-stage SVD: an n x n matrix reduced to upper band
+    form of bandwidth bw by orthogonal transformations, the "classical block
+    Householder reduction" of the accuracy protocol ("Accelerating
+    Bidiagonalization of Banded Matrices through Memory-Aware Bulge-Chasing on
+    GPUs", Section V; the GPU stage of "A two-stage reduction on an Apple M5
+    Pro" uses the same panels).  For each panel of bw columns k .. k+bw-1:
+    QR of the panel column by column (reflector of A(j.., j), applied from the
+    left to every later column), then LQ of the panel's rows to the right of
+    the band, row by row (reflector of A(i, i+bw ..), applied from the right
+    to every later row).  Reflectors are this oracle's larfg; annihilated
+    entries are set to exactly zero.  Returns a new array (same dtype)."""
+    a = np.array(a, copy=True)
+    n = a.shape[0]
+    if bw < 1:
+        raise ValueError("bw must be at least 1")
+    for k in range(0, n, bw):
+        kb = min(k + bw, n)
+        for j in range(k, kb):
+            if j + 1 >= n:
+                break
+            beta, v, tau = larfg(a[j, j], a[j + 1:, j].copy())
+            a[j, j] = beta
+            a[j + 1:, j] = 0
+            if tau != 0:
+                u = np.concatenate([[1.0], v]).astype(a.dtype)
+                y = u @ a[j:, j + 1:]
+                a[j:, j + 1:] -= tau * np.outer(u, y)
+        for i in range(k, kb):
+            c0 = i + bw
+            if c0 + 1 >= n:
+                break
+            beta, v, tau = larfg(a[i, c0], a[i, c0 + 1:].copy())
+            a[i, c0] = beta
+            a[i, c0 + 1:] = 0
+            if tau != 0:
+                u = np.concatenate([[1.0], v]).astype(a.dtype)
+                y = a[i + 1:, c0:] @ u
+                a[i + 1:, c0:] -= tau * np.outer(y, u)
+    return a
 
 
 # ------------------------------------------------ symmetric variant -------
