@@ -22,7 +22,9 @@ Also here:
   * ``bidiagonal_with_vectors``: the reduction with its reflectors kept and
     applied to the identity, A = U B V^T (the back-transformation);
   * ``dense_to_band``: stage 1, a dense matrix to upper band form by block
-    Householder (numpy, with this oracle's larfg).
+    Householder (numpy, with this oracle's larfg);
+  * half-precision storage: a float16 band is reduced with float arithmetic,
+    every entry written back rounded to binary16 (``has_half``).
 """
 from __future__ import annotations
 
@@ -60,7 +62,11 @@ def compile_library(src: str, out: str) -> str:
 def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     """Declare the argument and result types of the oracle's C functions."""
     i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-    for sfx in ("_d", "_f"):
+    lib.oracle_has_half.argtypes = []
+    lib.oracle_has_half.restype = ci
+    for sfx in ("_d", "_f", "_h"):
+        if sfx == "_h" and not lib.oracle_has_half():
+            continue
         getattr(lib, "oracle_larfg" + sfx).argtypes = [i64, p, p, i64, p]
         getattr(lib, "oracle_larfg" + sfx).restype = None
         getattr(lib, "oracle_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64, i64, i64]
@@ -78,6 +84,8 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).restype = ci
         getattr(lib, "oracle_reduce_band_record" + sfx).argtypes = [i64, i64, i64, p, i64, i64, p, p, p, p, p]
         getattr(lib, "oracle_reduce_band_record" + sfx).restype = i64
+        if sfx == "_h":
+            continue  # the symmetric variant has no half-precision storage instantiation
         getattr(lib, "oracle_sym_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64]
         getattr(lib, "oracle_sym_reduce_band" + sfx).restype = ci
         getattr(lib, "oracle_sym_reduce_dense" + sfx).argtypes = [i64, i64, i64, p]
@@ -104,7 +112,21 @@ def _sfx(arr: np.ndarray) -> str:
         return "_d"
     if arr.dtype == np.float32:
         return "_f"
+    if arr.dtype == np.float16:
+        if not has_half():
+            raise TypeError("this build of the oracle has no half-precision storage (no _Float16)")
+        return "_h"
     raise TypeError(f"unsupported dtype {arr.dtype}")
+
+
+def has_half() -> bool:
+    """Whether the oracle was built with the half-precision storage variant."""
+    return bool(_load().oracle_has_half())
+
+
+def _arith(dt) -> np.dtype:
+    """Arithmetic type of a band of dtype dt (float for half storage)."""
+    return np.dtype(np.float32) if np.dtype(dt) == np.float16 else np.dtype(dt)
 
 
 def _ptr(a: np.ndarray):
@@ -176,8 +198,8 @@ def reduce_band_record(band: np.ndarray, n: int, bw: int, tw: int):
     side = np.zeros(cap, dtype=np.int8)
     start = np.zeros(cap, dtype=np.int64)
     width = np.zeros(cap, dtype=np.int32)
-    taus = np.zeros(cap, dtype=band.dtype)
-    vs = np.zeros((cap, tw + 1), dtype=band.dtype)
+    taus = np.zeros(cap, dtype=_arith(band.dtype))
+    vs = np.zeros((cap, tw + 1), dtype=_arith(band.dtype))
     got = getattr(_load(), "oracle_reduce_band_record" + _sfx(band))(
         n, bw, tw, _ptr(band), band.shape[1], cap, _ptr(side), _ptr(start), _ptr(width), _ptr(taus), _ptr(vs))
     if got == -1:
@@ -231,8 +253,9 @@ def sweep_steps(n: int, b: int, t: int, r: int) -> int:
 
 
 def extract(band: np.ndarray, n: int, ku: int):
-    d = np.zeros(n, dtype=band.dtype)
-    e = np.zeros(max(n - 1, 0), dtype=band.dtype)
+    """(d, e) of band storage, in the arithmetic type (float for half storage)."""
+    d = np.zeros(n, dtype=_arith(band.dtype))
+    e = np.zeros(max(n - 1, 0), dtype=_arith(band.dtype))
     getattr(_load(), "oracle_extract_band" + _sfx(band))(n, ku, _ptr(band), band.shape[1],
                                                          _ptr(d), _ptr(e))
     return d, e
