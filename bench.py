@@ -470,7 +470,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
                 "data": "synthetic", "config": {"workload": w.name, "n": w.n, "bw": w.bw, "tw": w.tw},
-                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                                  "sample": f"whole serial reductions of {w.name}, one per step"},
                 "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
