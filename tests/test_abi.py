@@ -130,3 +130,9 @@ def test_group_plan_rejects_inconsistent_shapes(lib):
                  (0, 0, 1, 4, 0), (100, 16, 8, 4, -1)):
         with pytest.raises(bb.BBError):
             bb.bb_group_plan(*args)
+
+
+def test_singular_value_lanes_are_validated_without_a_gpu(lib):
+    fake = 0x1000  # never dereferenced: rejected before any CUDA call
+    for lanes in (-1, 3, 6, 33, 64):
+        assert lib.bb_singular_values_lanes(bb.BB_F64, 8, fake, fake, fake, lanes, None) == bb.BB_ERR_INVALID_ARG
