@@ -342,6 +342,27 @@ def _model_bytes_py(w):
     return tot
 
 
+def latency_chain(n: int, bw: int, tw: int, pass_ms):
+    """Per pass of the plan: the sweeps, the half-step lag L between
+    consecutive sweeps (2 when b - t >= 3, 3 when b - t == 2, 4 when
+    b - t == 1) and the measured time per lag unit, pass_ms / (sweeps * L).
+    A pass is a chain of about sweeps * L dependent half-steps, so this is
+    the effective latency of one link, the quantity the kernels must lower
+    (the bytes a link moves are fixed by the method)."""
+    out = []
+    b, i = bw, 0
+    while b > 1 and i < len(pass_ms):
+        t = min(tw, b - 1)
+        bp = b - t
+        lag = 2 if bp >= 3 else (3 if bp == 2 else 4)
+        sweeps = max(0, n - bp - 1)
+        us = (pass_ms[i] * 1e3 / (sweeps * lag)) if sweeps and pass_ms[i] is not None else None
+        out.append({"b": b, "t": t, "sweeps": sweeps, "lag": lag, "us_per_link": us})
+        b -= t
+        i += 1
+    return out
+
+
 KERNEL_NAMES = {1: "pass_cycle_kernel", 2: "pass_persistent_kernel", 3: "pass_group_kernel",
                 4: "pass_cycle_kernel"}
 SCHEDULER_NAMES = {0: "auto", 1: "per-cycle", 2: "flags", 3: "group", 4: "per-cycle-graph"}
@@ -477,7 +498,8 @@ def main():
             g2 = r2["model_bytes"] / (m2 * 1e-3) / 1e9
             sweep.append({"workload": name, "ms_per_reduction": m2, "min_ms": min(r2["ms"]),
                           "effective_gbs": g2, "frac_of_hbm": g2 / hbm,
-                          "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"]})
+                          "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"],
+                          "latency_chain": latency_chain(ww.n, ww.bw, ww.tw, r2["pass_ms_mean"])})
 
     svals = None
     if rank == 0 and world == 1 and not args.no_sweep:
@@ -510,6 +532,7 @@ def main():
             "wall_s": wall,
             "pass_kernels": res["kernels"],
             "pass_ms": res["pass_ms_mean"],
+            "latency_chain": latency_chain(w.n, w.bw, w.tw, res["pass_ms_mean"]),
             "per_workload": sweep,
             "singular_values": svals,
         }
