@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "bb_last_pass_kernel": ([p, i64], i64),
             "bb_last_pass_group": ([p, i64], i64),
             "bb_singular_values": ([ci, i64, p, p, p, p], ci),
+            "bb_singular_values_lanes": ([ci, i64, p, p, p, i64, p], ci),
             "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
         }
         for name, (args, res) in sig.items():
@@ -196,6 +197,11 @@ def bb_reduce_noalloc(band, n: int, bw: int, ldab: int, tw: int, dtype: int, d_o
     synchronizes the stream before returning."""
     _check(lib().bb_reduce_noalloc(_addr(band), n, bw, ldab, tw, dtype, _addr(d_out), _addr(e_out),
                                    _stream(stream)))
+
+
+def bb_singular_values_lanes(dtype: int, n: int, d, e, sigma_out, lanes: int, stream=None) -> None:
+    """bb_singular_values with the lanes per value fixed (0: the default rule)."""
+    _check(lib().bb_singular_values_lanes(dtype, n, _addr(d), _addr(e), _addr(sigma_out), lanes, _stream(stream)))
 
 
 def bb_group_plan(n: int, bw: int, tw: int, elem_bytes: int, pass_index: int, group_size: int = 0):

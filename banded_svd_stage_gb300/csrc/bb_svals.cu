@@ -117,8 +117,24 @@ bidiag_svals_kernel(const T* __restrict__ d, const T* __restrict__ e, int n, int
 
 }  // namespace bb
 
-extern "C" bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d, const void* e, void* sigma_out,
-                                        bb_stream_t stream) {
+namespace {
+
+// Steps of multisection with P lanes per value: each step keeps one of the
+// P + 1 equal parts of the interval, so the least s with (P + 1)^s >= 2^bits
+// brings it down to 2^-bits of the starting bound.
+int multisection_steps(int P, int bits) {
+    const unsigned long long target = 1ull << bits;
+    unsigned long long acc = 1;
+    int s = 0;
+    while (acc < target) {
+        acc = (acc > target / (unsigned long long)(P + 1)) ? target : acc * (unsigned long long)(P + 1);
+        ++s;
+    }
+    return s;
+}
+
+bb_status launch_svals(bb_dtype dtype, int64_t n, const void* d, const void* e, void* sigma_out, int64_t lanes,
+                       bb_stream_t stream) {
     if (n < 1 || n > (int64_t)1 << 29) {
         bb::set_last_error("bb_singular_values: n must be in [1, 2^29]");
         return BB_ERR_INVALID_ARG;
@@ -131,17 +147,24 @@ extern "C" bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d
         bb::set_last_error("bb_singular_values: unknown dtype");
         return BB_ERR_DTYPE;
     }
+    if (lanes != 0 && (lanes < 1 || lanes > 32 || (lanes & (lanes - 1)) != 0)) {
+        bb::set_last_error("bb_singular_values: lanes must be 0 or a power of two in [1, 32]");
+        return BB_ERR_INVALID_ARG;
+    }
     cudaStream_t s = (cudaStream_t)stream;
     // lanes per value: about enough threads to fill the GPU (152 SMs x 2048),
-    // a power of two from 1 to 32
-    int P = 1;
-    while (P < 32 && (int64_t)P * 2 * n <= (int64_t)152 * 2048) P *= 2;
-    // steps: the interval shrinks by P + 1 per step, down to 2^-27 (float)
-    // or 2^-56 (double) of the bound
-    const int bits = (dtype == BB_F32) ? 27 : 56;
-    int lg = 0;  // floor(log2(P + 1))
-    while ((2 << lg) <= P + 1) ++lg;
-    const int steps = (bits + lg - 1) / lg;
+    // a power of two; at most 32 in float, where a count is cheap, and 8 in
+    // double, where the division sequence of each count is the bound and
+    // extra lanes cost more counts than the steps they save
+    int P = (int)lanes;
+    if (P == 0) {
+        const int cap = (dtype == BB_F32) ? 32 : 8;
+        P = 1;
+        while (P < cap && (int64_t)P * 2 * n <= (int64_t)152 * 2048) P *= 2;
+    }
+    // the interval shrinks by P + 1 per step, down to 2^-27 (float) or 2^-56
+    // (double) of the bound
+    const int steps = multisection_steps(P, (dtype == BB_F32) ? 27 : 56);
     const unsigned grid = (unsigned)((n * P + bb::kSvThreads - 1) / bb::kSvThreads);
     // e may be null for n == 1: the kernel never reads it then (m = 1)
     if (dtype == BB_F32)
@@ -156,4 +179,16 @@ extern "C" bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d
         return BB_ERR_CUDA;
     }
     return BB_OK;
+}
+
+}  // namespace
+
+extern "C" bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d, const void* e, void* sigma_out,
+                                        bb_stream_t stream) {
+    return launch_svals(dtype, n, d, e, sigma_out, 0, stream);
+}
+
+extern "C" bb_status bb_singular_values_lanes(bb_dtype dtype, int64_t n, const void* d, const void* e,
+                                              void* sigma_out, int64_t lanes, bb_stream_t stream) {
+    return launch_svals(dtype, n, d, e, sigma_out, lanes, stream);
 }

@@ -226,15 +226,21 @@ bb_status bb_reduce_noalloc(void* band_ptr, int64_t n, int64_t bw, int64_t ldab,
  * pointers owned by the caller, of element type dtype; n >= 1.  Computed by
  * multisection on Sturm counts of the 2n x 2n Golub-Kahan tridiagonal (zero
  * diagonal, off-diagonal d_0, e_0, d_1, ..., d_{n-1}) with LAPACK xSTEBZ's
- * pivmin guard: a group of P lanes per value (P a power of two up to 32, the
- * most that fill the GPU) splits the interval into P + 1 parts per step,
- * down to about one ulp of the Gershgorin bound max_i(|a_{i-1}| + |a_i|),
- * the absolute accuracy.  This is the step
+ * pivmin guard: a group of P lanes per value (P a power of two, the most that
+ * fill the GPU, at most 32 in float and 8 in double) splits the interval
+ * into P + 1 parts per step, down to about one ulp of the Gershgorin bound
+ * max_i(|a_{i-1}| + |a_i|), the absolute accuracy.  This is the step
  * after the reduction in "A two-stage reduction on an Apple M5 Pro"
  * (Section 7).  Asynchronous on `stream`; allocates nothing; the return code
  * covers arguments and the launch. */
 bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d, const void* e, void* sigma_out,
                              bb_stream_t stream);
+/* As bb_singular_values with the lanes per value fixed: 0 for the default
+ * rule (the most that fill the GPU, at most 32 in float and 8 in double),
+ * else a power of two in [1, 32] (BB_ERR_INVALID_ARG otherwise).  For
+ * measurement and tests. */
+bb_status bb_singular_values_lanes(bb_dtype dtype, int64_t n, const void* d, const void* e, void* sigma_out,
+                                   int64_t lanes, bb_stream_t stream);
 
 #ifdef __cplusplus
 }

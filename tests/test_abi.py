@@ -132,6 +132,12 @@ def test_group_plan_rejects_inconsistent_shapes(lib):
             bb.bb_group_plan(*args)
 
 
+def test_singular_value_lanes_are_validated_without_a_gpu(lib):
+    fake = 0x1000  # never dereferenced: rejected before any CUDA call
+    for lanes in (-1, 3, 6, 33, 64):
+        assert lib.bb_singular_values_lanes(bb.BB_F64, 8, fake, fake, fake, lanes, None) == bb.BB_ERR_INVALID_ARG
+
+
 def test_header_is_c99_and_links_against_the_library(lib, tmp_path):
     # the boundary is a C ABI: a C99 translation unit includes the header with
     # every warning an error, takes the address of every declared function,

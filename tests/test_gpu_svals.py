@@ -120,3 +120,24 @@ def test_argument_errors():
         bb.bb_singular_values(bb.BB_F32, 0, 1, 1, 1)
     with pytest.raises(bb.BBError):
         bb.bb_singular_values(bb.BB_F32, 5, None, None, None)
+
+
+@pytest.mark.parametrize("lanes", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("dt", ["f32", "f64"])
+def test_every_lane_count(lanes, dt):
+    # the step count follows the lanes (each step keeps one of lanes + 1 parts)
+    rng = np.random.default_rng(lanes)
+    n = 700
+    d = rng.standard_normal(n).astype(np.float32 if dt == "f32" else np.float64)
+    e = rng.standard_normal(n - 1).astype(d.dtype)
+    dev = torch.device("cuda:0")
+    tdt = torch.float32 if dt == "f32" else torch.float64
+    dd = torch.from_numpy(d).to(dev)
+    ee = torch.from_numpy(e).to(dev)
+    s = torch.empty(n, dtype=tdt, device=dev)
+    bb.bb_singular_values_lanes(bb.dtype_code(dt), n, dd, ee, s, lanes, torch.cuda.current_stream(dev))
+    torch.cuda.synchronize()
+    got = s.cpu().numpy().astype(np.float64)
+    want = oracle.bidiagonal_singular_values(d.astype(np.float64), e.astype(np.float64))
+    fro = float(np.sqrt((d.astype(np.float64) ** 2).sum() + (e.astype(np.float64) ** 2).sum()))
+    assert np.abs(got - want).max() <= TOL[dt] * fro
