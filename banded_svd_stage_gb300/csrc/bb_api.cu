@@ -11,6 +11,7 @@
 
 #include "../../include/bb.h"
 #include "bb_internal.h"
+#include "bb_sym.h"
 
 namespace {
 

@@ -27,6 +27,7 @@
 
 #include "bb_device.cuh"
 #include "bb_internal.h"
+#include "bb_sym.h"
 
 namespace bb {
 
