@@ -139,23 +139,23 @@ bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, i
         (elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
         return fail(BB_ERR_INVALID_ARG, "bb_group_plan: argument out of range");
     try {
-    const PassPlan ps = pass_at(bw, tw, pass);
-    bb::PassArgs P{};
-    P.n = n;
-    P.b = ps.b;
-    P.t = ps.t;
-    P.bp = P.b - P.t;
-    P.ku = (int)(bw + tw);
-    P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
-    P.lagh = bb::pass_lag_half(P.b, P.t);
-    bb::GroupArgs ga{};
-    const bool ok = P.nsweeps > 0 &&
-                    bb::plan_group(P, bb::wmax_bucket(P.t + 1), (size_t)elem_bytes, (int)group_size, &ga);
-    *g = ok ? ga.g : 0;
-    *nslot = ok ? ga.nslot : 0;
-    *ahead = ok ? ga.ahead : 0;
-    *lds = ok ? ga.lds : 0;
-    return BB_OK;
+        const PassPlan ps = pass_at(bw, tw, pass);
+        bb::PassArgs P{};
+        P.n = n;
+        P.b = ps.b;
+        P.t = ps.t;
+        P.bp = P.b - P.t;
+        P.ku = (int)(bw + tw);
+        P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
+        P.lagh = bb::pass_lag_half(P.b, P.t);
+        bb::GroupArgs ga{};
+        const bool ok = P.nsweeps > 0 &&
+                        bb::plan_group(P, bb::wmax_bucket(P.t + 1), (size_t)elem_bytes, (int)group_size, &ga);
+        *g = ok ? ga.g : 0;
+        *nslot = ok ? ga.nslot : 0;
+        *ahead = ok ? ga.ahead : 0;
+        *lds = ok ? ga.lds : 0;
+        return BB_OK;
     } catch (const std::bad_alloc&) {
         return fail(BB_ERR_NOMEM, "bb_group_plan: host allocation failed");
     } catch (...) {
@@ -168,7 +168,8 @@ double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int
     const int64_t np = count_passes(bw, tw);
     for (int64_t pi = 0; pi < np; ++pi) {
         if (pass >= 0 && pi != pass) continue;
-        const int b = pass_at(bw, tw, pi).b, t = pass_at(bw, tw, pi).t;
+        const PassPlan ps = pass_at(bw, tw, pi);
+        const int b = ps.b, t = ps.t;
         for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) {
             const int64_t K = steps_of_sweep(n, b, t, r);
             for (int64_t k = 0; k < K; ++k) {
@@ -189,7 +190,8 @@ int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass) {
     const int64_t np = count_passes(bw, tw);
     for (int64_t pi = 0; pi < np; ++pi) {
         if (pass >= 0 && pi != pass) continue;
-        const int b = pass_at(bw, tw, pi).b, t = pass_at(bw, tw, pi).t;
+        const PassPlan ps = pass_at(bw, tw, pi);
+        const int b = ps.b, t = ps.t;
         for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) total += steps_of_sweep(n, b, t, r);
     }
     return total;

@@ -18,7 +18,9 @@ Also here:
     tridiagonal by the same passes, lower band storage
     A(i, j) = band[j, i - j];
   * ``bidiagonal_singular_values``: singular values of a bidiagonal by the
-    Golub-Kahan tridiagonal's eigenvalues.
+    Golub-Kahan tridiagonal's eigenvalues;
+  * ``bidiagonal_with_vectors``: the reduction with its reflectors kept and
+    applied to the identity, A = U B V^T (the back-transformation).
 """
 from __future__ import annotations
 
@@ -72,6 +74,8 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).argtypes = [i64, i64, i64, p, i64, i64,
                                                                        ctypes.c_double]
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).restype = ci
+        getattr(lib, "oracle_reduce_band_record" + sfx).argtypes = [i64, i64, i64, p, i64, i64, p, p, p, p, p]
+        getattr(lib, "oracle_reduce_band_record" + sfx).restype = i64
         getattr(lib, "oracle_sym_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64]
         getattr(lib, "oracle_sym_reduce_band" + sfx).restype = ci
         getattr(lib, "oracle_sym_reduce_dense" + sfx).argtypes = [i64, i64, i64, p]
@@ -154,6 +158,54 @@ def reduce_band_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: i
     if rc != 0:
         raise RuntimeError("oracle_reduce_band_pipelined: could not start the threads")
     return band
+
+
+def reflector_count(n: int, bw: int, tw: int) -> int:
+    """Reflectors of a whole reduction: two per step (right, then left)."""
+    return 2 * sum(sweep_steps(n, b, t, r) for (b, t) in pass_plan(bw, tw) for r in range(n))
+
+
+def reduce_band_record(band: np.ndarray, n: int, bw: int, tw: int):
+    """reduce_band in place, also returning every reflector in the order
+    applied: (side, start, width, tau, v) with side 0 = right (columns
+    start .. start+width-1), 1 = left (those rows), v of shape (count, tw+1)."""
+    assert band.flags.c_contiguous and band.shape[0] == n
+    cap = reflector_count(n, bw, tw)
+    side = np.zeros(cap, dtype=np.int8)
+    start = np.zeros(cap, dtype=np.int64)
+    width = np.zeros(cap, dtype=np.int32)
+    taus = np.zeros(cap, dtype=band.dtype)
+    vs = np.zeros((cap, tw + 1), dtype=band.dtype)
+    got = getattr(_load(), "oracle_reduce_band_record" + _sfx(band))(
+        n, bw, tw, _ptr(band), band.shape[1], cap, _ptr(side), _ptr(start), _ptr(width), _ptr(taus), _ptr(vs))
+    if got == -1:
+        raise ValueError("oracle_reduce_band_record: invalid arguments")
+    if got != cap:
+        raise RuntimeError(f"oracle_reduce_band_record: {got} reflectors, expected {cap}")
+    return side, start, width, taus, vs
+
+
+def bidiagonal_with_vectors(band: np.ndarray, n: int, bw: int, tw: int):
+    """(d, e, U, V) with A = U B V^T, B the upper bidiagonal (d, e), U, V
+    orthogonal (float64).  U = L_1 L_2 ... and V = R_1 R_2 ... in the order the
+    reduction applied the left and right reflectors, formed by applying each
+    reflector to the identity with numpy (the back-transformation)."""
+    work = np.ascontiguousarray(band.copy())
+    side, start, width, taus, vs = reduce_band_record(work, n, bw, tw)
+    d, e = extract(work, n, bw + tw)
+    U = np.eye(n)
+    V = np.eye(n)
+    for q in range(side.size):
+        tau = float(taus[q])
+        if tau == 0.0:
+            continue
+        c, w = int(start[q]), int(width[q])
+        v = vs[q, :w].astype(np.float64)
+        M = U if side[q] == 1 else V
+        # M <- M H on columns c .. c+w-1
+        y = M[:, c:c + w] @ v
+        M[:, c:c + w] -= tau * np.outer(y, v)
+    return d, e, U, V
 
 
 def reduce_dense(a: np.ndarray, bw: int, tw: int) -> np.ndarray:

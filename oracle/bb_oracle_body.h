@@ -85,6 +85,10 @@ void FN(oracle_larfg)(int64_t m, REAL* alpha, REAL* x, int64_t inc, REAL* tau) {
  * whole matrix instead of the windows above (entries outside the windows are
  * exactly zero, so the arithmetic inside the windows is the same).
  * ------------------------------------------------------------------------- */
+/* RECORD(side, c, w, v, tau) is a no-op except in the recording driver below,
+ * which keeps every reflector for the back-transformation. */
+#define RECORD(side, c, w, v, tau) ((void)0)
+
 #define STEP_BODY(ROW_LO, ROW_HI, COL_LO, COL_HI, DO_RIGHT, DO_LEFT)                    \
     do {                                                                                \
         int64_t c = r + (b - t) + k * b;                                                \
@@ -100,6 +104,7 @@ void FN(oracle_larfg)(int64_t m, REAL* alpha, REAL* x, int64_t inc, REAL* tau) {
             beta = v[0];                                                                \
             FN(oracle_larfg)(w - 1, &beta, v + 1, 1, &tau);                             \
             v[0] = 1;                                                                   \
+            RECORD(0, c, w, v, tau);                                                    \
             ELEM(p, c) = beta;                                                          \
             for (int64_t q = 1; q < w; ++q) ELEM(p, c + q) = 0;                         \
             if (tau != 0) {                                                             \
@@ -117,6 +122,7 @@ void FN(oracle_larfg)(int64_t m, REAL* alpha, REAL* x, int64_t inc, REAL* tau) {
             beta = v[0];                                                                \
             FN(oracle_larfg)(w - 1, &beta, v + 1, 1, &tau);                             \
             v[0] = 1;                                                                   \
+            RECORD(1, c, w, v, tau);                                                    \
             ELEM(c, c) = beta;                                                          \
             for (int64_t q = 1; q < w; ++q) ELEM(c + q, c) = 0;                         \
             if (tau != 0) {                                                             \
@@ -248,6 +254,55 @@ static void* FN(pipe_worker_)(void* arg) {
     return NULL;
 }
 
+/* The reduction as oracle_reduce_band (all passes, same arithmetic and
+ * order), also keeping every reflector H = I - tau v v^T in the order applied:
+ * for reflector q, side[q] = 0 for a right one (A <- A H on columns
+ * start[q] .. start[q] + width[q] - 1) or 1 for a left one (A <- H A on those
+ * rows), tau[q], and v at vs[q * (tw + 1) + 0 .. width[q] - 1] (v_0 = 1).
+ * With B the result, A = U B V^T where U = L_1 L_2 ... (the left reflectors
+ * in order) and V = R_1 R_2 ... (the right ones): the back-transformation
+ * that gives the singular vectors ("Accelerating Bidiagonalization of Banded
+ * Matrices through Memory-Aware Bulge-Chasing on GPUs", Section III: the
+ * reflector vectors are written back for it).  cap is the room for
+ * reflectors.  Returns the number recorded, -1 on invalid arguments, -2 when
+ * cap is too small. */
+int64_t FN(oracle_reduce_band_record)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab, int64_t cap,
+                                      int8_t* side, int64_t* start, int32_t* width, REAL* taus, REAL* vs) {
+    if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
+    if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
+    if (tw + 1 > ORACLE_WMAX || cap < 0) return -1;
+    const int64_t ku = bw + tw;
+    for (int64_t j = 0; j < n; ++j) {
+        for (int64_t q = 0; q < tw; ++q) band[q + j * ldab] = 0;
+        for (int64_t q = ku + 1; q <= ku + tw; ++q) band[q + j * ldab] = 0;
+    }
+    int64_t nrec = 0;
+#undef RECORD
+#define RECORD(SIDE, C, W, V, TAU)                                                     \
+    do {                                                                               \
+        if (nrec < cap) {                                                              \
+            side[nrec] = (int8_t)(SIDE);                                               \
+            start[nrec] = (C);                                                         \
+            width[nrec] = (int32_t)(W);                                                \
+            taus[nrec] = (TAU);                                                        \
+            for (int64_t u_ = 0; u_ < (W); ++u_) vs[nrec * (tw + 1) + u_] = (V)[u_];    \
+        }                                                                              \
+        ++nrec;                                                                        \
+    } while (0)
+    int64_t b = bw;
+    while (b > 1) {
+        int64_t t = (tw < b - 1) ? tw : b - 1;
+        for (int64_t r = 0; r + (b - t) + 1 <= n - 1; ++r) {
+            int64_t K = FN(oracle_sweep_steps)(n, b, t, r);
+            for (int64_t k = 0; k < K; ++k) STEP_BODY(p, ce, c, cend, 1, 1);
+        }
+        b -= t;
+    }
+#undef RECORD
+#define RECORD(side, c, w, v, tau) ((void)0)
+    return nrec <= cap ? nrec : -2;
+}
+
 /* Runs every pass of the plan on nthreads threads with `worker` (the
  * bidiagonal or the symmetric one), joining the threads between passes.
  * Returns 0, -2 when the time limit ran out, -3 when the threads or the
@@ -335,6 +390,7 @@ int FN(oracle_reduce_dense)(int64_t n, int64_t bw, int64_t tw, REAL* a) {
 }
 #undef ELEM
 
+#undef RECORD
 #undef FN
 #undef CAT
 #undef CAT2
