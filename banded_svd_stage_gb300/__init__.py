@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             "bb_singular_values": ([ci, i64, p, p, p, p], ci),
             "bb_singular_values_lanes": ([ci, i64, p, p, p, i64, p], ci),
             "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
+            "bb_sym_reduce": ([p, p, i64, i64, p, p, p], ci),
+            "bb_sym_required_ldab": ([i64, i64], i64),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -216,6 +218,15 @@ def bb_singular_values(dtype: int, n: int, d, e, sigma_out, stream=None) -> None
     """Singular values of the bidiagonal (d, e), descending, into sigma_out
     (device buffers; asynchronous on `stream`)."""
     _check(lib().bb_singular_values(dtype, n, _addr(d), _addr(e), _addr(sigma_out), _stream(stream)))
+
+
+def bb_sym_reduce(h, band, ldab: int, tw: int, d, e, stream=None) -> None:
+    """Symmetric band (lower band storage, device) -> tridiagonal (d, e)."""
+    _check(lib().bb_sym_reduce(h, _addr(band), ldab, tw, _addr(d), _addr(e), _stream(stream)))
+
+
+def bb_sym_required_ldab(bw: int, tw: int) -> int:
+    return lib().bb_sym_required_ldab(bw, tw)
 
 
 def dtype_code(dtype) -> int:

@@ -11,6 +11,7 @@
 
 #include "../../include/bb.h"
 #include "bb_internal.h"
+#include "bb_sym.h"
 
 namespace {
 
@@ -540,6 +541,53 @@ bb_status bb_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void
         return fail(BB_ERR_NOMEM, "bb_reduce: host allocation failed");
     } catch (...) {
         return fail(BB_ERR_INTERNAL, "bb_reduce: unexpected host exception");
+    }
+}
+
+int64_t bb_sym_required_ldab(int64_t bw, int64_t tw) { return bw + tw + 1; }
+
+static bb_status sym_checked(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out, void* e_out,
+                             bb_stream_t stream) {
+    if (!h) return fail(BB_ERR_INVALID_ARG, "null handle");
+    const int64_t tw_max = std::max<int64_t>(1, h->bw - 1);
+    if (tw < 1 || tw > tw_max) return fail(BB_ERR_INVALID_ARG, "need 1 <= tw <= max(1, bw - 1)");
+    if (tw > 64) return fail(BB_ERR_INVALID_ARG, "tw > 64 is not supported");
+    if (ldab < bb_sym_required_ldab(h->bw, tw)) return fail(BB_ERR_LDAB, "ldab < bw + tw + 1");
+    if ((double)ldab * (double)h->n > 9.0e18 / 8) return fail(BB_ERR_INVALID_ARG, "band too large");
+    if (!band_ptr || !d_out || (h->n > 1 && !e_out)) return fail(BB_ERR_INVALID_ARG, "null band, d or e pointer");
+    if (!is_device_pointer(band_ptr) || !is_device_pointer(d_out) || (h->n > 1 && !is_device_pointer(e_out)))
+        return fail(BB_ERR_INVALID_ARG, "band, d and e must be device pointers");
+    bb::SymLaunch L;
+    L.num_sms = h->num_sms;
+    L.max_ctas = h->max_ctas;
+    L.stall_sweep = h->stall_sweep;
+    L.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+    L.progress = h->d_progress;
+    L.status = h->d_status;
+    long long nl = 0;
+    cudaError_t err;
+    if (h->dtype == BB_F32)
+        err = bb::run_sym<float>((float*)band_ptr, h->n, ldab, (int)h->bw, (int)tw, (float*)d_out, (float*)e_out, L,
+                                 (cudaStream_t)stream, &nl);
+    else
+        err = bb::run_sym<double>((double*)band_ptr, h->n, ldab, (int)h->bw, (int)tw, (double*)d_out,
+                                  (double*)e_out, L, (cudaStream_t)stream, &nl);
+    h->last_launches = nl;
+    h->last_passes = 0;
+    h->pass_kernel.clear();
+    h->pass_group.clear();
+    if (err != cudaSuccess) return cuda_fail(err, "bb_sym_reduce launch");
+    return BB_OK;
+}
+
+bb_status bb_sym_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out, void* e_out,
+                        bb_stream_t stream) {
+    try {
+        return sym_checked(h, band_ptr, ldab, tw, d_out, e_out, stream);
+    } catch (const std::bad_alloc&) {
+        return fail(BB_ERR_NOMEM, "bb_sym_reduce: host allocation failed");
+    } catch (...) {
+        return fail(BB_ERR_INTERNAL, "bb_sym_reduce: unexpected host exception");
     }
 }
 

@@ -249,6 +249,55 @@ def run_svals(w: bi.Workload, steps: int, warmup: int):
                                      "a group of lanes per singular value"}
 
 
+def run_sym(w: bi.Workload, steps: int, warmup: int):
+    """Symmetric variant: device time of bb_sym_reduce on a symmetric band of
+    the workload's n, bandwidth, tw, entry distribution and dtype (L2
+    flushed and the band restored before each step, outside the events),
+    beside the oracle's pipelined multi-thread chase on the host."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sb_np = bi.make_sym_band(w.n, w.bw, w.tw, w.dtype, w.dist, seed=w.seed)
+    pristine = torch.from_numpy(sb_np).to(dev)
+    band = pristine.clone()
+    d = torch.empty(w.n, dtype=band.dtype, device=dev)
+    e = torch.empty(max(w.n - 1, 1), dtype=band.dtype, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    h = bb.bb_create(w.n, w.bw, bb.dtype_code(w.dtype))
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    try:
+        for i in range(warmup + steps):
+            band.copy_(pristine)
+            flush.fill_(i & 0xFF)
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            bb.bb_sym_reduce(h, band, band.shape[1], w.tw, d, e, stream)
+            ev1.record(stream)
+            if bb.bb_status_sync(h, stream) != bb.BB_OK:
+                raise RuntimeError("symmetric reduction failed: " + bb.bb_last_error())
+            if i >= warmup:
+                times.append(ev0.elapsed_time(ev1))
+    finally:
+        bb.bb_destroy(h)
+    out = {"ms": statistics.median(times), "n": w.n, "bw": w.bw, "tw": w.tw, "dtype": w.dtype,
+           "kernel": "sym_pass_kernel", "launches": int(bb.bb_num_passes(w.bw, w.tw)) + 2}
+    try:
+        import oracle
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        P = max(1, min(cores, 2 * w.n // (3 * max(w.bw, 1)), w.n // 256))
+        t0 = time.perf_counter()
+        work = sb_np.copy()
+        oracle.sym_reduce_band_pipelined(work, w.n, w.bw, w.tw, P, time_limit=60.0)
+        out["cpu_pipelined_ms"] = (time.perf_counter() - t0) * 1e3
+        out["cpu_threads"] = P
+    except Exception as ex:  # context only
+        out["cpu_pipelined_error"] = f"{type(ex).__name__}: {ex}"
+    return out
+
+
 def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
     """bb_reduce_host from pinned host memory: H2D of the band, reduction, D2H
     of d and e, inside the timed region (host wall clock around the call,
@@ -546,6 +595,12 @@ def main():
     svals = None
     if rank == 0 and world == 1 and not args.no_sweep:
         svals = run_svals(w, args.steps, args.warmup)
+    sym = None
+    if rank == 0 and world == 1 and not args.no_sweep:
+        try:
+            sym = run_sym(w, args.steps, args.warmup)
+        except Exception as ex:  # a side measurement never loses the line
+            sym = {"error": f"{type(ex).__name__}: {ex}"}
 
     cpu = cpu_pipe = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -579,6 +634,7 @@ def main():
             "per_scheduler": per_sched,
             "per_workload": sweep,
             "singular_values": svals,
+            "symmetric": sym,
         }
         print(json.dumps(line))
     if world > 1:

@@ -144,6 +144,29 @@ enum {
 bb_status bb_set_param(bb_handle* h, int param, int64_t value);
 int64_t bb_get_param(const bb_handle* h, int param);
 
+/* Symmetric variant: reduce a symmetric band matrix to symmetric tridiagonal
+ * form with the same passes BW -> BW - TW, one two-sided Householder
+ * reflector per step (the band to tridiagonal chase of "A two-stage
+ * reduction on an Apple M5 Pro", Section 6, with the passes of
+ * "Accelerating Bidiagonalization of Banded Matrices through Memory-Aware
+ * Bulge-Chasing on GPUs", Section III).
+ *   h        handle from bb_create(n, bw, dtype) (n, bw, dtype as there)
+ *   band_ptr device, LAPACK lower band storage, column-major: A(i, j) for
+ *            0 <= i - j <= bw at band[(i - j) + j * ldab]; rows bw+1 ..
+ *            bw+tw of each column are fill space (zeroed here).  Reduced in
+ *            place; on return the rows below the subdiagonal are zero.
+ *   ldab     >= bb_sym_required_ldab(bw, tw) = bw + tw + 1 (else BB_ERR_LDAB)
+ *   tw       1 <= tw <= max(1, bw - 1), tw <= 64
+ *   d_out    device, n entries: the diagonal; e_out device, n - 1 entries:
+ *            the subdiagonal (may be null when n == 1)
+ * Stream-ordered and asynchronous like bb_reduce; one CTA per sweep with the
+ * handle's progress counters (step k of sweep r after sweep r-1 finished
+ * min(k + L, its steps), L = 2, or 3 when b - t = 1); device-side failures
+ * are reported by bb_status_sync. */
+bb_status bb_sym_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out, void* e_out,
+                        bb_stream_t stream);
+int64_t bb_sym_required_ldab(int64_t bw, int64_t tw);
+
 /* Pass plan of (bw, tw) (b = bw; while b > 1: t = min(tw, b - 1); b -= t):
  * the number of passes, ceil((bw - 1) / tw), and the (b, t) of pass i,
  * b = bw - i tw, t = min(tw, b - 1).  Host-only and computed in closed form;
