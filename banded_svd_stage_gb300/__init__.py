@@ -22,7 +22,7 @@ BB_OK, BB_ERR_INVALID_ARG, BB_ERR_LDAB, BB_ERR_DTYPE, BB_ERR_CUDA, BB_ERR_TIMEOU
 STATUS_NAMES = {0: "BB_OK", 1: "BB_ERR_INVALID_ARG", 2: "BB_ERR_LDAB", 3: "BB_ERR_DTYPE",
                 4: "BB_ERR_CUDA", 5: "BB_ERR_TIMEOUT", 6: "BB_ERR_NOMEM"}
 (BB_PARAM_SCHEDULER, BB_PARAM_TPB, BB_PARAM_MAX_CTAS, BB_PARAM_WAIT_BUDGET_MS, BB_PARAM_PASS_LO,
- BB_PARAM_PASS_HI, BB_PARAM_STALL_SWEEP, BB_PARAM_TIMING, BB_PARAM_GROUP_SIZE) = range(9)
+ BB_PARAM_PASS_HI, BB_PARAM_STALL_SWEEP, BB_PARAM_TIMING, BB_PARAM_GROUP_SIZE, BB_PARAM_RECORD) = range(10)
 BB_ERR_INTERNAL = 7
 STATUS_NAMES[7] = "BB_ERR_INTERNAL"
 # scheduler values
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "bb_last_pass_group": ([p, i64], i64),
             "bb_singular_values": ([ci, i64, p, p, p, p], ci),
             "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
+            "bb_back_transform": ([p, p, i64, p, i64, p], ci),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -210,6 +211,12 @@ def bb_singular_values(dtype: int, n: int, d, e, sigma_out, stream=None) -> None
     """Singular values of the bidiagonal (d, e), descending, into sigma_out
     (device buffers; asynchronous on `stream`)."""
     _check(lib().bb_singular_values(dtype, n, _addr(d), _addr(e), _addr(sigma_out), _stream(stream)))
+
+
+def bb_back_transform(h, U, ldu: int, V, ldv: int, stream=None) -> None:
+    """U, V (device, column-major n x n; either may be None) of the last
+    reduction recorded with BB_PARAM_RECORD, so that A = U B V^T."""
+    _check(lib().bb_back_transform(h, _addr(U), ldu, _addr(V), ldv, _stream(stream)))
 
 
 def dtype_code(dtype) -> int:

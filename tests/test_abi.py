@@ -156,3 +156,7 @@ def test_header_is_c99_and_links_against_the_library(lib, tmp_path):
            "-Wl,--unresolved-symbols=ignore-in-shared-libs"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
+
+
+def test_back_transform_rejects_a_null_handle(lib):
+    assert lib.bb_back_transform(None, None, 1, None, 1, None) == bb.BB_ERR_INVALID_ARG
