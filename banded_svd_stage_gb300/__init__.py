@@ -22,7 +22,7 @@ BB_OK, BB_ERR_INVALID_ARG, BB_ERR_LDAB, BB_ERR_DTYPE, BB_ERR_CUDA, BB_ERR_TIMEOU
 STATUS_NAMES = {0: "BB_OK", 1: "BB_ERR_INVALID_ARG", 2: "BB_ERR_LDAB", 3: "BB_ERR_DTYPE",
                 4: "BB_ERR_CUDA", 5: "BB_ERR_TIMEOUT", 6: "BB_ERR_NOMEM"}
 (BB_PARAM_SCHEDULER, BB_PARAM_TPB, BB_PARAM_MAX_CTAS, BB_PARAM_WAIT_BUDGET_MS, BB_PARAM_PASS_LO,
- BB_PARAM_PASS_HI, BB_PARAM_STALL_SWEEP, BB_PARAM_TIMING, BB_PARAM_GROUP_SIZE) = range(9)
+ BB_PARAM_PASS_HI, BB_PARAM_STALL_SWEEP, BB_PARAM_TIMING, BB_PARAM_GROUP_SIZE, BB_PARAM_RECORD) = range(10)
 BB_ERR_INTERNAL = 7
 STATUS_NAMES[7] = "BB_ERR_INTERNAL"
 # scheduler values
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
             "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
             "bb_sym_reduce": ([p, p, i64, i64, p, p, p], ci),
             "bb_sym_required_ldab": ([i64, i64], i64),
+            "bb_back_transform": ([p, p, i64, p, i64, p], ci),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -227,6 +228,10 @@ def bb_sym_reduce(h, band, ldab: int, tw: int, d, e, stream=None) -> None:
 
 def bb_sym_required_ldab(bw: int, tw: int) -> int:
     return lib().bb_sym_required_ldab(bw, tw)
+def bb_back_transform(h, U, ldu: int, V, ldv: int, stream=None) -> None:
+    """U, V (device, column-major n x n; either may be None) of the last
+    reduction recorded with BB_PARAM_RECORD, so that A = U B V^T."""
+    _check(lib().bb_back_transform(h, _addr(U), ldu, _addr(V), ldv, _stream(stream)))
 
 
 def dtype_code(dtype) -> int:

@@ -12,6 +12,7 @@
 #include "../../include/bb.h"
 #include "bb_internal.h"
 #include "bb_sym.h"
+#include "bb_vectors.h"
 
 namespace {
 
@@ -108,6 +109,15 @@ struct bb_handle {
     };
     std::vector<PassGraph> graphs;  // by pass index
     cudaStream_t capture_stream = nullptr;
+    // reflector record of the last whole reduction (BB_PARAM_RECORD)
+    int record = 0;
+    void* rec_v = nullptr;
+    void* rec_tau = nullptr;
+    long long* rec_prefix = nullptr;  // per pass, steps of the sweeps before r
+    size_t rec_v_bytes = 0, rec_tau_bytes = 0, rec_prefix_bytes = 0;
+    std::vector<long long> rec_prefix_host;
+    bool rec_valid = false;
+    int64_t rec_tw = 0;
     // statistics of the last reduction
     int64_t last_launches = 0;
     std::vector<cudaEvent_t> ev;  // 2 per pass
@@ -235,6 +245,9 @@ void bb_destroy(bb_handle* h) {
     if (h->d_status) cudaFree(h->d_status);
     if (h->s_band) cudaFree(h->s_band);
     if (h->s_de) cudaFree(h->s_de);
+    if (h->rec_v) cudaFree(h->rec_v);
+    if (h->rec_tau) cudaFree(h->rec_tau);
+    if (h->rec_prefix) cudaFree(h->rec_prefix);
     if (h->work) cudaFree(h->work);
     for (auto& pg : h->graphs)
         if (pg.exec) cudaGraphExecDestroy(pg.exec);
@@ -282,6 +295,9 @@ bb_status bb_set_param(bb_handle* h, int param, int64_t value) {
             if (value < 0 || value > 32) return fail(BB_ERR_INVALID_ARG, "group size must be in [0, 32]");
             h->group_size = (int)value;
             return BB_OK;
+        case BB_PARAM_RECORD:
+            h->record = value ? 1 : 0;
+            return BB_OK;
         default:
             return fail(BB_ERR_INVALID_ARG, "unknown parameter");
     }
@@ -299,6 +315,7 @@ int64_t bb_get_param(const bb_handle* h, int param) {
         case BB_PARAM_STALL_SWEEP: return h->stall_sweep;
         case BB_PARAM_TIMING: return h->timing;
         case BB_PARAM_GROUP_SIZE: return h->group_size;
+        case BB_PARAM_RECORD: return h->record;
         default: return -1;
     }
 }
@@ -427,6 +444,45 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
     auto plan = plan_passes(h->bw, tw);
     const int64_t lo = std::max<int64_t>(0, h->pass_lo);
     const int64_t hi = std::min<int64_t>((int64_t)plan.size(), h->pass_hi);
+    // reflector record: whole reductions only, on the flag kernel
+    h->rec_valid = false;
+    const bool rec = h->record && lo == 0 && hi == (int64_t)plan.size();
+    const int sched = rec ? 2 : h->scheduler;
+    std::vector<long long> rec_base(plan.size(), 0);
+    std::vector<size_t> rec_prefix_off(plan.size(), 0);
+    if (rec) {
+        h->rec_prefix_host.clear();
+        long long total = 0;
+        for (size_t pi = 0; pi < plan.size(); ++pi) {
+            const int b = plan[pi].b, t = plan[pi].t;
+            rec_base[pi] = 2 * total;
+            rec_prefix_off[pi] = h->rec_prefix_host.size();
+            long long acc = 0;
+            for (int64_t r = 0; r < n; ++r) {
+                h->rec_prefix_host.push_back(acc);
+                acc += steps_of_sweep(n, b, t, r);
+            }
+            total += acc;
+        }
+        const size_t es = sizeof(T);
+        const size_t vb = es * (size_t)(2 * total) * (size_t)(tw + 1), tb = es * (size_t)(2 * total);
+        const size_t pb = sizeof(long long) * h->rec_prefix_host.size();
+        auto grow = [&](void** ptr, size_t* have, size_t need) -> cudaError_t {
+            if (*have >= need && *ptr) return cudaSuccess;
+            if (*ptr) cudaFree(*ptr);
+            *ptr = nullptr;
+            *have = 0;
+            cudaError_t e2 = cudaMalloc(ptr, std::max<size_t>(need, 16));
+            if (e2 == cudaSuccess) *have = need;
+            return e2;
+        };
+        err = grow(&h->rec_v, &h->rec_v_bytes, vb);
+        if (err == cudaSuccess) err = grow(&h->rec_tau, &h->rec_tau_bytes, tb);
+        if (err == cudaSuccess) err = grow((void**)&h->rec_prefix, &h->rec_prefix_bytes, pb);
+        if (err != cudaSuccess) return fail(BB_ERR_NOMEM, "reflector record allocation failed");
+        err = cudaMemcpyAsync(h->rec_prefix, h->rec_prefix_host.data(), pb, cudaMemcpyHostToDevice, s);
+        if (err != cudaSuccess) return cuda_fail(err, "reflector record prefix copy");
+    }
     auto pass_args = [&](int64_t pi, int64_t ld) {
         const int b = plan[pi].b, t = plan[pi].t;
         bb::PassArgs P;
@@ -441,6 +497,13 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         P.lagh = bb::pass_lag_half(b, t);
         P.stall_sweep = h->stall_sweep;
         P.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+        if (rec) {
+            P.rec_v = h->rec_v;
+            P.rec_tau = h->rec_tau;
+            P.rec_prefix = h->rec_prefix + rec_prefix_off[pi];
+            P.rec_base = rec_base[pi];
+            P.rec_stride = (int)tw + 1;
+        }
         return P;
     };
     // The group kernel moves whole columns with bulk copies, which need a
@@ -450,7 +513,7 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
     int64_t ldw = ldab;
     bool any_group = false;
     for (int64_t pi = lo; pi < hi; ++pi)
-        any_group = any_group || bb::choose_group(pass_args(pi, ldab), h->scheduler, h->group_size, sizeof(T), nullptr);
+        any_group = any_group || bb::choose_group(pass_args(pi, ldab), sched, h->group_size, sizeof(T), nullptr);
     if (any_group && !bb::group_layout_ok(band, ldab, sizeof(T))) {
         const int64_t q = 16 / (int64_t)sizeof(T);
         ldw = (ldab + q - 1) / q * q;
@@ -491,10 +554,10 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         cfg.group_size = h->group_size;
         bb::LaunchStats st;
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo)], s);
-        if (h->scheduler == 4) {
+        if (sched == 4) {
             err = run_pass_graph<T>(h, pi, wb, ldw, P, cfg, s, &st);
         } else {
-            err = bb::run_pass<T>(wb, P, h->scheduler, cfg, h->d_progress, h->d_status, s, &st);
+            err = bb::run_pass<T>(wb, P, sched, cfg, h->d_progress, h->d_status, s, &st);
         }
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo) + 1], s);
         h->last_launches += st.launches;
@@ -510,6 +573,10 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
         err = cudaMemcpy2DAsync(band, sizeof(T) * ldab, wb, sizeof(T) * ldw, sizeof(T) * ldab, (size_t)n,
                                 cudaMemcpyDeviceToDevice, s);
         if (err != cudaSuccess) return cuda_fail(err, "copy back from the working band");
+    }
+    if (rec) {
+        h->rec_valid = true;
+        h->rec_tw = tw;
     }
     return BB_OK;
 }
@@ -589,6 +656,29 @@ bb_status bb_sym_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, 
     } catch (...) {
         return fail(BB_ERR_INTERNAL, "bb_sym_reduce: unexpected host exception");
     }
+}
+
+bb_status bb_back_transform(bb_handle* h, void* U, int64_t ldu, void* V, int64_t ldv, bb_stream_t stream) {
+    if (!h) return fail(BB_ERR_INVALID_ARG, "null handle");
+    if (!h->rec_valid)
+        return fail(BB_ERR_INVALID_ARG, "bb_back_transform: no recorded reduction (set BB_PARAM_RECORD first)");
+    if ((U && ldu < h->n) || (V && ldv < h->n)) return fail(BB_ERR_INVALID_ARG, "ldu and ldv must be >= n");
+    if ((U && !is_device_pointer(U)) || (V && !is_device_pointer(V)))
+        return fail(BB_ERR_INVALID_ARG, "U and V must be device pointers");
+    long long nl = 0;
+    cudaError_t err;
+    const int stride = (int)h->rec_tw + 1;
+    if (h->dtype == BB_F32)
+        err = bb::run_back_transform<float>(h->n, (int)h->bw, (int)h->rec_tw, (const float*)h->rec_v,
+                                            (const float*)h->rec_tau, stride, (float*)U, ldu, (float*)V, ldv,
+                                            h->num_sms, (cudaStream_t)stream, &nl);
+    else
+        err = bb::run_back_transform<double>(h->n, (int)h->bw, (int)h->rec_tw, (const double*)h->rec_v,
+                                             (const double*)h->rec_tau, stride, (double*)U, ldu, (double*)V, ldv,
+                                             h->num_sms, (cudaStream_t)stream, &nl);
+    h->last_launches = nl;
+    if (err != cudaSuccess) return cuda_fail(err, "bb_back_transform launch");
+    return BB_OK;
 }
 
 bb_status bb_reduce_host(bb_handle* h, const void* band_host, int64_t ldab, int64_t tw,

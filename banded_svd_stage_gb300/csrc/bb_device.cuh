@@ -39,7 +39,30 @@ struct PassArgs {
     int lagh;             // half-step lag of the persistent scheduler (2, 3 or 4)
     int stall_sweep;      // fault injection: this sweep never publishes (-1: none)
     unsigned long long wait_budget;  // SM clock cycles a flag wait may spin
+    // Reflector record for the back-transformation (rec_v == nullptr: none).
+    // Reflector (sweep r, step k, side 0 right / 1 left) of this pass goes to
+    // index rec_base + 2 (rec_prefix[r] + k) + side: v in rec_v[index *
+    // rec_stride ..] (v_0 = 1), tau in rec_tau[index].  rec_prefix[r] = the
+    // steps of the sweeps before r in this pass.
+    void* rec_v = nullptr;
+    void* rec_tau = nullptr;
+    const long long* rec_prefix = nullptr;
+    long long rec_base = 0;
+    int rec_stride = 0;
 };
+
+// Records the reflector warp_larfg just built (s_v, s_tau) when the pass
+// keeps a record; called by the warp that built it.  Lane m wrote s_v[m]
+// itself and lane 0 the scalar, so no synchronisation is needed.
+template <typename T>
+__device__ __forceinline__ void record_reflector(const PassArgs& P, long long r, int k, int side, int W,
+                                                 const T* s_v, const T* s_tau, int lane) {
+    if (P.rec_v == nullptr) return;
+    const long long idx = P.rec_base + 2 * (P.rec_prefix[r] + k) + side;
+    T* v = static_cast<T*>(P.rec_v) + idx * P.rec_stride;
+    for (int m = lane; m < W; m += 32) v[m] = s_v[m];
+    if (lane == 0) static_cast<T*>(P.rec_tau)[idx] = *s_tau;
+}
 
 // Number of steps of sweep r: k runs while c_k + 1 <= n - 1.
 __device__ __forceinline__ int sweep_steps(const PassArgs& P, long long r) {
@@ -315,6 +338,7 @@ __device__ __forceinline__ bool right_pre(T* __restrict__ band, const PassArgs& 
             xp[q] = (m < W) ? sm.tile[(P.b + m) * sm.wp] : T(0);
         }
         T beta = warp_larfg<T, NPL>(xp, W, lane, sm.v, sm.tau);
+        record_reflector<T>(P, r, k, 0, W, sm.v, sm.tau, lane);
 #pragma unroll
         for (int q = 0; q < NPL; ++q) {
             const int m = lane + 32 * q;
@@ -346,6 +370,7 @@ __device__ __forceinline__ void right_post(T* __restrict__ band, const PassArgs&
                 xp[q] = (m < W) ? __ldcg(base + g.p + (g.c + m) * stride) : T(0);
             }
             T beta = warp_larfg<T, NPL>(xp, W, lane, sm.v, sm.tau);
+            record_reflector<T>(P, r, k, 0, W, sm.v, sm.tau, lane);
 #pragma unroll
             for (int q = 0; q < NPL; ++q) {
                 const int m = lane + 32 * q;
@@ -452,6 +477,7 @@ __device__ __forceinline__ void left_pre(T* __restrict__ band, const PassArgs& P
             xc[q] = (m < W) ? sm.tile[m] : T(0);
         }
         T beta = warp_larfg<T, NPL>(xc, W, lane, sm.v, sm.tau);
+        record_reflector<T>(P, r, k, 1, W, sm.v, sm.tau, lane);
         __syncwarp();
 #pragma unroll
         for (int q = 0; q < NPL; ++q) {

@@ -136,10 +136,15 @@ enum {
                                    pass never reports progress (-1 = off, default)      */
     BB_PARAM_TIMING = 7,        /* 1: record CUDA events around every pass launch, read
                                    back with bb_last_pass_ms (default 0)                */
-    BB_PARAM_GROUP_SIZE = 8     /* sweeps per group of the group kernel: 0 = largest
+    BB_PARAM_GROUP_SIZE = 8,    /* sweeps per group of the group kernel: 0 = largest
                                    that fits shared memory, at most 13, or 5 when a
                                    reflector of tw + 1 elements takes more than 68
                                    bytes (default)                                      */
+    BB_PARAM_RECORD = 9         /* 1: keep every reflector of the next whole reductions
+                                   (all passes) for bb_back_transform; the passes then
+                                   run on the flag kernel (scheduler 2) and the handle
+                                   holds 2 x steps x (tw + 1) + 2 x steps elements of
+                                   device memory (default 0)                            */
 };
 bb_status bb_set_param(bb_handle* h, int param, int64_t value);
 int64_t bb_get_param(const bb_handle* h, int param);
@@ -166,6 +171,17 @@ int64_t bb_get_param(const bb_handle* h, int param);
 bb_status bb_sym_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out, void* e_out,
                         bb_stream_t stream);
 int64_t bb_sym_required_ldab(int64_t bw, int64_t tw);
+/* Back-transformation of the last whole reduction run with BB_PARAM_RECORD:
+ * U = L_1 L_2 ... and V = R_1 R_2 ..., the products of the left and right
+ * reflectors in the order applied, so that A = U B V^T with B the bidiagonal
+ * (d, e).  U and V are device, column-major n x n (leading dimensions ldu,
+ * ldv >= n), the handle's element type; either may be null to skip it.  The
+ * singular vectors of A are then U U_b and V V_b for B = U_b S V_b^T.  Both
+ * are formed from the identity, one launch per sweep and matrix (the
+ * reflectors of a sweep act on disjoint columns and run at once).
+ * Asynchronous on `stream`.  BB_ERR_INVALID_ARG without such a reduction on
+ * this handle, or for bad arguments. */
+bb_status bb_back_transform(bb_handle* h, void* U, int64_t ldu, void* V, int64_t ldv, bb_stream_t stream);
 
 /* Pass plan of (bw, tw) (b = bw; while b > 1: t = min(tw, b - 1); b -= t):
  * the number of passes, ceil((bw - 1) / tw), and the (b, t) of pass i,

@@ -164,6 +164,10 @@ def test_header_is_c99_and_links_against_the_library(lib, tmp_path):
     assert res.returncode == 0, res.stderr
 
 
+def test_back_transform_rejects_a_null_handle(lib):
+    assert lib.bb_back_transform(None, None, 1, None, 1, None) == bb.BB_ERR_INVALID_ARG
+
+
 def test_noalloc_argument_errors_need_no_gpu(lib):
     # bb_reduce_noalloc checks every argument before its first CUDA call
     fake = 0x1000  # never dereferenced: every call below is rejected first
