@@ -114,11 +114,10 @@ __device__ __forceinline__ void load_v(const T* __restrict__ v, T (&vr)[WMAX]) {
 // The half-step's columns span fewer than nslot slots, so a slot index past
 // the end wraps with one subtraction.
 template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g, T* vb, T* taub) {
+__device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    const int s0 = cb.slot(g.c);
     // A(p + i, c + m) = cb.cols[a0 + i + m (lds - 1) - (m >= mwrap ? nslot lds : 0)]:
     // column c + m sits in slot s0 + m, wrapped once past the end
     const int a0 = s0 * cb.lds + cb.off + (g.p - g.c);
@@ -174,11 +173,10 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
 // one warp: reflector from column c, then lane i applies it to columns
 // c+1+i, +32, ...
 template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, T* vb, T* taub) {
+__device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    const int s0 = cb.slot(g.c);
     T* colc = cb.cols + s0 * cb.lds + cb.off;  // colc[m] = A(c + m, c)
     T xc[NPL];
 #pragma unroll
@@ -223,15 +221,18 @@ __device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, 
 }
 
 template <typename T, int WMAX>
-__device__ __forceinline__ void group_half(const PassArgs& P, const ColBuf<T>& cb, int r, int h, T* vb, T* taub) {
+// slot: the buffer slot of column c of this half-step's step (the caller
+// carries it from step to step, sparing a modulo on the critical path).
+__device__ __forceinline__ void group_half(const PassArgs& P, const ColBuf<T>& cb, int r, int h, int slot, T* vb,
+                                           T* taub) {
     const GGeom g = gstep(P, r, h >> 1);
     const bool full = g.w == WMAX;
     if ((h & 1) == 0) {
-        if (full) group_right<T, WMAX, true>(cb, g, vb, taub);
-        else group_right<T, WMAX, false>(cb, g, vb, taub);
+        if (full) group_right<T, WMAX, true>(cb, g, slot, vb, taub);
+        else group_right<T, WMAX, false>(cb, g, slot, vb, taub);
     } else {
-        if (full) group_left<T, WMAX, true>(cb, g, vb, taub);
-        else group_left<T, WMAX, false>(cb, g, vb, taub);
+        if (full) group_left<T, WMAX, true>(cb, g, slot, vb, taub);
+        else group_left<T, WMAX, false>(cb, g, slot, vb, taub);
     }
 }
 
@@ -469,6 +470,10 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
         if (warp < GA.g) {
             // ---- compute warps ----
             const int my_h_end = (warp < ng) ? 2 * s_nsteps[warp] : 0;
+            // slot of column c of this warp's current step: one modulo per
+            // group, then + b per step (one wrap when nslot > b, as the
+            // footprint of a whole step gives; the loop keeps it exact anyway)
+            int my_slot = -1;
             int stage = (int)(T0 % (unsigned)S);
             unsigned phase = (T0 / (unsigned)S) & 1u;
             for (int tau = 0; tau < tend; ++tau) {
@@ -481,7 +486,13 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 if (s_abort_tick <= tau) break;  // same tick for every compute warp
                 const int h = tau - L * warp;
                 if (!s_dead && h >= 0 && h < my_h_end) {
-                    group_half<T, WMAX>(P, cb, r0 + warp, h, vbuf + (size_t)warp * VS, taubuf + warp);
+                    if (my_slot < 0) {
+                        my_slot = cb.slot(r0 + warp + P.bp + (h >> 1) * P.b);
+                    } else if ((h & 1) == 0) {
+                        my_slot += P.b;
+                        while (my_slot >= cb.nslot) my_slot -= cb.nslot;
+                    }
+                    group_half<T, WMAX>(P, cb, r0 + warp, h, my_slot, vbuf + (size_t)warp * VS, taubuf + warp);
                     // the storer's bulk copies read these columns through the async proxy
                     if (GA.bulk_store) fence_proxy_async_smem();
                 }
