@@ -133,7 +133,8 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
-def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int, with_e2e: bool):
+def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int, with_e2e: bool,
+             group_size: int = 0):
     import torch
 
     import banded_svd_stage_gb300 as bb
@@ -147,6 +148,8 @@ def run_ours(w: bi.Workload, steps: int, warmup: int, scheduler: int, rank: int,
     work = torch.empty_like(pristine)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     red = Reducer(w.n, w.bw, tdt, scheduler=scheduler)
+    if group_size:
+        bb.bb_set_param(red.h, bb.BB_PARAM_GROUP_SIZE, group_size)
     red.enable_timing(True)
     d = torch.empty(w.n, dtype=tdt, device=dev)
     e = torch.empty(w.n, dtype=tdt, device=dev)
@@ -339,6 +342,27 @@ def _model_bytes_py(w):
     return tot
 
 
+def latency_chain(n: int, bw: int, tw: int, pass_ms):
+    """Per pass of the plan: the sweeps, the half-step lag L between
+    consecutive sweeps (2 when b - t >= 3, 3 when b - t == 2, 4 when
+    b - t == 1) and the measured time per lag unit, pass_ms / (sweeps * L).
+    A pass is a chain of about sweeps * L dependent half-steps, so this is
+    the effective latency of one link, the quantity the kernels must lower
+    (the bytes a link moves are fixed by the method)."""
+    out = []
+    b, i = bw, 0
+    while b > 1 and i < len(pass_ms):
+        t = min(tw, b - 1)
+        bp = b - t
+        lag = 2 if bp >= 3 else (3 if bp == 2 else 4)
+        sweeps = max(0, n - bp - 1)
+        us = (pass_ms[i] * 1e3 / (sweeps * lag)) if sweeps and pass_ms[i] is not None else None
+        out.append({"b": b, "t": t, "sweeps": sweeps, "lag": lag, "us_per_link": us})
+        b -= t
+        i += 1
+    return out
+
+
 KERNEL_NAMES = {1: "pass_cycle_kernel", 2: "pass_persistent_kernel", 3: "pass_group_kernel",
                 4: "pass_cycle_kernel"}
 SCHEDULER_NAMES = {0: "auto", 1: "per-cycle", 2: "flags", 3: "group", 4: "per-cycle-graph"}
@@ -388,6 +412,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=MAIN_WORKLOAD)
     ap.add_argument("--scheduler", type=int, default=0)
+    ap.add_argument("--group-size", type=int, default=0,
+                    help="sweeps per CTA of the group kernel (0: the planner's choice)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (e2e) leg")
@@ -438,7 +464,8 @@ def main():
     if sampler:
         sampler.start()
     t_wall0 = time.perf_counter()
-    res = run_ours(w, args.steps, args.warmup, args.scheduler, rank, with_e2e=(world == 1 and not args.no_e2e))
+    res = run_ours(w, args.steps, args.warmup, args.scheduler, rank, with_e2e=(world == 1 and not args.no_e2e),
+                   group_size=args.group_size)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -465,12 +492,14 @@ def main():
             if name == w.name:
                 continue
             ww = bi.by_name(name)
-            r2 = run_ours(ww, max(2, min(args.steps, 3)), 1, args.scheduler, rank, with_e2e=False)
+            r2 = run_ours(ww, max(2, min(args.steps, 3)), 1, args.scheduler, rank, with_e2e=False,
+                          group_size=args.group_size)
             m2 = statistics.median(r2["ms"])
             g2 = r2["model_bytes"] / (m2 * 1e-3) / 1e9
             sweep.append({"workload": name, "ms_per_reduction": m2, "min_ms": min(r2["ms"]),
                           "effective_gbs": g2, "frac_of_hbm": g2 / hbm,
-                          "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"]})
+                          "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"],
+                          "latency_chain": latency_chain(ww.n, ww.bw, ww.tw, r2["pass_ms_mean"])})
 
     svals = None
     if rank == 0 and world == 1 and not args.no_sweep:
@@ -490,6 +519,7 @@ def main():
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "n": w.n, "bw": w.bw, "tw": w.tw, "dist": w.dist,
                        "graded": w.graded, "scheduler": SCHEDULER_NAMES.get(args.scheduler, str(args.scheduler)),
+                       "group_size": args.group_size or "planner",
                        "l2": "flushed between steps (256 MiB write); band restored before each step",
                        "parallelism": f"replicas x{world}"},
             "frac_of_hbm": value / hbm,
@@ -502,6 +532,7 @@ def main():
             "wall_s": wall,
             "pass_kernels": res["kernels"],
             "pass_ms": res["pass_ms_mean"],
+            "latency_chain": latency_chain(w.n, w.bw, w.tw, res["pass_ms_mean"]),
             "per_workload": sweep,
             "singular_values": svals,
         }

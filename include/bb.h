@@ -224,10 +224,12 @@ bb_status bb_reduce_noalloc(void* band_ptr, int64_t n, int64_t bw, int64_t ldab,
  * entries) and superdiagonal e (n - 1 entries; may be NULL when n == 1), in
  * descending order, into sigma_out (n entries).  All three are device
  * pointers owned by the caller, of element type dtype; n >= 1.  Computed by
- * bisection on Sturm counts of the 2n x 2n Golub-Kahan tridiagonal (zero
- * diagonal, off-diagonal d_0, e_0, d_1, ..., d_{n-1}), one thread per value,
- * with LAPACK xSTEBZ's pivmin guard, to an absolute accuracy of about one
- * ulp of the Gershgorin bound max_i(|a_{i-1}| + |a_i|).  This is the step
+ * multisection on Sturm counts of the 2n x 2n Golub-Kahan tridiagonal (zero
+ * diagonal, off-diagonal d_0, e_0, d_1, ..., d_{n-1}) with LAPACK xSTEBZ's
+ * pivmin guard: a group of P lanes per value (P a power of two up to 32, the
+ * most that fill the GPU) splits the interval into P + 1 parts per step,
+ * down to about one ulp of the Gershgorin bound max_i(|a_{i-1}| + |a_i|),
+ * the absolute accuracy.  This is the step
  * after the reduction in "A two-stage reduction on an Apple M5 Pro"
  * (Section 7).  Asynchronous on `stream`; allocates nothing; the return code
  * covers arguments and the launch. */

@@ -130,3 +130,29 @@ def test_group_plan_rejects_inconsistent_shapes(lib):
                  (0, 0, 1, 4, 0), (100, 16, 8, 4, -1)):
         with pytest.raises(bb.BBError):
             bb.bb_group_plan(*args)
+
+
+def test_header_is_c99_and_links_against_the_library(lib, tmp_path):
+    # the boundary is a C ABI: a C99 translation unit includes the header with
+    # every warning an error, takes the address of every declared function,
+    # and links against libbb.so (nothing runs: that would need a GPU)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    names = declared_functions()
+    src = ["#include <stdio.h>", '#include "bb.h"', "int main(void) {", "    void* fns[] = {"]
+    src += [f"        (void*){n}," for n in names]
+    src += ["    };", "    unsigned long long s = 0;",
+            "    for (unsigned i = 0; i < sizeof fns / sizeof fns[0]; ++i) s += (unsigned long long)fns[i] != 0;",
+            '    printf("%llu\\n", s);', "    return 0;", "}"]
+    c = tmp_path / "uses_bb.c"
+    c.write_text("\n".join(src) + "\n")
+    libdir = os.path.dirname(bb.LIB_PATH)
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror",
+           "-I", os.path.join(ROOT, "include"), str(c), "-o", str(tmp_path / "uses_bb"),
+           "-L", libdir, "-l:libbb.so", f"-Wl,-rpath-link,{libdir}",
+           "-Wl,--unresolved-symbols=ignore-in-shared-libs"]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr

@@ -89,3 +89,14 @@ def test_traffic_digest_covers_the_pass_kernels_only():
     # the boundary and the other kernels are not part of it
     assert not srcs & {"bb_api.cu", "bb_noalloc.cu", "bb_svals.cu"}
     assert len(bl.source_digest()) == 16
+
+
+def test_latency_chain_of_the_main_workload():
+    # measured pass times of the main workload (n = 4096, bw = 16, tw = 8)
+    out = bench.latency_chain(4096, 16, 8, [11.19, 19.89])
+    assert [(p["b"], p["t"], p["sweeps"], p["lag"]) for p in out] == [(16, 8, 4087, 2), (8, 7, 4094, 4)]
+    assert abs(out[0]["us_per_link"] - 11.19e3 / (4087 * 2)) < 1e-9
+    assert abs(out[1]["us_per_link"] - 19.89e3 / (4094 * 4)) < 1e-9
+    # every pass of the largest workload, lags 2 except the last (b - t = 1)
+    big = bench.latency_chain(32768, 256, 32, [1.0] * 8)
+    assert [p["lag"] for p in big] == [2] * 7 + [4] and big[-1]["t"] == 31
