@@ -1,7 +1,8 @@
 """Benchmark of the band -> bidiagonal reduction on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--scheduler 0|1|2|3|4] [--no-sweep]
+                    [--workload NAME] [--scheduler 0|1|2|3|4] [--group-size G]
+                    [--no-sweep] [--no-cpu] [--no-e2e]
 
 One step is one whole reduction (every pass down to bidiagonal form, plus the
 fill-row zeroing and the d/e extraction) of one synthetic band.  Before each
@@ -19,6 +20,15 @@ is all ranks' bytes over the slowest rank's time.
 
 --impl reference times the CPU oracle (the plain serial implementation the
 tests check the GPU against) on the host, on the same workload and metric.
+
+Besides the contract's keys the line carries: roofline (the dominant pass
+kernel against the measured HBM copy rate, with its ncu DRAM traffic),
+cpu_baseline (the serial oracle on one host core), cpu_pipelined (the
+oracle's multi-thread pipelined chase, context only), e2e (host buffers in,
+d and e out, copies timed), latency_chain (per pass: sweeps, half-step lag
+and the measured time per dependent link, the quantity that bounds these
+latency chains), per_workload (the other workloads) and singular_values
+(bb_singular_values on the reduction's output).
 """
 from __future__ import annotations
 

@@ -20,7 +20,11 @@ Also here:
   * ``bidiagonal_singular_values``: singular values of a bidiagonal by the
     Golub-Kahan tridiagonal's eigenvalues;
   * ``bidiagonal_with_vectors``: the reduction with its reflectors kept and
-    applied to the identity, A = U B V^T (the back-transformation).
+    applied to the identity, A = U B V^T (the back-transformation);
+  * ``dense_to_band``: stage 1, a dense matrix to upper band form by block
+    Householder (numpy, with this oracle's larfg);
+  * half-precision storage: a float16 band is reduced with float arithmetic,
+    every entry written back rounded to binary16 (``has_half``).
 """
 from __future__ import annotations
 
@@ -58,7 +62,11 @@ def compile_library(src: str, out: str) -> str:
 def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     """Declare the argument and result types of the oracle's C functions."""
     i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-    for sfx in ("_d", "_f"):
+    lib.oracle_has_half.argtypes = []
+    lib.oracle_has_half.restype = ci
+    for sfx in ("_d", "_f", "_h"):
+        if sfx == "_h" and not lib.oracle_has_half():
+            continue
         getattr(lib, "oracle_larfg" + sfx).argtypes = [i64, p, p, i64, p]
         getattr(lib, "oracle_larfg" + sfx).restype = None
         getattr(lib, "oracle_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64, i64, i64]
@@ -76,6 +84,8 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).restype = ci
         getattr(lib, "oracle_reduce_band_record" + sfx).argtypes = [i64, i64, i64, p, i64, i64, p, p, p, p, p]
         getattr(lib, "oracle_reduce_band_record" + sfx).restype = i64
+        if sfx == "_h":
+            continue  # the symmetric variant has no half-precision storage instantiation
         getattr(lib, "oracle_sym_reduce_band" + sfx).argtypes = [i64, i64, i64, p, i64]
         getattr(lib, "oracle_sym_reduce_band" + sfx).restype = ci
         getattr(lib, "oracle_sym_reduce_dense" + sfx).argtypes = [i64, i64, i64, p]
@@ -102,7 +112,21 @@ def _sfx(arr: np.ndarray) -> str:
         return "_d"
     if arr.dtype == np.float32:
         return "_f"
+    if arr.dtype == np.float16:
+        if not has_half():
+            raise TypeError("this build of the oracle has no half-precision storage (no _Float16)")
+        return "_h"
     raise TypeError(f"unsupported dtype {arr.dtype}")
+
+
+def has_half() -> bool:
+    """Whether the oracle was built with the half-precision storage variant."""
+    return bool(_load().oracle_has_half())
+
+
+def _arith(dt) -> np.dtype:
+    """Arithmetic type of a band of dtype dt (float for half storage)."""
+    return np.dtype(np.float32) if np.dtype(dt) == np.float16 else np.dtype(dt)
 
 
 def _ptr(a: np.ndarray):
@@ -174,8 +198,8 @@ def reduce_band_record(band: np.ndarray, n: int, bw: int, tw: int):
     side = np.zeros(cap, dtype=np.int8)
     start = np.zeros(cap, dtype=np.int64)
     width = np.zeros(cap, dtype=np.int32)
-    taus = np.zeros(cap, dtype=band.dtype)
-    vs = np.zeros((cap, tw + 1), dtype=band.dtype)
+    taus = np.zeros(cap, dtype=_arith(band.dtype))
+    vs = np.zeros((cap, tw + 1), dtype=_arith(band.dtype))
     got = getattr(_load(), "oracle_reduce_band_record" + _sfx(band))(
         n, bw, tw, _ptr(band), band.shape[1], cap, _ptr(side), _ptr(start), _ptr(width), _ptr(taus), _ptr(vs))
     if got == -1:
@@ -229,8 +253,9 @@ def sweep_steps(n: int, b: int, t: int, r: int) -> int:
 
 
 def extract(band: np.ndarray, n: int, ku: int):
-    d = np.zeros(n, dtype=band.dtype)
-    e = np.zeros(max(n - 1, 0), dtype=band.dtype)
+    """(d, e) of band storage, in the arithmetic type (float for half storage)."""
+    d = np.zeros(n, dtype=_arith(band.dtype))
+    e = np.zeros(max(n - 1, 0), dtype=_arith(band.dtype))
     getattr(_load(), "oracle_extract_band" + _sfx(band))(n, ku, _ptr(band), band.shape[1],
                                                          _ptr(d), _ptr(e))
     return d, e
@@ -249,6 +274,50 @@ def bidiagonal_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: in
     work = np.ascontiguousarray(band.copy())
     reduce_band_pipelined(work, n, bw, tw, threads, time_limit)
     return extract(work, n, bw + tw)
+
+
+# ------------------------------------------------ stage 1: dense -> band ---
+
+def dense_to_band(a: np.ndarray, bw: int) -> np.ndarray:
+    """Stage 1 of the two-stage SVD: an n x n matrix reduced to upper band
+    form of bandwidth bw by orthogonal transformations, the "classical block
+    Householder reduction" of the accuracy protocol ("Accelerating
+    Bidiagonalization of Banded Matrices through Memory-Aware Bulge-Chasing on
+    GPUs", Section V; the GPU stage of "A two-stage reduction on an Apple M5
+    Pro" uses the same panels).  For each panel of bw columns k .. k+bw-1:
+    QR of the panel column by column (reflector of A(j.., j), applied from the
+    left to every later column), then LQ of the panel's rows to the right of
+    the band, row by row (reflector of A(i, i+bw ..), applied from the right
+    to every later row).  Reflectors are this oracle's larfg; annihilated
+    entries are set to exactly zero.  Returns a new array (same dtype)."""
+    a = np.array(a, copy=True)
+    n = a.shape[0]
+    if bw < 1:
+        raise ValueError("bw must be at least 1")
+    for k in range(0, n, bw):
+        kb = min(k + bw, n)
+        for j in range(k, kb):
+            if j + 1 >= n:
+                break
+            beta, v, tau = larfg(a[j, j], a[j + 1:, j].copy())
+            a[j, j] = beta
+            a[j + 1:, j] = 0
+            if tau != 0:
+                u = np.concatenate([[1.0], v]).astype(a.dtype)
+                y = u @ a[j:, j + 1:]
+                a[j:, j + 1:] -= tau * np.outer(u, y)
+        for i in range(k, kb):
+            c0 = i + bw
+            if c0 + 1 >= n:
+                break
+            beta, v, tau = larfg(a[i, c0], a[i, c0 + 1:].copy())
+            a[i, c0] = beta
+            a[i, c0 + 1:] = 0
+            if tau != 0:
+                u = np.concatenate([[1.0], v]).astype(a.dtype)
+                y = a[i + 1:, c0:] @ u
+                a[i + 1:, c0:] -= tau * np.outer(y, u)
+    return a
 
 
 # ------------------------------------------------ symmetric variant -------

@@ -90,3 +90,19 @@ static double oracle_now_(void) {
 #include "bb_oracle_body.h"
 #include "sb_oracle_body.h"
 #undef STEP_BODY
+
+/* half-precision storage, float arithmetic (suffix _h): the band is IEEE
+ * binary16; every half-step reads its entries into float, forms and applies
+ * the reflector in float, and rounds each entry it writes to binary16 (round
+ * to nearest even).  Built where the compiler has _Float16. */
+#ifdef __FLT16_MANT_DIG__
+#undef SFX
+#define SFX _h
+#define BAND_T _Float16
+#include "bb_oracle_body.h"
+#undef STEP_BODY
+#undef BAND_T
+int oracle_has_half(void) { return 1; }
+#else
+int oracle_has_half(void) { return 0; }
+#endif

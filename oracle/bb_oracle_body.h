@@ -10,6 +10,14 @@
 #define CAT(a, b) CAT2(a, b)
 #define FN(name) CAT(name, SFX)
 
+/* Element type of the band storage; the arithmetic type is REAL.  They are
+ * the same except in the half-precision storage instantiation, where every
+ * read widens to REAL and every write rounds to the storage type. */
+#ifndef BAND_T
+#define BAND_T REAL
+#define BAND_T_DEFAULTED_
+#endif
+
 /* Euclidean norm of x[0], x[inc], ..., x[(m-1)*inc]: plain sum of squares in
  * index order.  When that sum under- or overflows while the entries are
  * finite and not all zero, the same sum is taken on entries divided by the
@@ -142,7 +150,7 @@ void FN(oracle_larfg)(int64_t m, REAL* alpha, REAL* x, int64_t inc, REAL* tau) {
 
 /* One half-step (side 0 = right/horizontal, 1 = left/vertical) of sweep r,
  * step k of the pass (b, t), windows exactly as in STEP_BODY. */
-void FN(oracle_halfstep_band)(int64_t n, int64_t b, int64_t t, int64_t ku, REAL* band, int64_t ldab,
+void FN(oracle_halfstep_band)(int64_t n, int64_t b, int64_t t, int64_t ku, BAND_T* band, int64_t ldab,
                               int64_t r, int64_t k, int side) {
     if (side == 0) STEP_BODY(p, ce, c, cend, 1, 0);
     else           STEP_BODY(p, ce, c, cend, 0, 1);
@@ -161,7 +169,7 @@ int64_t FN(oracle_sweep_steps)(int64_t n, int64_t b, int64_t t, int64_t r) {
  * advances), so that a run can be split at pass boundaries.
  * The fill rows 0..tw-1 and ku+1..ku+tw of every column are zeroed first when
  * pass_lo == 0.  Returns 0, or -1 on invalid arguments. */
-int FN(oracle_reduce_band)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab,
+int FN(oracle_reduce_band)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab,
                            int64_t pass_lo, int64_t pass_hi) {
     if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
     if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
@@ -212,7 +220,7 @@ int FN(oracle_reduce_band)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_
  * ------------------------------------------------------------------------- */
 typedef struct {
     int64_t n, b, t, ku, ldab, nthreads, thread;
-    REAL* band;
+    BAND_T* band;
     _Atomic int64_t* done;
     _Atomic int* stop;
     double deadline;
@@ -266,7 +274,7 @@ static void* FN(pipe_worker_)(void* arg) {
  * reflector vectors are written back for it).  cap is the room for
  * reflectors.  Returns the number recorded, -1 on invalid arguments, -2 when
  * cap is too small. */
-int64_t FN(oracle_reduce_band_record)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab, int64_t cap,
+int64_t FN(oracle_reduce_band_record)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab, int64_t cap,
                                       int8_t* side, int64_t* start, int32_t* width, REAL* taus, REAL* vs) {
     if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
     if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
@@ -307,7 +315,7 @@ int64_t FN(oracle_reduce_band_record)(int64_t n, int64_t bw, int64_t tw, REAL* b
  * bidiagonal or the symmetric one), joining the threads between passes.
  * Returns 0, -2 when the time limit ran out, -3 when the threads or the
  * counters could not be created. */
-static int FN(pipe_run_)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab, int64_t nthreads,
+static int FN(pipe_run_)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab, int64_t nthreads,
                          double time_limit_s, void* (*worker)(void*)) {
     const int64_t ku = bw + tw;
     _Atomic int64_t* done = (_Atomic int64_t*)malloc((size_t)n * sizeof(_Atomic int64_t));
@@ -347,7 +355,7 @@ static int FN(pipe_run_)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t 
  * nthreads (1 .. 1024) threads.  Returns 0; -1 on invalid arguments; -2 when
  * time_limit_s ran out (the band is then partly reduced); -3 when the
  * threads or the counters could not be created. */
-int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* band, int64_t ldab,
+int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab,
                                      int64_t nthreads, double time_limit_s) {
     if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
     if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
@@ -362,7 +370,7 @@ int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL* ba
 }
 
 /* d_i = A(i, i), e_i = A(i, i+1) from band storage. */
-void FN(oracle_extract_band)(int64_t n, int64_t ku, const REAL* band, int64_t ldab, REAL* d, REAL* e) {
+void FN(oracle_extract_band)(int64_t n, int64_t ku, const BAND_T* band, int64_t ldab, REAL* d, REAL* e) {
     for (int64_t i = 0; i < n; ++i) d[i] = ELEM(i, i);
     for (int64_t i = 0; i + 1 < n; ++i) e[i] = ELEM(i, i + 1);
 }
@@ -394,3 +402,7 @@ int FN(oracle_reduce_dense)(int64_t n, int64_t bw, int64_t tw, REAL* a) {
 #undef FN
 #undef CAT
 #undef CAT2
+#ifdef BAND_T_DEFAULTED_
+#undef BAND_T
+#undef BAND_T_DEFAULTED_
+#endif

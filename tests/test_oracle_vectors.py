@@ -135,3 +135,53 @@ def test_recording_mutant_is_caught(name, tmp_path, bound_library):
     ok = (np.linalg.norm(a - U @ dense_b(d, e) @ V.T) <= 1e-13 * np.linalg.norm(a)
           and np.abs(U.T @ U - np.eye(n)).max() <= 1e-13 and np.abs(V.T @ V - np.eye(n)).max() <= 1e-13)
     assert not ok, f"mutant {name} passes"
+
+
+def test_reflectors_of_one_sweep_are_disjoint_and_commute():
+    # what a blocked back-transformation relies on: within one sweep the right
+    # (left) reflectors act on disjoint column (row) ranges, so any order of
+    # applying them gives the same U, V bit for bit; consecutive sweeps
+    # overlap, so the order of the sweeps does matter
+    n, bw, tw = 60, 12, 5
+    band = bi.make_band(n, bw, tw, "f64", seed=8)
+    side, start, width, taus, vs = oracle.reduce_band_record(band.copy(), n, bw, tw)
+    # reflectors in order: pass -> sweep -> step -> (right, left)
+    groups = []
+    q = 0
+    for (b, t) in oracle.pass_plan(bw, tw):
+        for r in range(n):
+            K = oracle.sweep_steps(n, b, t, r)
+            if K:
+                groups.append(list(range(q, q + 2 * K)))
+                q += 2 * K
+    assert q == side.size
+
+    def apply(order):
+        U, V = np.eye(n), np.eye(n)
+        for i in order:
+            c, w, tau = int(start[i]), int(width[i]), float(taus[i])
+            if tau == 0.0:
+                continue
+            v = vs[i, :w]
+            M = U if side[i] == 1 else V
+            y = M[:, c:c + w] @ v
+            M[:, c:c + w] -= tau * np.outer(y, v)
+        return U, V
+
+    U0, V0 = apply(range(q))
+    rng = np.random.default_rng(0)
+    for g in groups:
+        for s_ in (0, 1):
+            idx = [i for i in g if side[i] == s_]
+            spans = sorted((int(start[i]), int(start[i]) + int(width[i]) - 1) for i in idx)
+            assert all(a[1] < b_[0] for a, b_ in zip(spans, spans[1:]))   # disjoint
+    shuffled = []
+    for g in groups:
+        g = list(g)
+        rng.shuffle(g)
+        shuffled += g
+    U1, V1 = apply(shuffled)
+    assert np.array_equal(U0, U1) and np.array_equal(V0, V1)
+    # consecutive sweeps overlap: reversing the sweep order changes the result
+    U2, V2 = apply([i for g in reversed(groups) for i in g])
+    assert not (np.array_equal(U0, U2) and np.array_equal(V0, V2))
