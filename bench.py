@@ -27,8 +27,11 @@ cpu_baseline (the serial oracle on one host core), cpu_pipelined (the
 oracle's multi-thread pipelined chase, context only), e2e (host buffers in,
 d and e out, copies timed), latency_chain (per pass: sweeps, half-step lag
 and the measured time per dependent link, the quantity that bounds these
-latency chains), per_workload (the other workloads) and singular_values
-(bb_singular_values on the reduction's output).
+latency chains), median_ms / min_ms (of this rank's timed steps),
+per_scheduler (the main workload under each scheduler: per-cycle launches,
+their CUDA-graph replay, the flag and the group kernel), per_workload (the
+other workloads) and singular_values (bb_singular_values on the reduction's
+output).
 """
 from __future__ import annotations
 
@@ -277,6 +280,20 @@ def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
             "d2h_bytes_per_step": int((2 * w.n - 1) * (4 if w.dtype == "f32" else 8))}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (Linux), for the CPU timings' context."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_oracle_rate(w: bi.Workload, budget_s: float = 12.0):
     """The oracle, as it stands, on one host core: whole reductions of the
     workload repeated until about budget_s seconds have elapsed (one at least)."""
@@ -297,7 +314,7 @@ def cpu_oracle_rate(w: bi.Workload, budget_s: float = 12.0):
         if el >= budget_s or el / reps * (reps + 1) > 2.5 * budget_s:
             break
     sec = el / reps
-    return {"value": model_bytes / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": model_bytes / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
             "ms_per_reduction": sec * 1e3,
             "sample": f"{reps} whole serial reductions of {w.name} ({el:.1f} s)"}
 
@@ -327,6 +344,7 @@ def cpu_pipelined_rate(w: bi.Workload, budget_s: float = 6.0):
             break
     sec = el / reps
     return {"value": model_bytes / sec / 1e9, "unit": "GB/s", "cores": P, "kind": "oracle, pipelined sweeps",
+            "cpu": cpu_model(),
             "ms_per_reduction": sec * 1e3,
             "sample": f"{reps} whole reductions of {w.name} on {P} threads ({el:.1f} s)"}
 
@@ -452,7 +470,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
                 "data": "synthetic", "config": {"workload": w.name, "n": w.n, "bw": w.bw, "tw": w.tw},
-                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                                  "sample": f"whole serial reductions of {w.name}, one per step"},
                 "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -511,6 +529,20 @@ def main():
                           "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"],
                           "latency_chain": latency_chain(ww.n, ww.bw, ww.tw, r2["pass_ms_mean"])})
 
+    # both scheduler families on the main workload, measured in the same run:
+    # per-cycle launches (plain and replayed from a CUDA graph) and the
+    # persistent kernels (flag, group); the headline uses the automatic choice
+    per_sched = None
+    if rank == 0 and world == 1 and not args.no_sweep:
+        per_sched = {}
+        for sc in (1, 4, 2, 3):
+            try:
+                rs = run_ours(w, max(2, min(args.steps, 3)), 1, sc, rank, with_e2e=False)
+                per_sched[SCHEDULER_NAMES[sc]] = {"median_ms": statistics.median(rs["ms"]), "min_ms": min(rs["ms"]),
+                                                  "launches": rs["launches"], "pass_ms": rs["pass_ms_mean"]}
+            except Exception as ex:  # a side measurement never loses the line
+                per_sched[SCHEDULER_NAMES[sc]] = {"error": f"{type(ex).__name__}: {ex}"}
+
     svals = None
     if rank == 0 and world == 1 and not args.no_sweep:
         svals = run_svals(w, args.steps, args.warmup)
@@ -543,6 +575,8 @@ def main():
             "pass_kernels": res["kernels"],
             "pass_ms": res["pass_ms_mean"],
             "latency_chain": latency_chain(w.n, w.bw, w.tw, res["pass_ms_mean"]),
+            "median_ms": statistics.median(res["ms"]), "min_ms": min(res["ms"]),
+            "per_scheduler": per_sched,
             "per_workload": sweep,
             "singular_values": svals,
         }

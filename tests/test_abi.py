@@ -156,3 +156,19 @@ def test_header_is_c99_and_links_against_the_library(lib, tmp_path):
            "-Wl,--unresolved-symbols=ignore-in-shared-libs"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
+
+
+def test_noalloc_argument_errors_need_no_gpu(lib):
+    # bb_reduce_noalloc checks every argument before its first CUDA call
+    fake = 0x1000  # never dereferenced: every call below is rejected first
+    f = lib.bb_reduce_noalloc
+    assert f(fake, 100, 8, 23, 7, 7, fake, fake, None) == bb.BB_ERR_DTYPE           # dtype
+    assert f(fake, 0, 0, 2, 1, bb.BB_F32, fake, fake, None) == bb.BB_ERR_INVALID_ARG  # n < 1
+    assert f(fake, 10, 10, 31, 1, bb.BB_F32, fake, fake, None) == bb.BB_ERR_INVALID_ARG  # bw >= n
+    assert f(fake, 65537, 8, 23, 7, bb.BB_F32, fake, fake, None) == bb.BB_ERR_INVALID_ARG  # beyond scratch
+    assert f(fake, 100, 8, 23, 8, bb.BB_F32, fake, fake, None) == bb.BB_ERR_INVALID_ARG  # tw > bw - 1
+    assert f(fake, 100, 8, 22, 7, bb.BB_F32, fake, fake, None) == bb.BB_ERR_LDAB          # ldab too small
+    assert f(None, 100, 8, 23, 7, bb.BB_F32, fake, fake, None) == bb.BB_ERR_INVALID_ARG  # null band
+    assert f(fake, 100, 8, 23, 7, bb.BB_F32, fake, None, None) == bb.BB_ERR_INVALID_ARG  # null e
+    # a band too wide for the flag kernel's shared-memory tile
+    assert f(fake, 20000, 9000, 9001 + 2 * 64, 64, bb.BB_F64, fake, fake, None) == bb.BB_ERR_INVALID_ARG

@@ -100,3 +100,8 @@ def test_latency_chain_of_the_main_workload():
     # every pass of the largest workload, lags 2 except the last (b - t = 1)
     big = bench.latency_chain(32768, 256, 32, [1.0] * 8)
     assert [p["lag"] for p in big] == [2] * 7 + [4] and big[-1]["t"] == 31
+
+
+def test_cpu_model_is_reported():
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m.strip()
