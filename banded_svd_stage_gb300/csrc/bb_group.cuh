@@ -79,16 +79,45 @@ __device__ __forceinline__ GGeom gstep(const PassArgs& P, int r, int k) {
     return g;
 }
 
+// Each warp's reflector buffer is padded to a multiple of 16 bytes, so that
+// the apply loads v into registers with 16-byte loads once per half-step.
+__host__ __device__ constexpr int group_v_stride(int wmax, int elem) {
+    return ((wmax * elem + 15) / 16 * 16) / elem;
+}
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+    using type = float4;
+};
+template <>
+struct Vec16<double> {
+    using type = double2;
+};
+template <typename T, int WMAX>
+__device__ __forceinline__ void load_v(const T* __restrict__ v, T (&vr)[WMAX]) {
+    constexpr int PER = 16 / (int)sizeof(T);
+    constexpr int NV = (WMAX + PER - 1) / PER;
+    using V = typename Vec16<T>::type;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+        const V c = reinterpret_cast<const V*>(v)[q];
+        const T* e = reinterpret_cast<const T*>(&c);
+#pragma unroll
+        for (int u = 0; u < PER; ++u)
+            if (q * PER + u < WMAX) vr[q * PER + u] = e[u];
+    }
+}
+
 // Right half-step (rows p..ce of columns c..ce) on the buffered band, by one
 // warp: reflector from row p, then lane i applies it to rows p+1+i, +32, ...
 // The half-step's columns span fewer than nslot slots, so a slot index past
 // the end wraps with one subtraction.
 template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g, T* vb, T* taub) {
+__device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    const int s0 = cb.slot(g.c);
     // A(p + i, c + m) = cb.cols[a0 + i + m (lds - 1) - (m >= mwrap ? nslot lds : 0)]:
     // column c + m sits in slot s0 + m, wrapped once past the end
     const int a0 = s0 * cb.lds + cb.off + (g.p - g.c);
@@ -112,7 +141,16 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
     __syncwarp();
     const T tau = *taub;
     if (tau == T(0)) return;
-    const T* v = vb;
+    // narrow reflectors: v in registers (16-byte loads, once per half-step);
+    // wide ones keep reading the shared buffer, which spares the registers
+    constexpr bool kVReg = WMAX * sizeof(T) <= 16 * 4;
+    T vreg[kVReg ? WMAX : 1];
+    if constexpr (kVReg) load_v<T, WMAX>(vb, vreg);
+    const T* vsh = vb;
+    auto v = [&](int m) -> T {
+        if constexpr (kVReg) return vreg[m];
+        else return vsh[m];
+    };
     const int nrows = g.ce - g.p;
     for (int i = 1 + lane; i <= nrows; i += 32) {
         const int a = a0 + i;
@@ -122,12 +160,12 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
                 x[m] = cb.cols[a + m * dm - ((m >= mwrap) ? wrap : 0)];
-                y = fma(x[m], v[m], y);
+                y = fma(x[m], v(m), y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) cb.cols[a + m * dm - ((m >= mwrap) ? wrap : 0)] = fma(-s, v[m], x[m]);
+            if (m < W) cb.cols[a + m * dm - ((m >= mwrap) ? wrap : 0)] = fma(-s, v(m), x[m]);
     }
 }
 
@@ -135,11 +173,10 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
 // one warp: reflector from column c, then lane i applies it to columns
 // c+1+i, +32, ...
 template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, T* vb, T* taub) {
+__device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    const int s0 = cb.slot(g.c);
     T* colc = cb.cols + s0 * cb.lds + cb.off;  // colc[m] = A(c + m, c)
     T xc[NPL];
 #pragma unroll
@@ -156,7 +193,14 @@ __device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, 
     __syncwarp();
     const T tau = *taub;
     if (tau == T(0)) return;
-    const T* v = vb;
+    constexpr bool kVReg = WMAX * sizeof(T) <= 16 * 4;
+    T vreg[kVReg ? WMAX : 1];
+    if constexpr (kVReg) load_v<T, WMAX>(vb, vreg);
+    const T* vsh = vb;
+    auto v = [&](int m) -> T {
+        if constexpr (kVReg) return vreg[m];
+        else return vsh[m];
+    };
     for (int dj = 1 + lane; dj <= g.cend - g.c; dj += 32) {
         int sl = s0 + dj;
         if (sl >= cb.nslot) sl -= cb.nslot;
@@ -167,25 +211,28 @@ __device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, 
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
                 x[m] = cj[m];
-                y = fma(v[m], x[m], y);
+                y = fma(v(m), x[m], y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) cj[m] = fma(-s, v[m], x[m]);
+            if (m < W) cj[m] = fma(-s, v(m), x[m]);
     }
 }
 
 template <typename T, int WMAX>
-__device__ __forceinline__ void group_half(const PassArgs& P, const ColBuf<T>& cb, int r, int h, T* vb, T* taub) {
+// slot: the buffer slot of column c of this half-step's step (the caller
+// carries it from step to step, sparing a modulo on the critical path).
+__device__ __forceinline__ void group_half(const PassArgs& P, const ColBuf<T>& cb, int r, int h, int slot, T* vb,
+                                           T* taub) {
     const GGeom g = gstep(P, r, h >> 1);
     const bool full = g.w == WMAX;
     if ((h & 1) == 0) {
-        if (full) group_right<T, WMAX, true>(cb, g, vb, taub);
-        else group_right<T, WMAX, false>(cb, g, vb, taub);
+        if (full) group_right<T, WMAX, true>(cb, g, slot, vb, taub);
+        else group_right<T, WMAX, false>(cb, g, slot, vb, taub);
     } else {
-        if (full) group_left<T, WMAX, true>(cb, g, vb, taub);
-        else group_left<T, WMAX, false>(cb, g, vb, taub);
+        if (full) group_left<T, WMAX, true>(cb, g, slot, vb, taub);
+        else group_left<T, WMAX, false>(cb, g, slot, vb, taub);
     }
 }
 
@@ -341,7 +388,7 @@ constexpr int kMaxStages = 8;
 // Shared memory of the group kernel: per-sweep reflectors and scalars, then
 // (16-byte aligned) the circular column buffer.
 __host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem) {
-    const size_t head = elem * ((size_t)g * wmax + (size_t)((g + 1) & ~1));
+    const size_t head = elem * ((size_t)g * group_v_stride(wmax, (int)elem) + (size_t)((g + 1) & ~1));
     return (head + 15) & ~(size_t)15;
 }
 
@@ -381,8 +428,9 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     __shared__ int s_written;     // storer: columns < s_written are written back and complete
     __shared__ volatile int s_abort_tick;  // first tick the CTA does not run
     __shared__ volatile int s_dead;  // a warp gave up waiting on a signal that never came
-    T* vbuf = reinterpret_cast<T*>(smem_raw);  // [g][WMAX]
-    T* taubuf = vbuf + (size_t)GA.g * WMAX;    // [g]
+    constexpr int VS = group_v_stride(WMAX, (int)sizeof(T));
+    T* vbuf = reinterpret_cast<T*>(smem_raw);  // [g][VS], 16-byte aligned rows
+    T* taubuf = vbuf + (size_t)GA.g * VS;      // [g]
     ColBuf<T> cb;
     cb.cols = reinterpret_cast<T*>(smem_raw + group_cols_offset(GA.g, WMAX, sizeof(T)));
     cb.nslot = GA.nslot;
@@ -422,6 +470,10 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
         if (warp < GA.g) {
             // ---- compute warps ----
             const int my_h_end = (warp < ng) ? 2 * s_nsteps[warp] : 0;
+            // slot of column c of this warp's current step: one modulo per
+            // group, then + b per step (one wrap when nslot > b, as the
+            // footprint of a whole step gives; the loop keeps it exact anyway)
+            int my_slot = -1;
             int stage = (int)(T0 % (unsigned)S);
             unsigned phase = (T0 / (unsigned)S) & 1u;
             for (int tau = 0; tau < tend; ++tau) {
@@ -434,7 +486,13 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 if (s_abort_tick <= tau) break;  // same tick for every compute warp
                 const int h = tau - L * warp;
                 if (!s_dead && h >= 0 && h < my_h_end) {
-                    group_half<T, WMAX>(P, cb, r0 + warp, h, vbuf + (size_t)warp * WMAX, taubuf + warp);
+                    if (my_slot < 0) {
+                        my_slot = cb.slot(r0 + warp + P.bp + (h >> 1) * P.b);
+                    } else if ((h & 1) == 0) {
+                        my_slot += P.b;
+                        while (my_slot >= cb.nslot) my_slot -= cb.nslot;
+                    }
+                    group_half<T, WMAX>(P, cb, r0 + warp, h, my_slot, vbuf + (size_t)warp * VS, taubuf + warp);
                     // the storer's bulk copies read these columns through the async proxy
                     if (GA.bulk_store) fence_proxy_async_smem();
                 }
