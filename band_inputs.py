@@ -107,6 +107,21 @@ def make_workload(w: Workload, ldab: int | None = None, n: int | None = None) ->
                      w.seed, ldab)
 
 
+def perturb_ulp(band: np.ndarray, seed: int) -> np.ndarray:
+    """A copy of band with every entry multiplied by 1 + eps * N(0, 1) (eps of
+    the band's dtype; rng = numpy.random.default_rng(seed), draws in band
+    order), rounded back to that dtype: a relative perturbation of about one
+    ulp, which the tests use to measure how much the reduction's output moves
+    under rounding-sized changes of its input."""
+    rng = np.random.default_rng(seed)
+    eps = np.finfo(band.dtype).eps
+    return (band * (1 + eps * rng.standard_normal(band.shape))).astype(band.dtype)
+
+
+# Seeds of the one-ulp perturbations behind the measured sensitivity.
+SENSITIVITY_SEEDS = (101, 202, 303)
+
+
 def band_to_dense(band: np.ndarray, n: int, ku: int) -> np.ndarray:
     """Dense n x n matrix of every entry the band storage can hold."""
     ldab = band.shape[1]

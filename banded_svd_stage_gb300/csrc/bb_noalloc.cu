@@ -110,10 +110,18 @@ bb_status run_all(T* band, int64_t n, int64_t bw, int64_t ldab, int64_t tw, T* d
         b -= t;
     }
     if (err == cudaSuccess) err = bb::run_extract<T>(band, n, ldab, ku, d, e, s);
-    if (err != cudaSuccess) return fail(BB_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(err));
+    if (err != cudaSuccess) {
+        // Work of earlier passes may still run on the shared scratch: drain the
+        // stream before the caller's lock is released, so that the next call
+        // does not clear the counters and the status word under it.
+        (void)cudaStreamSynchronize(s);
+        (void)cudaGetLastError();
+        return fail(BB_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(err));
+    }
     int st = 0;
     err = cudaMemcpyAsync(&st, status, sizeof(int), cudaMemcpyDeviceToHost, s);
-    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    const cudaError_t sync_err = cudaStreamSynchronize(s);  // always drained before the lock is released
+    if (err == cudaSuccess) err = sync_err;
     if (err != cudaSuccess) return fail(BB_ERR_CUDA, std::string("completion: ") + cudaGetErrorString(err));
     if (st != 0) return fail((bb_status)st, "device-side progress wait timed out");
     return BB_OK;

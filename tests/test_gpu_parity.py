@@ -4,10 +4,21 @@ Acceptance (the oracle runs in the same precision as the GPU path):
   * singular values of the bidiagonal: max |sigma - sigma_ref| / ||A||_F at
     most 1e-12 (float64) or 2e-5 (float32);
   * |d| and |e|: max | |d|-|d_ref| |, | |e|-|e_ref| | / ||A||_F at most
-    max(that tolerance, 32 x the oracle's own change under a one-ulp input
+    max(that tolerance, 4 x the oracle's own change under a one-ulp input
     perturbation) -- see gpu_helpers.DE_FACTOR for why the entries need the
-    measured conditioning while the singular values do not.
+    measured conditioning while the singular values do not;
+  * float32 workloads: the GPU's |d|, |e| distance from the float64 oracle
+    on the same input is at most 2 x the float32 oracle's own (plus the
+    tolerance), so no error hides under the conditioning allowance.
+
+All five workloads are compared at full size: the three smaller ones with the
+oracle run here, the n = 16384 and n = 32768 ones with the oracle's results
+stored by tests/golden/make_full_size.py (minutes of CPU work each).
 """
+import functools
+import hashlib
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -15,7 +26,7 @@ import torch
 import band_inputs as bi
 import banded_svd_stage_gb300 as bb
 import oracle
-from gpu_helpers import (DE_FACTOR, TOL, de_error, fourth_moment_band, fourth_moment_bidiagonal,
+from gpu_helpers import (DE_FACTOR, FWD_FACTOR, TOL, de_error, fourth_moment_band, fourth_moment_bidiagonal,
                          fro_of_band, gpu_reduce, off_bidiagonal_nonzeros, oracle_sensitivity, record,
                          sigma_bidiagonal)
 
@@ -30,27 +41,66 @@ EDGE_CASES = [
 ]
 
 
-def check_against_oracle(band, n, bw, tw, dt, scheduler, params=None):
+def check_against_oracle(band, n, bw, tw, dt, scheduler, params=None, ref64=None):
     d_ref, e_ref = oracle.bidiagonal(band, n, bw, tw)
     d, e = gpu_reduce(band, n, bw, tw, dt, scheduler, params)
-    return assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler)
+    return assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler, ref64=ref64)
 
 
-def assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler=0):
+def assert_parity(d, e, d_ref, e_ref, band, n, bw, tw, dt, scheduler=0, sens=None, ref64=None):
+    """sens: the oracle's sensitivity when already known (else measured here
+    if needed); ref64: (d, e) of the float64 oracle on the same input, for the
+    float32 forward-error check."""
     fro = max(fro_of_band(band), 1e-300)
     s = sigma_bidiagonal(d, e)
     s_ref = sigma_bidiagonal(d_ref, e_ref)
     serr = float(np.abs(s - s_ref).max()) / fro if n else 0.0
     err = de_error(d, e, d_ref, e_ref, fro)
-    tol_de, sens = TOL[dt], None
+    tol_de = TOL[dt]
     if err > tol_de:
-        sens = oracle_sensitivity(band, n, bw, tw)
+        if sens is None:
+            sens = oracle_sensitivity(band, n, bw, tw)
         tol_de = max(TOL[dt], DE_FACTOR * sens)
+    fwd = fwd_ref = None
+    if ref64 is not None:
+        fwd = de_error(d, e, ref64[0], ref64[1], fro)
+        fwd_ref = de_error(d_ref, e_ref, ref64[0], ref64[1], fro)
     record("parity", n=n, bw=bw, tw=tw, dt=dt, scheduler=scheduler, sigma_err=serr, de_err=err,
-           de_sens=sens, de_tol=tol_de)
+           de_sens=sens, de_tol=tol_de, fwd_err=fwd, fwd_oracle=fwd_ref)
     assert serr <= TOL[dt], f"sigma error {serr:.3e} > {TOL[dt]}"
     assert err <= tol_de, f"|d|,|e| error {err:.3e} > {tol_de:.3e} (oracle sensitivity {sens})"
+    if ref64 is not None:
+        assert fwd <= FWD_FACTOR * fwd_ref + TOL[dt], \
+            f"forward error {fwd:.3e} against the float64 oracle; the float32 oracle's is {fwd_ref:.3e}"
     return err
+
+
+def oracle_f64(band, n, bw, tw):
+    """(d, e) of the float64 oracle on the float32 band widened exactly (the
+    oracle's multi-thread driver, bitwise equal to its serial order)."""
+    try:
+        threads = max(1, min(16, len(os.sched_getaffinity(0))))
+    except AttributeError:
+        threads = 1
+    return oracle.bidiagonal_pipelined(band.astype(np.float64), n, bw, tw, threads)
+
+
+@functools.lru_cache(maxsize=None)
+def workload_f64_reference(idx):
+    w = bi.WORKLOADS[idx]
+    return oracle_f64(bi.make_workload(w), w.n, w.bw, w.tw)
+
+
+def stored_oracle(idx):
+    """The workload's band and the oracle results stored for it."""
+    w = bi.WORKLOADS[idx]
+    band = bi.make_workload(w)
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", f"full_{w.name}.npz")
+    with np.load(path) as z:
+        stored = {k: z[k] for k in z.files}
+    digest = hashlib.sha256(np.ascontiguousarray(band).tobytes()).hexdigest()
+    assert str(stored["band_sha256"]) == digest, "the stored oracle results are of another input"
+    return w, band, stored
 
 
 SCHEDULERS = [bb.SCHED_AUTO, bb.SCHED_CYCLE, bb.SCHED_FLAGS, bb.SCHED_GROUP, bb.SCHED_CYCLE_GRAPH]
@@ -73,13 +123,35 @@ def test_workload_n256_full(scheduler):
 @pytest.mark.parametrize("scheduler", SCHEDULERS)
 def test_workload_n4096_full(scheduler):
     w = bi.WORKLOADS[1]
-    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler)
+    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler,
+                         ref64=workload_f64_reference(1))
 
 
 @pytest.mark.parametrize("scheduler", [bb.SCHED_AUTO, bb.SCHED_FLAGS])
 def test_workload_n8192_full(scheduler):
     w = bi.WORKLOADS[2]
-    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler)
+    check_against_oracle(bi.make_workload(w), w.n, w.bw, w.tw, w.dtype, scheduler,
+                         ref64=workload_f64_reference(2))
+
+
+@pytest.mark.parametrize("scheduler", [bb.SCHED_AUTO, bb.SCHED_FLAGS])
+def test_workload_n16384_full(scheduler):
+    """The graded float64 workload at full size against the stored oracle
+    result (near-zero reflectors: entries down to 1e-8 of the first column)."""
+    w, band, z = stored_oracle(3)
+    d, e = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, scheduler)
+    assert_parity(d, e, z["d"], z["e"], band, w.n, w.bw, w.tw, w.dtype, scheduler, sens=float(z["sens"]))
+
+
+@pytest.mark.parametrize("scheduler", [bb.SCHED_AUTO, bb.SCHED_FLAGS])
+def test_workload_n32768_full(scheduler):
+    """The float32 workload with eight passes at full size against the stored
+    float32 oracle result, and its forward error against the stored float64
+    oracle result on the same input."""
+    w, band, z = stored_oracle(4)
+    d, e = gpu_reduce(band, w.n, w.bw, w.tw, w.dtype, scheduler)
+    assert_parity(d, e, z["d"], z["e"], band, w.n, w.bw, w.tw, w.dtype, scheduler, sens=float(z["sens"]),
+                  ref64=(z["d64"], z["e64"]))
 
 
 @pytest.mark.parametrize("g", [1, 2, 3, 5, 8])
@@ -96,7 +168,9 @@ def test_wide_workloads_at_oracle_size(idx, n):
     # the n16384 and n32768 recipes (same bw, tw, dtype, distribution) at a
     # size the oracle finishes in seconds; 2111 leaves a ragged last block
     w = bi.WORKLOADS[idx]
-    check_against_oracle(bi.make_workload(w, n=n), n, w.bw, w.tw, w.dtype, 0)
+    band = bi.make_workload(w, n=n)
+    ref64 = oracle_f64(band, n, w.bw, w.tw) if w.dtype == "f32" else None
+    check_against_oracle(band, n, w.bw, w.tw, w.dtype, 0, ref64=ref64)
 
 
 @pytest.mark.parametrize("idx", [2, 3])
