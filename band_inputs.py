@@ -20,7 +20,8 @@ Draw order (identical for every workload): Z = rng.<dist>(size=(n, bw+1)) in
 float64 with rng = numpy.random.default_rng(seed); entry A(i, j), 0 <= j-i <=
 bw, i >= 0, is Z[j, bw - (j - i)], i.e. band[j, tw + q] = Z[j, q]; draws that
 would fall above row 0 are discarded.  A graded workload multiplies column j by
-10 ** (-8 j / n).  float32 workloads round the float64 draws.
+10 ** (-8 j / n) (correctly rounded).  float32 workloads round the float64
+draws.
 """
 from __future__ import annotations
 
@@ -90,7 +91,7 @@ def make_band(n: int, bw: int, tw: int, dtype="f64", dist="normal", graded=False
     else:
         raise ValueError(dist)
     if graded:
-        z = z * (10.0 ** (-8.0 * np.arange(n, dtype=np.float64) / n))[:, None]
+        z = z * graded_scale(n)[:, None]
     npd = np.float32 if dtype == "f32" else np.float64
     band = np.zeros((n, ldab), dtype=npd)
     # column j holds rows i = j - bw + q, q = 0..bw; drop i < 0
@@ -99,6 +100,17 @@ def make_band(n: int, bw: int, tw: int, dtype="f64", dist="normal", graded=False
     keep = (j - bw + q[None, :]) >= 0
     band[:, tw:tw + bw + 1] = np.where(keep, z, 0.0).astype(npd)
     return band
+
+
+def graded_scale(n: int) -> np.ndarray:
+    """10 ** (-8 j / n), j = 0 .. n-1, each correctly rounded to float64
+    (decimal arithmetic), so that the graded workload's input is the same on
+    every machine (vectorised power routines differ in the last bit)."""
+    import decimal
+    ctx = decimal.Context(prec=40)
+    ten, den = decimal.Decimal(10), decimal.Decimal(n)
+    return np.array([float(ctx.power(ten, ctx.divide(decimal.Decimal(-8 * j), den))) for j in range(n)],
+                    dtype=np.float64)
 
 
 def make_workload(w: Workload, ldab: int | None = None, n: int | None = None) -> np.ndarray:
