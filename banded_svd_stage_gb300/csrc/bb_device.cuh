@@ -88,6 +88,41 @@ __device__ __forceinline__ double dev_hypot(double a, double b) { return hypot(a
 __device__ __forceinline__ float dev_sqrt(float a) { return sqrtf(a); }
 __device__ __forceinline__ double dev_sqrt(double a) { return sqrt(a); }
 
+// Explicit shared-memory accesses by shared-window address.  A pointer into
+// dynamic shared memory that travels through a struct or a function argument
+// may compile to generic loads and stores; these always compile to
+// ld/st.shared and use 32-bit addresses.  They are volatile so that they keep
+// their program order with respect to each other and to the barriers around
+// them.
+__device__ __forceinline__ unsigned sh_addr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+template <typename T>
+__device__ __forceinline__ T sh_ld(unsigned a);
+template <>
+__device__ __forceinline__ float sh_ld<float>(unsigned a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+template <>
+__device__ __forceinline__ double sh_ld<double>(unsigned a) {
+    double v;
+    asm volatile("ld.shared.f64 %0, [%1];" : "=d"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sh_st(unsigned a, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ void sh_st(unsigned a, double v) {
+    asm volatile("st.shared.f64 [%0], %1;" ::"r"(a), "d"(v) : "memory");
+}
+// 16 bytes from a 16-byte aligned shared address
+__device__ __forceinline__ void sh_ld16(unsigned a, float (&v)[4]) {
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(a));
+}
+__device__ __forceinline__ void sh_ld16(unsigned a, double (&v)[2]) {
+    asm volatile("ld.shared.v2.f64 {%0, %1}, [%2];" : "=d"(v[0]), "=d"(v[1]) : "r"(a));
+}
+
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll

@@ -52,15 +52,19 @@ __device__ __forceinline__ long long half_min_col(const PassArgs& P, int r, int 
     return (long long)r + P.bp + (long long)(h >> 1) * P.b;
 }
 
-// Accessor of the buffered band: A(i, j) lives at
-// cols[slot(j) * lds + (i - j + off)], slot(j) = j mod nslot, off = ku - top:
-// buffered column j is band rows top .. top + lds - 1 of column j.
+// Accessor of the buffered band: A(i, j) lives at element
+// slot(j) * lds + (i - j + off) of the buffer, slot(j) = j mod nslot,
+// off = ku - top: buffered column j is band rows top .. top + lds - 1 of
+// column j.  The compute warps address it by shared-window byte address
+// (base); the loader and the storer use the generic pointer (cols).
 template <typename T>
 struct ColBuf {
     T* cols;
+    unsigned base;  // shared-window address of cols
     int nslot, lds, off;
     __device__ __forceinline__ int slot(int j) const { return j % nslot; }
     __device__ __forceinline__ T* col(int j) const { return cols + slot(j) * lds; }
+    __device__ __forceinline__ unsigned at(int idx) const { return base + (unsigned)idx * (unsigned)sizeof(T); }
 };
 
 // Geometry of step k of sweep r in 32-bit arithmetic (the group kernel runs
@@ -95,18 +99,25 @@ struct Vec16<double> {
     using type = double2;
 };
 template <typename T, int WMAX>
-__device__ __forceinline__ void load_v(const T* __restrict__ v, T (&vr)[WMAX]) {
+__device__ __forceinline__ void load_v(unsigned v, T (&vr)[WMAX]) {
     constexpr int PER = 16 / (int)sizeof(T);
     constexpr int NV = (WMAX + PER - 1) / PER;
-    using V = typename Vec16<T>::type;
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
-        const V c = reinterpret_cast<const V*>(v)[q];
-        const T* e = reinterpret_cast<const T*>(&c);
+        T e[PER];
+        sh_ld16(v + 16u * q, e);
 #pragma unroll
         for (int u = 0; u < PER; ++u)
             if (q * PER + u < WMAX) vr[q * PER + u] = e[u];
     }
+}
+
+// Whether the applies hold v in registers: reflectors of up to 64 bytes, and
+// 33 floats (those kernels run 8 warps with up to 255 registers); the others
+// read it from shared memory.
+template <typename T, int WMAX>
+__host__ __device__ constexpr bool group_v_in_registers() {
+    return WMAX * sizeof(T) <= 64 || (sizeof(T) == 4 && WMAX > 17 && WMAX <= 33);
 }
 
 // Right half-step (rows p..ce of columns c..ce) on the buffered band, by one
@@ -116,56 +127,61 @@ __device__ __forceinline__ void load_v(const T* __restrict__ v, T (&vr)[WMAX]) {
 template <typename T, int WMAX, bool FULL>
 __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
+    constexpr unsigned S = sizeof(T);
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    // A(p + i, c + m) = cb.cols[a0 + i + m (lds - 1) - (m >= mwrap ? nslot lds : 0)]:
+    // A(p + i, c + m) is element a0 + i + m (lds - 1) - (m >= mwrap ? nslot lds : 0):
     // column c + m sits in slot s0 + m, wrapped once past the end
     const int a0 = s0 * cb.lds + cb.off + (g.p - g.c);
     const int dm = cb.lds - 1;
     const int mwrap = cb.nslot - s0;
     const int wrap = cb.nslot * cb.lds;
     T xp[NPL];
-    int xo[NPL];
+    unsigned xa[NPL];
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        xo[q] = a0 + m * dm - ((m >= mwrap) ? wrap : 0);
-        xp[q] = (m < W) ? cb.cols[xo[q]] : T(0);
+        xa[q] = cb.at(a0 + m * dm - ((m >= mwrap) ? wrap : 0));
+        xp[q] = (m < W) ? sh_ld<T>(xa[q]) : T(0);
     }
     T beta = warp_larfg<T, NPL>(xp, W, lane, vb, taub);
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        if (m < W) cb.cols[xo[q]] = (m == 0) ? beta : T(0);
+        if (m < W) sh_st(xa[q], (m == 0) ? beta : T(0));
     }
     __syncwarp();
-    const T tau = *taub;
+    const T tau = sh_ld<T>(sh_addr(taub));
     if (tau == T(0)) return;
-    // narrow reflectors: v in registers (16-byte loads, once per half-step);
-    // wide ones keep reading the shared buffer, which spares the registers
-    constexpr bool kVReg = WMAX * sizeof(T) <= 16 * 4;
+    // v in registers (16-byte loads, once per half-step) where the registers
+    // allow; otherwise read from shared memory at each use
+    constexpr bool kVReg = group_v_in_registers<T, WMAX>();
+    const unsigned vaddr = sh_addr(vb);
     T vreg[kVReg ? WMAX : 1];
-    if constexpr (kVReg) load_v<T, WMAX>(vb, vreg);
-    const T* vsh = vb;
+    if constexpr (kVReg) load_v<T, WMAX>(vaddr, vreg);
     auto v = [&](int m) -> T {
         if constexpr (kVReg) return vreg[m];
-        else return vsh[m];
+        else return sh_ld<T>(vaddr + S * (unsigned)m);
     };
+    // byte offset of column c + m from column c, wrap included
+    unsigned om[WMAX];
+#pragma unroll
+    for (int m = 0; m < WMAX; ++m) om[m] = S * (unsigned)(m * dm - ((m >= mwrap) ? wrap : 0));
     const int nrows = g.ce - g.p;
     for (int i = 1 + lane; i <= nrows; i += 32) {
-        const int a = a0 + i;
+        const unsigned ra = cb.at(a0 + i);
         T x[WMAX];
         T y = 0;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
-                x[m] = cb.cols[a + m * dm - ((m >= mwrap) ? wrap : 0)];
+                x[m] = sh_ld<T>(ra + om[m]);
                 y = fma(x[m], v(m), y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) cb.cols[a + m * dm - ((m >= mwrap) ? wrap : 0)] = fma(-s, v(m), x[m]);
+            if (m < W) sh_st(ra + om[m], fma(-s, v(m), x[m]));
     }
 }
 
@@ -175,48 +191,49 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
 template <typename T, int WMAX, bool FULL>
 __device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
+    constexpr unsigned S = sizeof(T);
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    T* colc = cb.cols + s0 * cb.lds + cb.off;  // colc[m] = A(c + m, c)
+    const unsigned colc = cb.at(s0 * cb.lds + cb.off);  // colc + S m = A(c + m, c)
     T xc[NPL];
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        xc[q] = (m < W) ? colc[m] : T(0);
+        xc[q] = (m < W) ? sh_ld<T>(colc + S * (unsigned)m) : T(0);
     }
     T beta = warp_larfg<T, NPL>(xc, W, lane, vb, taub);
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        if (m < W) colc[m] = (m == 0) ? beta : T(0);
+        if (m < W) sh_st(colc + S * (unsigned)m, (m == 0) ? beta : T(0));
     }
     __syncwarp();
-    const T tau = *taub;
+    const T tau = sh_ld<T>(sh_addr(taub));
     if (tau == T(0)) return;
-    constexpr bool kVReg = WMAX * sizeof(T) <= 16 * 4;
+    constexpr bool kVReg = group_v_in_registers<T, WMAX>();
+    const unsigned vaddr = sh_addr(vb);
     T vreg[kVReg ? WMAX : 1];
-    if constexpr (kVReg) load_v<T, WMAX>(vb, vreg);
-    const T* vsh = vb;
+    if constexpr (kVReg) load_v<T, WMAX>(vaddr, vreg);
     auto v = [&](int m) -> T {
         if constexpr (kVReg) return vreg[m];
-        else return vsh[m];
+        else return sh_ld<T>(vaddr + S * (unsigned)m);
     };
     for (int dj = 1 + lane; dj <= g.cend - g.c; dj += 32) {
         int sl = s0 + dj;
         if (sl >= cb.nslot) sl -= cb.nslot;
-        T* cj = cb.cols + sl * cb.lds + cb.off - dj;  // cj[m] = A(c + m, c + dj)
+        const unsigned cj = cb.at(sl * cb.lds + cb.off - dj);  // cj + S m = A(c + m, c + dj)
         T x[WMAX];
         T y = 0;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
-                x[m] = cj[m];
+                x[m] = sh_ld<T>(cj + S * (unsigned)m);
                 y = fma(v(m), x[m], y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) cj[m] = fma(-s, v(m), x[m]);
+            if (m < W) sh_st(cj + S * (unsigned)m, fma(-s, v(m), x[m]));
     }
 }
 
@@ -383,7 +400,7 @@ __device__ __forceinline__ long long tick_min_col(const PassArgs& P, int r0, int
     return a;
 }
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 10;
 
 // Shared memory of the group kernel: per-sweep reflectors and scalars, then
 // (16-byte aligned) the circular column buffer.
@@ -422,7 +439,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_flag;
     __shared__ int s_nsteps[32];  // steps of each sweep of the group
-    __shared__ __align__(8) unsigned long long s_full[kMaxStages], s_done[kMaxStages];
+    __shared__ __align__(8) unsigned long long s_full[kMaxStages], s_done[kMaxStages], s_stored[kMaxStages];
     __shared__ int s_freed;       // storer: columns < s_freed are written back
     __shared__ int s_retired;     // storer: last tick whose columns it retired
     __shared__ int s_written;     // storer: columns < s_written are written back and complete
@@ -433,6 +450,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     T* taubuf = vbuf + (size_t)GA.g * VS;      // [g]
     ColBuf<T> cb;
     cb.cols = reinterpret_cast<T*>(smem_raw + group_cols_offset(GA.g, WMAX, sizeof(T)));
+    cb.base = sh_addr(cb.cols);
     cb.nslot = GA.nslot;
     cb.lds = GA.lds;
     cb.off = P.ku - GA.top;
@@ -447,6 +465,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
         for (int s = 0; s < S; ++s) {
             mbar_init(&s_full[s], 1);
             mbar_init(&s_done[s], 1);
+            mbar_init(&s_stored[s], 1);
         }
         s_abort_tick = 0x7fffffff;
         s_dead = 0;
@@ -512,19 +531,28 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
             int stage = (int)(T0 % (unsigned)S);
             for (int u = 0; u < tend; ++u) {
                 bool ok = true;
-                // stay within `ahead` ticks of the storer (mbarrier phases)
-                if (u - GA.ahead - 1 >= 0) {
-                    const long long t0 = clock64();
-                    while (ld_acquire_cta_shared(&s_retired) < u - GA.ahead - 1) {
-                        if ((unsigned long long)(clock64() - t0) > inner_budget || s_dead) { ok = false; break; }
+                // Storer progress: tick X is retired once s_retired >= X.  The
+                // loader sleeps on the storer's per-tick mbarrier rather than
+                // polling shared memory.  The storer is never past tick u - 1
+                // here (compute has not run tick u), so the phase of tick X < u
+                // cannot have been overtaken.
+                auto storer_done = [&](int X) -> bool {
+                    while (ld_acquire_cta_shared(&s_retired) < X) {
+                        const unsigned q = T0 + (unsigned)X;
+                        if (!mbar_wait(&s_stored[q % S], (q / S) & 1u, inner_budget, &s_abort_tick, u, &s_dead))
+                            return false;
                     }
-                }
+                    return true;
+                };
+                // stay within `ahead` ticks of the storer (mbarrier phases)
+                if (u - GA.ahead - 1 >= 0) ok = storer_done(u - GA.ahead - 1);
                 const long long xn = ok ? tick_max_col(P, r0, ng, L, s_nsteps, u) : -1;
                 if (ok && xn > B) {
-                    // slots of the columns xn - nslot + 1 .. xn must be free
-                    const long long t0 = clock64();
-                    while ((long long)ld_acquire_cta_shared(&s_freed) < xn - GA.nslot + 1) {
-                        if ((unsigned long long)(clock64() - t0) > inner_budget || s_dead) { ok = false; break; }
+                    // slots of the columns xn - nslot + 1 .. xn must be free: wait
+                    // for the storer's next ticks (at most up to tick u - 1)
+                    while (ok && (long long)ld_acquire_cta_shared(&s_freed) < xn - GA.nslot + 1) {
+                        const int X = ld_acquire_cta_shared(&s_retired) + 1;
+                        ok = (X <= u - 1) && storer_done(X);
                     }
                     if (ok && G > 0) ok = warp_wait(wm + G - 1, (int)(xn + 1), status, P, seen);
                 }
@@ -624,6 +652,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                     st_release_cta_shared(&s_freed, (int)A);
                     st_release_cta_shared(&s_retired, v);
                     st_release_cta_shared(&s_written, a_prev);
+                    mbar_arrive(&s_stored[(T0 + (unsigned)v) % (unsigned)S]);  // release: orders the stores above
                 }
                 a_prev = (int)A;
             }

@@ -94,6 +94,16 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
     }
     if (best.g == 0) return false;
     if (requested > 0 && best.g != requested) return false;
+    // With g fixed, let the loader run further ahead (a larger buffer) while
+    // shared memory allows: the loader then issues its copies earlier and
+    // waits less for the storer to free slots.
+    for (int a = best.ahead + 1; a <= kMaxStages - 2; ++a) {
+        GroupArgs ga = best;
+        ga.ahead = a;
+        ga.nslot = std::max(1, group_footprint(P, ga.g, a));
+        if (group_smem_bytes(ga, wmax, elem) > budget) break;
+        best = ga;
+    }
     *out = best;
     return true;
 }
