@@ -108,9 +108,14 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
     return true;
 }
 
+// Threads per block of the flag and per-cycle kernels (capped by the
+// kernel's register budget when launched).  Measured on the n = 16384 and
+// n = 32768 workloads' passes: from b = 96 the most threads the kernel allows
+// is fastest; below, one thread per row of the (b + t + 1)-row block with at
+// least four warps.
 int auto_tpb(int b, int t) {
-    int rows = b + t;
-    int tpb = ((rows + 31) / 32) * 32;
-    return std::min(1024, std::max(64, tpb));
+    if (b >= 96) return 1024;
+    const int tpb = ((b + t + 31) / 32) * 32;
+    return std::min(1024, std::max(128, tpb));
 }
 }  // namespace bb

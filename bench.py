@@ -22,16 +22,19 @@ is all ranks' bytes over the slowest rank's time.
 tests check the GPU against) on the host, on the same workload and metric.
 
 Besides the contract's keys the line carries: roofline (the dominant pass
-kernel against the measured HBM copy rate, with its ncu DRAM traffic),
-cpu_baseline (the serial oracle on one host core), cpu_pipelined (the
-oracle's multi-thread pipelined chase, context only), e2e (host buffers in,
-d and e out, copies timed), latency_chain (per pass: sweeps, half-step lag
-and the measured time per dependent link, the quantity that bounds these
-latency chains), median_ms / min_ms (of this rank's timed steps),
-per_scheduler (the main workload under each scheduler: per-cycle launches,
-their CUDA-graph replay, the flag and the group kernel), per_workload (the
-other workloads) and singular_values (bb_singular_values on the reduction's
-output).
+kernel against the measured HBM copy rate, and against the nominal ~8 TB/s,
+on which the 40% target is judged; with its ncu DRAM traffic), cpu_baseline
+(the serial oracle on one host core), cpu_pipelined (the oracle's
+multi-thread pipelined chase, context only), e2e (host buffers in, d and e
+out, copies timed), latency_chain (per pass: sweeps, half-step lag and the
+measured time per dependent link, the quantity that bounds these latency
+chains), median_ms / min_ms (of this rank's timed steps), per_scheduler (the
+main workload under each scheduler: per-cycle launches, their CUDA-graph
+replay, the flag and the group kernel), per_workload (each other workload,
+5 timed steps after 2 warm-up steps: its own roofline, e2e and CPU baseline
+-- the serial oracle where a reduction takes seconds, else the oracle's
+multi-thread driver on the first pass), singular_values (bb_singular_values
+on the reduction's output) and symmetric (the symmetric band variant).
 """
 from __future__ import annotations
 
@@ -55,6 +58,10 @@ METRIC = "band→bidiagonal ms/reduction and effective GB/s (% of HBM peak), N=4
 MAIN_WORKLOAD = bi.WORKLOADS[1].name
 SWEEP_WORKLOADS = [w.name for w in bi.WORKLOADS[1:]]
 HBM_FALLBACK_GBS = 6800.0
+# GB300 HBM3e nominal bandwidth (about 8 TB/s).  The 40% target is judged
+# against this figure, the stricter of the two; fractions of the measured
+# copy rate (MEASURED_PEAKS.json) are reported beside it.
+NOMINAL_HBM_GBS = 7900.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -330,7 +337,17 @@ def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
 
 
 def cpu_model() -> str:
-    """The host CPU's model name (Linux), for the CPU timings' context."""
+    """The host CPU's model name (Linux: lscpu's "Model name", else
+    /proc/cpuinfo), for the CPU timings' context."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(line.split(":", 1) for line in out.splitlines() if ":" in line)
+        name = fields.get("Model name", "").strip()
+        vendor = fields.get("Vendor ID", "").strip()
+        if name and name != "-":
+            return f"{vendor} {name}".strip() if vendor and vendor not in name else name
+    except Exception:
+        pass
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
@@ -398,7 +415,51 @@ def cpu_pipelined_rate(w: bi.Workload, budget_s: float = 6.0):
             "sample": f"{reps} whole reductions of {w.name} on {P} threads ({el:.1f} s)"}
 
 
+def cpu_baseline_for(w: bi.Workload, budget_s: float = 12.0, serial_limit_bytes: float = 60e9):
+    """CPU baseline of workload w, on the host cores, as the oracle stands:
+    the serial oracle on one core (whole reductions, repeated for about
+    budget_s) where one reduction takes seconds, otherwise a bounded sample:
+    the oracle's multi-thread driver on the first pass only (its bytes over
+    its time; the thread count follows that driver's limits).  Workloads of
+    more than serial_limit_bytes algorithmic bytes take the second form."""
+    import oracle
+    elem = 4 if w.dtype == "f32" else 8
+    total = model_bytes_np(w.n, w.bw, w.tw, elem)
+    if total <= serial_limit_bytes:
+        out = cpu_oracle_rate(w, budget_s)
+        out["model_bytes"] = total
+        return out
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    P = max(1, min(cores, 2 * w.n // (3 * max(w.bw, 1)), w.n // 256))
+    band = bi.make_workload(w)
+    pass_bytes = model_bytes_np(w.n, w.bw, w.tw, elem, 0)
+    t0 = time.perf_counter()
+    oracle.reduce_band_pipelined(band, w.n, w.bw, w.tw, P, time_limit=300.0, pass_lo=0, pass_hi=1)
+    sec = time.perf_counter() - t0
+    t = min(w.tw, w.bw - 1)
+    return {"value": pass_bytes / sec / 1e9, "unit": "GB/s", "cores": P, "kind": "oracle, pipelined sweeps",
+            "cpu": cpu_model(), "ms_per_pass": sec * 1e3,
+            "sample": f"first pass ({w.bw}->{w.bw - t}) of {w.name} on {P} threads ({sec:.1f} s, "
+                      f"{pass_bytes / 1e9:.1f} GB of the reduction's {total / 1e9:.1f} GB)"}
+
+
+def roofline_of(res, hbm: float, peak_src: str, workload: str):
+    """Roofline entry of the dominant pass kernel of one run (run_ours)."""
+    kname, achieved, nl, kbytes, kms = dominant_kernel(res)
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": (achieved / hbm) if achieved else None,
+            "frac_of_nominal": (achieved / NOMINAL_HBM_GBS) if achieved else None,
+            "nominal_peak": NOMINAL_HBM_GBS, "traffic": traffic_for(kname, workload),
+            "kernel": kname, "peak_source": peak_src, "launches_per_step": nl,
+            "algorithmic_bytes_per_launch": kbytes / nl if nl else None,
+            "ms_per_launch": kms / nl if nl else None,
+            "achieved_def": "algorithmic bytes of the kernel's passes / their CUDA-event time "
+                            "(events on the launching stream around each pass launch)"}
+
+
 def _model_bytes_py(w):
+    """Algorithmic bytes of workload w, step by step (plain Python; the
+    definition, kept for the tests)."""
     s = 4 if w.dtype == "f32" else 8
     tot, b = 0, w.bw
     while b > 1:
@@ -417,6 +478,36 @@ def _model_bytes_py(w):
                 c += b
         b -= t
     return tot
+
+
+def model_bytes_np(n: int, bw: int, tw: int, elem: int, pass_index: int = -1) -> float:
+    """The same count as _model_bytes_py (and bb_model_bytes), vectorised over
+    the sweeps with numpy, one step index at a time: every step's right block
+    (rows p..ce x cols c..ce) and left block (rows c..ce x cols c..cend) read
+    once and written once.  Needs no GPU library (the reference arm uses it)."""
+    import numpy as np
+    tot, b, pi = 0, bw, 0
+    while b > 1:
+        t = min(tw, b - 1)
+        bp = b - t
+        if pass_index < 0 or pi == pass_index:
+            r = np.arange(max(0, n - bp - 1), dtype=np.int64)
+            k = 0
+            while r.size:
+                c = r + bp + k * b
+                r = r[c + 1 <= n - 1]
+                c = c[c + 1 <= n - 1]
+                if not r.size:
+                    break
+                p = r if k == 0 else c - b
+                ce = np.minimum(c + t, n - 1)
+                cend = np.minimum(ce + b, n - 1)
+                ww = ce - c + 1
+                tot += int((2 * elem * ((ce - p + 1) * ww + ww * (cend - c + 1))).sum())
+                k += 1
+        b -= t
+        pi += 1
+    return float(tot)
 
 
 def latency_chain(n: int, bw: int, tw: int, pass_ms):
@@ -509,10 +600,7 @@ def main():
             oracle.bidiagonal(band, w.n, w.bw, w.tw)
             if i >= args.warmup:
                 times.append(time.perf_counter() - t0)
-        mb = _model_bytes_py(w) if w.n <= 4096 else None
-        if mb is None:
-            import banded_svd_stage_gb300 as bb
-            mb = bb.bb_model_bytes(w.n, w.bw, w.tw, 4 if w.dtype == "f32" else 8)
+        mb = model_bytes_np(w.n, w.bw, w.tw, 4 if w.dtype == "f32" else 8)
         sec = sum(times) / len(times)
         val = mb / sec / 1e9
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
@@ -553,30 +641,28 @@ def main():
     value = bytes_all / (ms_max * 1e-3) / 1e9
     # roofline of the dominant kernel: the pass kernel (one launch a pass for
     # the flag and group kernels) that takes the most time in a step
-    kname, achieved, nl, kbytes, kms = dominant_kernel(res)
-    traffic = traffic_for(kname, w.name)
-    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
-            "kernel": kname, "peak_source": peak_src, "launches_per_step": nl,
-            "algorithmic_bytes_per_launch": kbytes / nl if nl else None,
-            "ms_per_launch": kms / nl if nl else None,
-            "achieved_def": "algorithmic bytes of the kernel's passes / their CUDA-event time "
-                            "(events on the launching stream around each pass launch)"}
+    roof = roofline_of(res, hbm, peak_src, w.name)
 
     sweep = []
     if rank == 0 and world == 1 and not args.no_sweep:
-        for name in SWEEP_WORKLOADS:
-            if name == w.name:
+        for ww in bi.WORKLOADS:
+            if ww.name == w.name:
                 continue
-            ww = bi.by_name(name)
-            r2 = run_ours(ww, max(2, min(args.steps, 3)), 1, args.scheduler, rank, with_e2e=False,
-                          group_size=args.group_size)
+            r2 = run_ours(ww, 5, 2, args.scheduler, rank, with_e2e=not args.no_e2e, group_size=args.group_size)
             m2 = statistics.median(r2["ms"])
             g2 = r2["model_bytes"] / (m2 * 1e-3) / 1e9
-            sweep.append({"workload": name, "ms_per_reduction": m2, "min_ms": min(r2["ms"]),
-                          "effective_gbs": g2, "frac_of_hbm": g2 / hbm,
-                          "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"],
-                          "latency_chain": latency_chain(ww.n, ww.bw, ww.tw, r2["pass_ms_mean"])})
+            entry = {"workload": ww.name, "config": ww.describe(), "dtype": ww.dtype, "steps": 5, "warmup": 2,
+                     "ms_per_reduction": m2, "min_ms": min(r2["ms"]), "effective_gbs": g2,
+                     "frac_of_hbm": g2 / hbm, "frac_of_nominal_hbm": g2 / NOMINAL_HBM_GBS,
+                     "model_bytes": r2["model_bytes"], "roofline": roofline_of(r2, hbm, peak_src, ww.name),
+                     "e2e": r2["e2e"], "pass_ms": r2["pass_ms_mean"], "pass_kernels": r2["kernels"],
+                     "latency_chain": latency_chain(ww.n, ww.bw, ww.tw, r2["pass_ms_mean"])}
+            if not args.no_cpu:
+                try:
+                    entry["cpu_baseline"] = cpu_baseline_for(ww)
+                except Exception as ex:  # a side measurement never loses the line
+                    entry["cpu_baseline"] = {"error": f"{type(ex).__name__}: {ex}"}
+            sweep.append(entry)
 
     # both scheduler families on the main workload, measured in the same run:
     # per-cycle launches (plain and replayed from a CUDA graph) and the
@@ -620,6 +706,7 @@ def main():
                        "l2": "flushed between steps (256 MiB write); band restored before each step",
                        "parallelism": f"replicas x{world}"},
             "frac_of_hbm": value / hbm,
+            "frac_of_nominal_hbm": value / NOMINAL_HBM_GBS,
             "roofline": roof,
             "cpu_baseline": cpu,
             "cpu_pipelined": cpu_pipe,

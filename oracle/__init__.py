@@ -82,6 +82,9 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).argtypes = [i64, i64, i64, p, i64, i64,
                                                                        ctypes.c_double]
         getattr(lib, "oracle_reduce_band_pipelined" + sfx).restype = ci
+        getattr(lib, "oracle_reduce_band_pipelined_range" + sfx).argtypes = [i64, i64, i64, p, i64, i64,
+                                                                             ctypes.c_double, i64, i64]
+        getattr(lib, "oracle_reduce_band_pipelined_range" + sfx).restype = ci
         getattr(lib, "oracle_reduce_band_record" + sfx).argtypes = [i64, i64, i64, p, i64, i64, p, p, p, p, p]
         getattr(lib, "oracle_reduce_band_record" + sfx).restype = i64
         if sfx == "_h":
@@ -166,15 +169,16 @@ def reduce_band(band: np.ndarray, n: int, bw: int, tw: int, pass_lo: int = 0,
 
 
 def reduce_band_pipelined(band: np.ndarray, n: int, bw: int, tw: int, threads: int,
-                          time_limit: float = 600.0) -> np.ndarray:
+                          time_limit: float = 600.0, pass_lo: int = 0, pass_hi: int = 1 << 62) -> np.ndarray:
     """reduce_band on host threads: sweep r on thread r mod threads, each sweep
     spinning on its predecessor's count of finished half-steps (the pipelined
     chase of "A two-stage reduction on an Apple M5 Pro", Section 6, with the
-    half-step separation rule).  Bitwise equal to reduce_band.  Raises
-    TimeoutError after time_limit seconds of waiting."""
+    half-step separation rule).  Bitwise equal to reduce_band (also over a
+    pass range [pass_lo, pass_hi)).  Raises TimeoutError after time_limit
+    seconds of waiting."""
     assert band.flags.c_contiguous and band.shape[0] == n
-    rc = getattr(_load(), "oracle_reduce_band_pipelined" + _sfx(band))(
-        n, bw, tw, _ptr(band), band.shape[1], threads, float(time_limit))
+    rc = getattr(_load(), "oracle_reduce_band_pipelined_range" + _sfx(band))(
+        n, bw, tw, _ptr(band), band.shape[1], threads, float(time_limit), pass_lo, pass_hi)
     if rc == -1:
         raise ValueError("oracle_reduce_band_pipelined: invalid arguments")
     if rc == -2:

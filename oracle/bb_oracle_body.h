@@ -316,7 +316,7 @@ int64_t FN(oracle_reduce_band_record)(int64_t n, int64_t bw, int64_t tw, BAND_T*
  * Returns 0, -2 when the time limit ran out, -3 when the threads or the
  * counters could not be created. */
 static int FN(pipe_run_)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab, int64_t nthreads,
-                         double time_limit_s, void* (*worker)(void*)) {
+                         double time_limit_s, void* (*worker)(void*), int64_t pass_lo, int64_t pass_hi) {
     const int64_t ku = bw + tw;
     _Atomic int64_t* done = (_Atomic int64_t*)malloc((size_t)n * sizeof(_Atomic int64_t));
     pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
@@ -327,8 +327,12 @@ static int FN(pipe_run_)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_
     if (!done || !th || !args) rc = -3;
     const double deadline = oracle_now_() + time_limit_s;
     int64_t b = bw;
-    while (rc == 0 && b > 1) {
+    for (int64_t pass = 0; rc == 0 && b > 1; ++pass) {
         const int64_t t = (tw < b - 1) ? tw : b - 1;
+        if (pass < pass_lo || pass >= pass_hi) {  /* skipped: the bandwidth still follows the plan */
+            b -= t;
+            continue;
+        }
         const int64_t nsweeps = n - (b - t) - 1;
         for (int64_t r = 0; r < n; ++r) atomic_init(&done[r], 0);
         int64_t P = nthreads < nsweeps ? nthreads : nsweeps, started = 0;
@@ -351,22 +355,32 @@ static int FN(pipe_run_)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_
     return rc;
 }
 
-/* Same arguments and result as oracle_reduce_band over all passes, on
+/* Same arguments and result as oracle_reduce_band over passes [pass_lo,
+ * pass_hi) of the plan (the fill rows are zeroed only when pass_lo == 0), on
  * nthreads (1 .. 1024) threads.  Returns 0; -1 on invalid arguments; -2 when
  * time_limit_s ran out (the band is then partly reduced); -3 when the
  * threads or the counters could not be created. */
-int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab,
-                                     int64_t nthreads, double time_limit_s) {
+int FN(oracle_reduce_band_pipelined_range)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab,
+                                           int64_t nthreads, double time_limit_s, int64_t pass_lo,
+                                           int64_t pass_hi) {
     if (n < 1 || bw < 0 || bw >= n || tw < 1 || ldab < bw + 2 * tw + 1) return -1;
     if (tw > (bw > 2 ? bw - 1 : 1)) return -1;
     if (tw + 1 > ORACLE_WMAX) return -1;
     if (nthreads < 1 || nthreads > 1024 || !(time_limit_s > 0)) return -1;
     const int64_t ku = bw + tw;
-    for (int64_t j = 0; j < n; ++j) {
-        for (int64_t q = 0; q < tw; ++q) band[q + j * ldab] = 0;
-        for (int64_t q = ku + 1; q <= ku + tw; ++q) band[q + j * ldab] = 0;
+    if (pass_lo == 0) {
+        for (int64_t j = 0; j < n; ++j) {
+            for (int64_t q = 0; q < tw; ++q) band[q + j * ldab] = 0;
+            for (int64_t q = ku + 1; q <= ku + tw; ++q) band[q + j * ldab] = 0;
+        }
     }
-    return FN(pipe_run_)(n, bw, tw, band, ldab, nthreads, time_limit_s, FN(pipe_worker_));
+    return FN(pipe_run_)(n, bw, tw, band, ldab, nthreads, time_limit_s, FN(pipe_worker_), pass_lo, pass_hi);
+}
+
+/* All passes (oracle_reduce_band_pipelined_range over the whole plan). */
+int FN(oracle_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, BAND_T* band, int64_t ldab,
+                                     int64_t nthreads, double time_limit_s) {
+    return FN(oracle_reduce_band_pipelined_range)(n, bw, tw, band, ldab, nthreads, time_limit_s, 0, INT64_MAX);
 }
 
 /* d_i = A(i, i), e_i = A(i, i+1) from band storage. */

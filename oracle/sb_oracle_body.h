@@ -157,7 +157,7 @@ int FN(oracle_sym_reduce_band_pipelined)(int64_t n, int64_t bw, int64_t tw, REAL
     if (nthreads < 1 || nthreads > 1024 || !(time_limit_s > 0)) return -1;
     for (int64_t j = 0; j < n; ++j)
         for (int64_t q = bw + 1; q <= bw + tw; ++q) band[q + j * ldab] = 0;
-    return FN(pipe_run_)(n, bw, tw, band, ldab, nthreads, time_limit_s, FN(sym_pipe_worker_));
+    return FN(pipe_run_)(n, bw, tw, band, ldab, nthreads, time_limit_s, FN(sym_pipe_worker_), 0, INT64_MAX);
 }
 
 /* d_i = A(i, i), e_i = A(i+1, i) from the lower band storage. */

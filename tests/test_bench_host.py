@@ -105,3 +105,26 @@ def test_latency_chain_of_the_main_workload():
 def test_cpu_model_is_reported():
     m = bench.cpu_model()
     assert isinstance(m, str) and m.strip()
+
+
+def test_model_bytes_without_the_gpu_library():
+    """The reference arm's vectorised count equals the plain step-by-step
+    definition (and, through tests/test_abi.py, the library's)."""
+    import band_inputs as bi
+    for (n, bw, tw, dt) in ((300, 20, 7, "f32"), (257, 8, 7, "f64"), (100, 33, 32, "f32"), (64, 1, 1, "f64"),
+                            (50, 30, 4, "f64")):
+        w = bi.Workload("x", n, bw, tw, dt, "normal", False, 0)
+        elem = 4 if dt == "f32" else 8
+        assert bench.model_bytes_np(n, bw, tw, elem) == bench._model_bytes_py(w)
+        npass = len(__import__("oracle").pass_plan(bw, tw))
+        assert sum(bench.model_bytes_np(n, bw, tw, elem, p) for p in range(npass)) == bench._model_bytes_py(w)
+
+
+def test_cpu_baseline_for_both_kinds():
+    import band_inputs as bi
+    w = bi.Workload("small", 600, 24, 8, "f32", "normal", False, 0)
+    serial = bench.cpu_baseline_for(w, budget_s=0.2)
+    assert serial["kind"] == "oracle" and serial["cores"] == 1 and serial["value"] > 0
+    pipe = bench.cpu_baseline_for(w, budget_s=0.2, serial_limit_bytes=0)
+    assert pipe["kind"].startswith("oracle, pipelined") and pipe["cores"] >= 1 and pipe["value"] > 0
+    assert "first pass (24->16)" in pipe["sample"]

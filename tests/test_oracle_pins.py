@@ -493,6 +493,22 @@ def test_pipelined_threads_larger_bands(n, bw, tw):
         assert np.array_equal(work, serial)
 
 
+@pytest.mark.parametrize("dt", ["f32", "f64"])
+def test_pipelined_pass_range_equals_serial_pass_range(dt):
+    # the multi-threaded chase over a pass range (the CPU baseline times the
+    # first pass of the largest workloads this way) is the serial range
+    n, bw, tw = 700, 64, 16
+    band = bi.make_band(n, bw, tw, dt, "normal", seed=9)
+    serial, work = band.copy(), band.copy()
+    for lo, hi in ((0, 1), (1, 3), (3, 4)):
+        oracle.reduce_band(serial, n, bw, tw, lo, hi)
+        oracle.reduce_band_pipelined(work, n, bw, tw, 5, pass_lo=lo, pass_hi=hi)
+        assert np.array_equal(work, serial), (lo, hi)
+    whole = band.copy()
+    oracle.reduce_band(whole, n, bw, tw)
+    assert np.array_equal(work, whole)
+
+
 def test_pipelined_invalid_arguments():
     band = bi.make_band(20, 4, 2, "f64", seed=1)
     for threads, limit in ((0, 10.0), (2000, 10.0), (2, 0.0), (2, -1.0)):
