@@ -17,7 +17,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbb.so")
 
-BB_F32, BB_F64 = 0, 1
+BB_F32, BB_F64, BB_F16 = 0, 1, 2
 BB_OK, BB_ERR_INVALID_ARG, BB_ERR_LDAB, BB_ERR_DTYPE, BB_ERR_CUDA, BB_ERR_TIMEOUT, BB_ERR_NOMEM = range(7)
 STATUS_NAMES = {0: "BB_OK", 1: "BB_ERR_INVALID_ARG", 2: "BB_ERR_LDAB", 3: "BB_ERR_DTYPE",
                 4: "BB_ERR_CUDA", 5: "BB_ERR_TIMEOUT", 6: "BB_ERR_NOMEM"}
@@ -235,10 +235,13 @@ def bb_back_transform(h, U, ldu: int, V, ldv: int, stream=None) -> None:
 
 
 def dtype_code(dtype) -> int:
-    """BB_F32 / BB_F64 from a torch or numpy dtype or the strings 'f32'/'f64'."""
+    """BB_F32 / BB_F64 / BB_F16 from a torch or numpy dtype or the strings
+    'f32' / 'f64' / 'f16'."""
     s = str(dtype)
     if s in ("f32", "float32", "torch.float32"):
         return BB_F32
     if s in ("f64", "float64", "torch.float64"):
         return BB_F64
+    if s in ("f16", "float16", "torch.float16"):
+        return BB_F16
     raise ValueError(f"unsupported dtype {dtype}")

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "../../include/bb.h"
+#include "bb_half.h"
 #include "bb_internal.h"
 #include "bb_sym.h"
 #include "bb_vectors.h"
@@ -68,7 +69,7 @@ int64_t steps_of_sweep(int64_t n, int b, int t, int64_t r) {
     return last < 0 ? 0 : last / b + 1;
 }
 
-size_t elem_size(bb_dtype d) { return d == BB_F64 ? 8 : 4; }
+size_t elem_size(bb_dtype d) { return d == BB_F64 ? 8 : d == BB_F16 ? 2 : 4; }
 
 bool is_device_pointer(const void* p) {
     cudaPointerAttributes a;
@@ -208,7 +209,7 @@ int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass) {
 }
 
 bb_handle* bb_create(int64_t n, int64_t bw, bb_dtype dtype) {
-    if (dtype != BB_F32 && dtype != BB_F64) {
+    if (dtype != BB_F32 && dtype != BB_F64 && dtype != BB_F16) {
         fail(BB_ERR_DTYPE, "bb_create: unknown dtype");
         return nullptr;
     }
@@ -371,8 +372,9 @@ static bb_status check_reduce_args(bb_handle* h, int64_t ldab, int64_t tw) {
     if (ldab < bb_required_ldab(h->bw, tw)) return fail(BB_ERR_LDAB, "ldab < bw + 2*tw + 1");
     if ((double)ldab * (double)h->n > 9.0e18 / 8) return fail(BB_ERR_INVALID_ARG, "band too large");
     // shared memory of the widest pass (the first): tile of (b + t + 1)
-    // columns; later passes have a smaller b and no larger t
-    if (count_passes(h->bw, tw) > 0 &&
+    // columns; later passes have a smaller b and no larger t (the binary16
+    // path keeps no tile)
+    if (h->dtype != BB_F16 && count_passes(h->bw, tw) > 0 &&
         flag_tile_bytes(h->bw, std::min<int64_t>(tw, h->bw - 1), elem_size(h->dtype)) > 227 * 1024)
         return fail(BB_ERR_INVALID_ARG, "bandwidth too large for the shared-memory tile");
     return BB_OK;
@@ -581,6 +583,71 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
     return BB_OK;
 }
 
+// Binary16 storage (float arithmetic): one persistent kernel per pass, the
+// flag kernel's progress protocol (bb_half.cu).  The scheduler parameter
+// does not apply; the pass range, timing, grid cap, wait budget and fault
+// injection do.
+static bb_status half_reduce(bb_handle* h, void* band, int64_t ldab, int64_t tw, void* d, void* e,
+                             cudaStream_t s) {
+    const int64_t n = h->n;
+    const int ku = (int)(h->bw + tw);
+    cudaError_t err;
+    h->last_launches = 0;
+    h->last_passes = 0;
+    h->pass_kernel.clear();
+    h->pass_group.clear();
+    h->rec_valid = false;
+    const int64_t np = count_passes(h->bw, tw);
+    const int64_t lo = std::max<int64_t>(0, h->pass_lo);
+    const int64_t hi = std::min<int64_t>(np, h->pass_hi);
+    if (lo == 0) {
+        err = bb::run_half_zero_fill(band, n, ldab, (int)tw, ku, h->num_sms, s);
+        if (err != cudaSuccess) return cuda_fail(err, "zero fill launch");
+        h->last_launches += 1;
+    }
+    if (h->timing) {
+        const size_t need = 2 * (size_t)std::max<int64_t>(0, hi - lo);
+        while (h->ev.size() < need) {
+            cudaEvent_t ev;
+            err = cudaEventCreate(&ev);
+            if (err != cudaSuccess) return cuda_fail(err, "cudaEventCreate");
+            h->ev.push_back(ev);
+        }
+    }
+    bb::HalfLaunch L;
+    L.num_sms = h->num_sms;
+    L.max_ctas = h->max_ctas;
+    L.progress = h->d_progress;
+    L.status = h->d_status;
+    for (int64_t pi = lo; pi < hi; ++pi) {
+        const PassPlan ps = pass_at(h->bw, tw, pi);
+        bb::PassArgs P;
+        P.n = n;
+        P.ldab = ldab;
+        P.b = ps.b;
+        P.t = ps.t;
+        P.bp = ps.b - ps.t;
+        P.ku = ku;
+        P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
+        P.lag = bb::pass_lag_cycle(P.b, P.t);
+        P.lagh = bb::pass_lag_half(P.b, P.t);
+        P.stall_sweep = h->stall_sweep;
+        P.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+        if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo)], s);
+        err = bb::run_half_pass(band, P, L, s);
+        if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo) + 1], s);
+        if (err != cudaSuccess) return cuda_fail(err, "pass launch");
+        h->last_launches += (P.nsweeps > 0) ? 1 : 0;
+        h->last_passes += 1;
+        h->pass_kernel.push_back(5);
+        h->pass_group.push_back(0);
+    }
+    err = bb::run_half_extract(band, n, ldab, ku, d, e, h->num_sms, s);
+    if (err != cudaSuccess) return cuda_fail(err, "extract launch");
+    h->last_launches += 1;
+    return BB_OK;
+}
+
 extern "C" {
 
 static bb_status reduce_checked(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out,
@@ -593,6 +660,7 @@ static bb_status reduce_checked(bb_handle* h, void* band_ptr, int64_t ldab, int6
         (h->n > 1 && !is_device_pointer(e_out)))
         return fail(BB_ERR_INVALID_ARG, "band, d and e must be device pointers");
     cudaStream_t s = (cudaStream_t)stream;
+    if (h->dtype == BB_F16) return half_reduce(h, band_ptr, ldab, tw, d_out, e_out, s);
     if (h->dtype == BB_F32)
         return reduce_impl<float>(h, (float*)band_ptr, ldab, tw, (float*)d_out, (float*)e_out, s);
     return reduce_impl<double>(h, (double*)band_ptr, ldab, tw, (double*)d_out, (double*)e_out, s);
@@ -616,6 +684,7 @@ int64_t bb_sym_required_ldab(int64_t bw, int64_t tw) { return bw + tw + 1; }
 static bb_status sym_checked(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out, void* e_out,
                              bb_stream_t stream) {
     if (!h) return fail(BB_ERR_INVALID_ARG, "null handle");
+    if (h->dtype == BB_F16) return fail(BB_ERR_DTYPE, "bb_sym_reduce: binary16 storage is not supported");
     const int64_t tw_max = std::max<int64_t>(1, h->bw - 1);
     if (tw < 1 || tw > tw_max) return fail(BB_ERR_INVALID_ARG, "need 1 <= tw <= max(1, bw - 1)");
     if (tw > 64) return fail(BB_ERR_INVALID_ARG, "tw > 64 is not supported");

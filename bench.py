@@ -34,7 +34,8 @@ replay, the flag and the group kernel), per_workload (each other workload,
 5 timed steps after 2 warm-up steps: its own roofline, e2e and CPU baseline
 -- the serial oracle where a reduction takes seconds, else the oracle's
 multi-thread driver on the first pass), singular_values (bb_singular_values
-on the reduction's output) and symmetric (the symmetric band variant).
+on the reduction's output), symmetric (the symmetric band variant) and
+half_storage (the main workload's band in binary16 storage, BB_F16).
 """
 from __future__ import annotations
 
@@ -303,6 +304,46 @@ def run_sym(w: bi.Workload, steps: int, warmup: int):
     except Exception as ex:  # context only
         out["cpu_pipelined_error"] = f"{type(ex).__name__}: {ex}"
     return out
+
+
+def run_half(w: bi.Workload, steps: int, warmup: int):
+    """Binary16 storage (BB_F16): device time of bb_reduce on the workload's
+    band rounded to binary16 (L2 flushed and the band restored before each
+    step, outside the events), with its algorithmic bytes at 2 bytes an
+    entry."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    dev = torch.device("cuda", torch.cuda.current_device())
+    band_np = bi.make_band(w.n, w.bw, w.tw, "f64", w.dist, w.graded, w.seed).astype(np.float16)
+    pristine = torch.from_numpy(band_np).to(dev)
+    band = pristine.clone()
+    d = torch.empty(w.n, dtype=torch.float16, device=dev)
+    e = torch.empty(max(w.n - 1, 1), dtype=torch.float16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    h = bb.bb_create(w.n, w.bw, bb.BB_F16)
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    try:
+        for i in range(warmup + steps):
+            band.copy_(pristine)
+            flush.fill_(i & 0xFF)
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            bb.bb_reduce(h, band, band.shape[1], w.tw, d, e, stream)
+            ev1.record(stream)
+            if bb.bb_status_sync(h, stream) != bb.BB_OK:
+                raise RuntimeError("binary16 reduction failed: " + bb.bb_last_error())
+            if i >= warmup:
+                times.append(ev0.elapsed_time(ev1))
+    finally:
+        bb.bb_destroy(h)
+    ms = statistics.median(times)
+    mb = model_bytes_np(w.n, w.bw, w.tw, 2)
+    return {"ms": ms, "n": w.n, "bw": w.bw, "tw": w.tw, "dtype": "f16 storage, f32 arithmetic",
+            "effective_gbs": mb / (ms * 1e-3) / 1e9, "kernel": "pass_half_kernel",
+            "launches": int(bb.bb_num_passes(w.bw, w.tw)) + 2}
 
 
 def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
@@ -688,6 +729,13 @@ def main():
         except Exception as ex:  # a side measurement never loses the line
             sym = {"error": f"{type(ex).__name__}: {ex}"}
 
+    half = None
+    if rank == 0 and world == 1 and not args.no_sweep:
+        try:
+            half = run_half(w, args.steps, args.warmup)
+        except Exception as ex:  # a side measurement never loses the line
+            half = {"error": f"{type(ex).__name__}: {ex}"}
+
     cpu = cpu_pipe = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_oracle_rate(w)
@@ -722,6 +770,7 @@ def main():
             "per_workload": sweep,
             "singular_values": svals,
             "symmetric": sym,
+            "half_storage": half,
         }
         print(json.dumps(line))
     if world > 1:

@@ -40,8 +40,15 @@
 extern "C" {
 #endif
 
-/* Element type of the band, d and e. */
-typedef enum { BB_F32 = 0, BB_F64 = 1 } bb_dtype;
+/* Element type of the band, d and e.  BB_F16: IEEE binary16 storage with
+ * float arithmetic -- every step reads its entries into float, builds and
+ * applies its reflectors in float, and writes every entry it changes back
+ * rounded to binary16 (round to nearest even); d and e are binary16 too.
+ * The paper runs the method in FP16 as well (Section V).  BB_F16 handles
+ * run every pass on one persistent kernel with the flag kernel's progress
+ * protocol (BB_PARAM_SCHEDULER does not apply), and are accepted by
+ * bb_create, bb_reduce, bb_reduce_host and bb_status_sync only. */
+typedef enum { BB_F32 = 0, BB_F64 = 1, BB_F16 = 2 } bb_dtype;
 
 /* Return codes. */
 typedef enum {
@@ -218,9 +225,9 @@ int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass);
 int64_t bb_last_launches(const bb_handle* h);
 
 /* Kernel that ran pass i of the last reduction: 1 per-cycle, 2 flag kernel,
- * 3 group kernel, 4 per-cycle launches replayed from a CUDA graph (-1 if out
- * of range), and, for the group kernel, its group size (sweeps per CTA; 0
- * otherwise).  With scheduler 4, bb_last_launches counts the kernels the
+ * 3 group kernel, 4 per-cycle launches replayed from a CUDA graph, 5 the
+ * binary16 storage kernel (-1 if out of range), and, for the group kernel,
+ * its group size (sweeps per CTA; 0 otherwise).  With scheduler 4, bb_last_launches counts the kernels the
  * graphs ran. */
 int64_t bb_last_pass_kernel(const bb_handle* h, int64_t i);
 int64_t bb_last_pass_group(const bb_handle* h, int64_t i);
