@@ -240,6 +240,14 @@ __device__ __forceinline__ T warp_larfg(T (&x)[NPL], int w, int lane, T* s_v, T*
     return beta;
 }
 
+// Applies that stream each row (column) through shared memory twice (dot
+// product, then update) instead of holding it in registers: the kernels
+// with reflectors of 256 bytes or more (32 and 33 doubles), which otherwise
+// run out of registers and spill the row to local memory.  The arithmetic
+// and its order are the same either way.
+template <typename T, int WMAX>
+constexpr bool kStreamApply = WMAX * sizeof(T) >= 256;
+
 // Shared-memory layout of one CTA (ncolmax = b + t + 1 of the pass).
 //   v[WMAX]              reflector of the current half-step
 //   tau                  its scalar
@@ -424,18 +432,34 @@ __device__ __forceinline__ void right_post(T* __restrict__ band, const PassArgs&
     for (int i = tid; i < g.nrows; i += nthr) {
         T x[WMAX];
         const T* src = sm.rtile + i * sm.wp;
+        if constexpr (kStreamApply<T, WMAX>) {
+            // dot product from shared memory, then each entry read again and
+            // updated: the row is never held whole in registers
+            T s = 0;
+            if (tau != T(0)) {
+                T y = 0;
 #pragma unroll
-        for (int m = 0; m < WMAX; ++m)
-            if (m < W) x[m] = src[m];
-        if (tau != T(0)) {
-            T y = 0;
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < W) y = fma(src[m], sm.v[m], y);
+                s = tau * y;
+            }
 #pragma unroll
             for (int m = 0; m < WMAX; ++m)
-                if (m < W) y = fma(x[m], sm.v[m], y);
-            const T s = tau * y;
+                if (m < W) x[m] = (tau != T(0)) ? fma(-s, sm.v[m], src[m]) : src[m];
+        } else {
 #pragma unroll
             for (int m = 0; m < WMAX; ++m)
-                if (m < W) x[m] = fma(-s, sm.v[m], x[m]);
+                if (m < W) x[m] = src[m];
+            if (tau != T(0)) {
+                T y = 0;
+#pragma unroll
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < W) y = fma(x[m], sm.v[m], y);
+                const T s = tau * y;
+#pragma unroll
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < W) x[m] = fma(-s, sm.v[m], x[m]);
+            }
         }
         const int rr = i - row_c;  // row c + rr
         if (rr < 0) {
@@ -540,19 +564,30 @@ __device__ __forceinline__ void left_post(T* __restrict__ band, const PassArgs& 
     const T tau = *sm.tau;
     if (tau != T(0)) {
         for (int jl = 1 + tid; jl < ncol; jl += nthr) {
-            T x[WMAX];
             T* col = sm.tile + jl * wp;
-            T y = 0;
+            if constexpr (kStreamApply<T, WMAX>) {
+                T y = 0;
 #pragma unroll
-            for (int m = 0; m < WMAX; ++m)
-                if (m < w) {
-                    x[m] = col[m];
-                    y = fma(sm.v[m], x[m], y);
-                }
-            const T s = tau * y;
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < w) y = fma(sm.v[m], col[m], y);
+                const T s = tau * y;
 #pragma unroll
-            for (int m = 0; m < WMAX; ++m)
-                if (m < w) col[m] = fma(-s, sm.v[m], x[m]);
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < w) col[m] = fma(-s, sm.v[m], col[m]);
+            } else {
+                T x[WMAX];
+                T y = 0;
+#pragma unroll
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < w) {
+                        x[m] = col[m];
+                        y = fma(sm.v[m], x[m], y);
+                    }
+                const T s = tau * y;
+#pragma unroll
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < w) col[m] = fma(-s, sm.v[m], x[m]);
+            }
         }
     }
     __syncthreads();
