@@ -3,6 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--scheduler 0|1|2|3|4] [--group-size G]
                     [--no-sweep] [--no-cpu] [--no-e2e]
+    python bench.py --profile-pass WORKLOAD:N:PASS:SCHEDULER:DTYPE[:MAX_CTAS]
 
 One step is one whole reduction (every pass down to bidiagonal form, plus the
 fill-row zeroing and the d/e extraction) of one synthetic band.  Before each
@@ -613,6 +614,40 @@ def traffic_for(kernel: str, workload: str):
         return None
 
 
+def profile_pass(spec: str) -> int:
+    """--profile-pass WORKLOAD:N:PASS:SCHEDULER:DTYPE[:MAX_CTAS] -- one run of
+    one pass of the workload's recipe at order N (DTYPE f32, f64 or f16), for
+    an ncu capture of that pass's kernel; prints one line, no timing."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    parts = spec.split(":")
+    name, n, p, sched, dt = parts[0], int(parts[1]), int(parts[2]), int(parts[3]), parts[4]
+    ctas = int(parts[5]) if len(parts) > 5 else 0
+    w = bi.by_name(name)
+    if dt == "f16":
+        band_np = bi.make_band(n, w.bw, w.tw, "f64", w.dist, w.graded, w.seed).astype(np.float16)
+    else:
+        band_np = bi.make_band(n, w.bw, w.tw, dt, w.dist, w.graded, w.seed)
+    torch.cuda.set_device(0)
+    band = torch.from_numpy(band_np).cuda()
+    d = torch.empty(n, dtype=band.dtype, device="cuda")
+    e = torch.empty(n, dtype=band.dtype, device="cuda")
+    h = bb.bb_create(n, w.bw, bb.dtype_code(dt))
+    try:
+        bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, sched)
+        bb.bb_set_param(h, bb.BB_PARAM_MAX_CTAS, ctas)
+        bb.bb_set_param(h, bb.BB_PARAM_PASS_LO, p)
+        bb.bb_set_param(h, bb.BB_PARAM_PASS_HI, p + 1)
+        s = torch.cuda.current_stream()
+        bb.bb_reduce(h, band, band.shape[1], w.tw, d, e, s)
+        st = bb.bb_status_sync(h, s)
+    finally:
+        bb.bb_destroy(h)
+    print(f"profile pass: {name} n={n} pass={p} scheduler={sched} dtype={dt} max_ctas={ctas} status={st}")
+    return 0 if st == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -626,7 +661,11 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (e2e) leg")
+    ap.add_argument("--profile-pass", default=None, metavar="WORKLOAD:N:PASS:SCHEDULER:DTYPE[:MAX_CTAS]",
+                    help="run one pass once for a profiler capture and exit (no measurement)")
     args = ap.parse_args()
+    if args.profile_pass:
+        return profile_pass(args.profile_pass)
     rank, world, local = dist_env()
     w = bi.by_name(args.workload)
 
