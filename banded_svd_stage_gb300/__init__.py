@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
             "bb_singular_values_lanes": ([ci, i64, p, p, p, i64, p], ci),
             "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
             "bb_sym_reduce": ([p, p, i64, i64, p, p, p], ci),
+            "bb_dense_to_band_workspace": ([i64, ci], i64),
+            "bb_dense_to_band": ([ci, i64, i64, p, i64, p, i64, p], ci),
+            "bb_pack_band": ([ci, i64, i64, i64, p, i64, p, i64, p], ci),
             "bb_sym_required_ldab": ([i64, i64], i64),
             "bb_back_transform": ([p, p, i64, p, i64, p], ci),
         }
@@ -224,6 +227,20 @@ def bb_singular_values(dtype: int, n: int, d, e, sigma_out, stream=None) -> None
 def bb_sym_reduce(h, band, ldab: int, tw: int, d, e, stream=None) -> None:
     """Symmetric band (lower band storage, device) -> tridiagonal (d, e)."""
     _check(lib().bb_sym_reduce(h, _addr(band), ldab, tw, _addr(d), _addr(e), _stream(stream)))
+
+
+def bb_dense_to_band_workspace(n: int, dtype: int) -> int:
+    return lib().bb_dense_to_band_workspace(n, dtype)
+
+
+def bb_dense_to_band(dtype: int, n: int, bw: int, a, lda: int, workspace, workspace_bytes: int, stream=None) -> None:
+    """Stage 1: dense column-major a (device) -> upper band of bandwidth bw, in place."""
+    _check(lib().bb_dense_to_band(dtype, n, bw, _addr(a), lda, _addr(workspace), workspace_bytes, _stream(stream)))
+
+
+def bb_pack_band(dtype: int, n: int, bw: int, tw: int, a, lda: int, band, ldab: int, stream=None) -> None:
+    """The upper band of dense column-major a (device) into bb_reduce's band storage."""
+    _check(lib().bb_pack_band(dtype, n, bw, tw, _addr(a), lda, _addr(band), ldab, _stream(stream)))
 
 
 def bb_sym_required_ldab(bw: int, tw: int) -> int:

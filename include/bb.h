@@ -288,6 +288,34 @@ bb_status bb_singular_values(bb_dtype dtype, int64_t n, const void* d, const voi
 bb_status bb_singular_values_lanes(bb_dtype dtype, int64_t n, const void* d, const void* e, void* sigma_out,
                                    int64_t lanes, bb_stream_t stream);
 
+/* Stage 1 of the two-stage SVD, the step before this library's reduction:
+ * the dense n x n matrix a (device, column-major, leading dimension
+ * lda >= n, element type dtype: BB_F32 or BB_F64) is reduced in place to
+ * upper band form of bandwidth bw >= 1 by orthogonal transformations, the
+ * block Householder reduction that the accuracy protocol of "Accelerating
+ * Bidiagonalization of Banded Matrices through Memory-Aware Bulge-Chasing
+ * on GPUs" (Section V) runs before the band stage.  For each panel of bw
+ * columns k .. k+bw-1: QR of the panel column by column (the reflector of
+ * A(j.., j), LAPACK xLARFG convention, applied from the left to every later
+ * column), then LQ of the panel's rows right of the band (the reflector of
+ * A(i, i+bw ..), applied from the right to every later row).  Entries outside
+ * the band (0 <= j - i <= bw) become exactly zero.  workspace: device memory
+ * of at least bb_dense_to_band_workspace(n, dtype) bytes, owned by the caller
+ * and not read afterwards.  Asynchronous on `stream` (one or two kernel
+ * launches per reflector); the return code covers arguments and launches.
+ * bb_dense_to_band_workspace returns -1 for invalid arguments. */
+int64_t bb_dense_to_band_workspace(int64_t n, bb_dtype dtype);
+bb_status bb_dense_to_band(bb_dtype dtype, int64_t n, int64_t bw, void* a, int64_t lda, void* workspace,
+                           int64_t workspace_bytes, bb_stream_t stream);
+
+/* Copy the upper band (0 <= j - i <= bw) of the dense column-major matrix a
+ * (device, lda >= n) into the band storage of bb_reduce (device, ldab >=
+ * bw + 2*tw + 1, A(i, j) at band[(bw + tw + i - j) + j * ldab]), every other
+ * stored entry zero, so that stage 1's result feeds bb_reduce directly.
+ * dtype BB_F32 or BB_F64; 0 <= bw < n, tw >= 0.  Asynchronous on `stream`. */
+bb_status bb_pack_band(bb_dtype dtype, int64_t n, int64_t bw, int64_t tw, const void* a, int64_t lda, void* band,
+                       int64_t ldab, bb_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
