@@ -108,12 +108,16 @@ __device__ __forceinline__ void sym_step(T* __restrict__ band, const PassArgs& P
             for (int m = 0; m < WMAX; ++m)
                 if (m < w) sym_st(band, ld, i, c + m, fma(-s, s_v[m], a[m]));
         } else {
+            // row u of x = tau S v; unrolled over the compiled width so that
+            // the row's loads are in flight together
             const int u = idx - nleft - nbelow;
             T y = 0;
-            for (int q = 0; q < w; ++q) {
-                const T sq = (u >= q) ? sym_ld(band, ld, c + u, c + q) : sym_ld(band, ld, c + q, c + u);
-                y = fma(sq, s_v[q], y);
-            }
+#pragma unroll
+            for (int q = 0; q < WMAX; ++q)
+                if (q < w) {
+                    const T sq = (u >= q) ? sym_ld(band, ld, c + u, c + q) : sym_ld(band, ld, c + q, c + u);
+                    y = fma(sq, s_v[q], y);
+                }
             s_x[u] = tau * y;
         }
     }
@@ -126,12 +130,16 @@ __device__ __forceinline__ void sym_step(T* __restrict__ band, const PassArgs& P
         for (int u = threadIdx.x; u < w; u += 32) s_x[u] = fma(alpha, s_v[u], s_x[u]);
     }
     __syncthreads();
-    // S -= v x^T + x v^T on the lower triangle: one thread per column q
-    for (int q = threadIdx.x; q < w; q += blockDim.x) {
-        for (int u = q; u < w; ++u) {
-            const T a = sym_ld(band, ld, c + u, c + q);
-            sym_st(band, ld, c + u, c + q, a - s_v[u] * s_x[q] - s_x[u] * s_v[q]);
-        }
+    // S -= v x^T + x v^T on the lower triangle: one thread per entry (u, q),
+    // 0 <= q <= u < w, entry e = u (u + 1) / 2 + q
+    const int npairs = w * (w + 1) / 2;
+    for (int e = threadIdx.x; e < npairs; e += blockDim.x) {
+        int u = (int)((sqrtf(8.f * (float)e + 1.f) - 1.f) * 0.5f);
+        while (u * (u + 1) / 2 > e) --u;
+        while ((u + 1) * (u + 2) / 2 <= e) ++u;
+        const int q = e - u * (u + 1) / 2;
+        const T a = sym_ld(band, ld, c + u, c + q);
+        sym_st(band, ld, c + u, c + q, a - s_v[u] * s_x[q] - s_x[u] * s_v[q]);
     }
 }
 

@@ -35,8 +35,10 @@ replay, the flag and the group kernel), per_workload (each other workload,
 5 timed steps after 2 warm-up steps: its own roofline, e2e and CPU baseline
 -- the serial oracle where a reduction takes seconds, else the oracle's
 multi-thread driver on the first pass), singular_values (bb_singular_values
-on the reduction's output), symmetric (the symmetric band variant) and
-half_storage (the main workload's band in binary16 storage, BB_F16).
+on the reduction's output), symmetric (the symmetric band variant),
+half_storage (the main workload's band in binary16 storage, BB_F16) and
+stage1 (bb_dense_to_band on a dense matrix of the main workload's order,
+bandwidth and dtype).
 """
 from __future__ import annotations
 
@@ -345,6 +347,55 @@ def run_half(w: bi.Workload, steps: int, warmup: int):
     return {"ms": ms, "n": w.n, "bw": w.bw, "tw": w.tw, "dtype": "f16 storage, f32 arithmetic",
             "effective_gbs": mb / (ms * 1e-3) / 1e9, "kernel": "pass_half_kernel",
             "launches": int(bb.bb_num_passes(w.bw, w.tw)) + 2}
+
+
+def stage1_flops(n: int, bw: int) -> float:
+    """Flops of stage 1's rank-one applications (a dot product and an update,
+    4 flops an entry): every QR reflector j on rows j.. of columns j+1..,
+    every LQ reflector i on rows i+1.. of columns i+bw.."""
+    tot = 0.0
+    for k in range(0, n, bw):
+        for j in range(k, min(k + bw, n)):
+            if j + 1 < n:
+                tot += 4.0 * (n - j) * (n - j - 1)
+        for i in range(k, min(k + bw, n)):
+            c0 = i + bw
+            if c0 + 1 < n:
+                tot += 4.0 * (n - i - 1) * (n - c0)
+    return tot
+
+
+def run_stage1(w: bi.Workload, steps: int, warmup: int):
+    """Stage 1 (bb_dense_to_band) on a seeded dense n x n matrix of the
+    workload's dtype, to the workload's bandwidth: device time per call."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rng = np.random.default_rng(w.seed)
+    a_np = rng.standard_normal((w.n, w.n)).astype(np.float32 if w.dtype == "f32" else np.float64)
+    pristine = torch.from_numpy(a_np).to(dev)
+    a = pristine.clone()
+    code = bb.dtype_code(w.dtype)
+    nbytes = bb.bb_dense_to_band_workspace(w.n, code)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    for i in range(warmup + steps):
+        a.copy_(pristine)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        bb.bb_dense_to_band(code, w.n, w.bw, a, w.n, ws, nbytes, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            times.append(ev0.elapsed_time(ev1))
+    ms = statistics.median(times)
+    fl = stage1_flops(w.n, w.bw)
+    return {"ms": ms, "n": w.n, "bw": w.bw, "dtype": w.dtype, "gflops": fl / (ms * 1e-3) / 1e9,
+            "flops_model": "4 flops per entry of every rank-one application",
+            "kernels": "s1_larfg_kernel, s1_apply_left_kernel, s1_gemv_rows_kernel, s1_rank1_kernel"}
 
 
 def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
@@ -768,6 +819,12 @@ def main():
         except Exception as ex:  # a side measurement never loses the line
             sym = {"error": f"{type(ex).__name__}: {ex}"}
 
+    stage1 = None
+    if rank == 0 and world == 1 and not args.no_sweep:
+        try:
+            stage1 = run_stage1(w, 3, 1)
+        except Exception as ex:  # a side measurement never loses the line
+            stage1 = {"error": f"{type(ex).__name__}: {ex}"}
     half = None
     if rank == 0 and world == 1 and not args.no_sweep:
         try:
@@ -810,6 +867,7 @@ def main():
             "singular_values": svals,
             "symmetric": sym,
             "half_storage": half,
+            "stage1": stage1,
         }
         print(json.dumps(line))
     if world > 1:

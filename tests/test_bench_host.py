@@ -128,3 +128,11 @@ def test_cpu_baseline_for_both_kinds():
     pipe = bench.cpu_baseline_for(w, budget_s=0.2, serial_limit_bytes=0)
     assert pipe["kind"].startswith("oracle, pipelined") and pipe["cores"] >= 1 and pipe["value"] > 0
     assert "first pass (24->16)" in pipe["sample"]
+
+
+def test_stage1_flop_model():
+    # n = 5, bw = 2: QR reflectors j = 0..3 act on (5 - j) x (4 - j) entries,
+    # LQ reflectors of panel 0 (i = 0, 1; c0 = 2, 3) on (4 - i) x (5 - c0),
+    # of panel 1 (i = 2; c0 = 4 -> none)
+    want = 4.0 * (5 * 4 + 4 * 3 + 3 * 2 + 2 * 1) + 4.0 * (4 * 3 + 3 * 2)
+    assert bench.stage1_flops(5, 2) == want
