@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "bb_singular_values": ([ci, i64, p, p, p, p], ci),
             "bb_singular_values_lanes": ([ci, i64, p, p, p, i64, p], ci),
             "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
+            "bb_sym_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
             "bb_sym_reduce": ([p, p, i64, i64, p, p, p], ci),
             "bb_dense_to_band_workspace": ([i64, ci], i64),
             "bb_dense_to_band": ([ci, i64, i64, p, i64, p, i64, p], ci),
@@ -215,6 +216,15 @@ def bb_group_plan(n: int, bw: int, tw: int, elem_bytes: int, pass_index: int, gr
     when the group kernel cannot take it.  Host-only."""
     vals = [ctypes.c_int64() for _ in range(4)]
     _check(lib().bb_group_plan(n, bw, tw, elem_bytes, pass_index, group_size, *[ctypes.byref(v) for v in vals]))
+    return tuple(v.value for v in vals)
+
+
+def bb_sym_group_plan(n: int, bw: int, tw: int, elem_bytes: int, pass_index: int, group_size: int = 0):
+    """(g, nslot, ahead, lds) of the symmetric chase's group-kernel plan for
+    one pass; g = 0 when its group kernel cannot take it.  Host-only."""
+    vals = [ctypes.c_int64() for _ in range(4)]
+    _check(lib().bb_sym_group_plan(n, bw, tw, elem_bytes, pass_index, group_size,
+                                   *[ctypes.byref(v) for v in vals]))
     return tuple(v.value for v in vals)
 
 

@@ -18,8 +18,8 @@ BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
 LIB_PATH = os.path.join(HERE, "libbb.so")
 SOURCES = ["bb_api.cu", "bb_kernels_f32.cu", "bb_kernels_f64.cu", "bb_kernels_f32_narrow.cu",
            "bb_kernels_f32_wide.cu", "bb_kernels_f64_narrow.cu", "bb_kernels_f64_wide.cu", "bb_noalloc.cu",
-           "bb_svals.cu", "bb_plan.cu", "bb_sym.cu", "bb_vectors.cu", "bb_half.cu",
-           "bb_stage1.cu"]
+           "bb_svals.cu", "bb_plan.cu", "bb_sym.cu", "bb_sym_group_f32.cu", "bb_sym_group_f64.cu",
+           "bb_vectors.cu", "bb_half.cu", "bb_stage1.cu"]
 # The pass kernels: their device code and the host planner that fixes their
 # launch shape.  The C-ABI checks (bb_api.cu), the allocation-free entry
 # (bb_noalloc.cu) and the singular-value kernel (bb_svals.cu) are not part of

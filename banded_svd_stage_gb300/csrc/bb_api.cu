@@ -174,6 +174,39 @@ bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, i
     }
 }
 
+bb_status bb_sym_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass,
+                            int64_t group_size, int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds) {
+    if (n < 1 || n >= bb::kGroupMaxN || bw < 0 || bw >= n || tw < 1 || tw > std::max<int64_t>(1, bw - 1) ||
+        pass < 0 || pass >= count_passes(bw, tw) || !g || !nslot || !ahead || !lds ||
+        (elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
+        return fail(BB_ERR_INVALID_ARG, "bb_sym_group_plan: argument out of range");
+    try {
+        const PassPlan ps = pass_at(bw, tw, pass);
+        bb::PassArgs P{};
+        P.n = n;
+        P.b = ps.b;
+        P.t = ps.t;
+        P.bp = P.b - P.t;
+        P.ku = 0;
+        P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
+        P.lag = bb::sym_pass_lag(P.b, P.t);
+        P.lagh = P.lag;
+        const int wmax = bb::sym_group_wmax(P.t + 1);
+        bb::GroupArgs ga{};
+        const bool ok = P.nsweeps > 0 && wmax > 0 &&
+                        bb::plan_group(P, wmax, (size_t)elem_bytes, (int)group_size, &ga, bb::ChaseKind::kSym);
+        *g = ok ? ga.g : 0;
+        *nslot = ok ? ga.nslot : 0;
+        *ahead = ok ? ga.ahead : 0;
+        *lds = ok ? ga.lds : 0;
+        return BB_OK;
+    } catch (const std::bad_alloc&) {
+        return fail(BB_ERR_NOMEM, "bb_sym_group_plan: host allocation failed");
+    } catch (...) {
+        return fail(BB_ERR_INTERNAL, "bb_sym_group_plan: unexpected host exception");
+    }
+}
+
 double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass) {
     double total = 0;
     const int64_t np = count_passes(bw, tw);
@@ -700,18 +733,48 @@ static bb_status sym_checked(bb_handle* h, void* band_ptr, int64_t ldab, int64_t
     L.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
     L.progress = h->d_progress;
     L.status = h->d_status;
+    L.scheduler = h->scheduler;
+    L.group_size = h->group_size;
     long long nl = 0;
+    bb::SymPassStats st;
     cudaError_t err;
+    const size_t elem = (h->dtype == BB_F32) ? 4 : 8;
+    const cudaStream_t s = (cudaStream_t)stream;
+    // The group kernel moves whole columns with bulk copies, which need a
+    // 16-byte aligned column stride: on any other layout the reduction runs
+    // on an aligned working copy (one strided copy in, one out).
+    void* wb = band_ptr;
+    int64_t ldw = ldab;
+    if (bb::sym_any_group(h->n, (int)h->bw, (int)tw, L, elem) && !bb::group_layout_ok(band_ptr, ldab, elem)) {
+        const int64_t q = 16 / (int64_t)elem;
+        ldw = (ldab + q - 1) / q * q;
+        const size_t bytes = elem * (size_t)ldw * (size_t)h->n;
+        if (h->work_bytes < bytes) {
+            if (h->work) cudaFree(h->work);
+            h->work = nullptr;
+            h->work_bytes = 0;
+            err = cudaMalloc(&h->work, bytes);
+            if (err != cudaSuccess) return fail(BB_ERR_NOMEM, "working band allocation failed");
+            h->work_bytes = bytes;
+        }
+        wb = h->work;
+        err = cudaMemcpy2DAsync(wb, elem * ldw, band_ptr, elem * ldab, elem * ldab, (size_t)h->n,
+                                cudaMemcpyDeviceToDevice, s);
+        if (err != cudaSuccess) return cuda_fail(err, "copy to the working band");
+    }
     if (h->dtype == BB_F32)
-        err = bb::run_sym<float>((float*)band_ptr, h->n, ldab, (int)h->bw, (int)tw, (float*)d_out, (float*)e_out, L,
-                                 (cudaStream_t)stream, &nl);
+        err = bb::run_sym<float>((float*)wb, h->n, ldw, (int)h->bw, (int)tw, (float*)d_out, (float*)e_out, L, s,
+                                 &nl, &st);
     else
-        err = bb::run_sym<double>((double*)band_ptr, h->n, ldab, (int)h->bw, (int)tw, (double*)d_out,
-                                  (double*)e_out, L, (cudaStream_t)stream, &nl);
+        err = bb::run_sym<double>((double*)wb, h->n, ldw, (int)h->bw, (int)tw, (double*)d_out, (double*)e_out, L,
+                                  s, &nl, &st);
+    if (err == cudaSuccess && wb != band_ptr)
+        err = cudaMemcpy2DAsync(band_ptr, elem * ldab, wb, elem * ldw, elem * ldab, (size_t)h->n,
+                                cudaMemcpyDeviceToDevice, s);
     h->last_launches = nl;
-    h->last_passes = 0;
-    h->pass_kernel.clear();
-    h->pass_group.clear();
+    h->last_passes = (int64_t)st.kernel.size();
+    h->pass_kernel = st.kernel;
+    h->pass_group = st.group;
     if (err != cudaSuccess) return cuda_fail(err, "bb_sym_reduce launch");
     return BB_OK;
 }

@@ -237,21 +237,35 @@ __device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, 
     }
 }
 
-template <typename T, int WMAX>
-// slot: the buffer slot of column c of this half-step's step (the caller
-// carries it from step to step, sparing a modulo on the critical path).
-__device__ __forceinline__ void group_half(const PassArgs& P, const ColBuf<T>& cb, int r, int h, int slot, T* vb,
-                                           T* taub) {
-    const GGeom g = gstep(P, r, h >> 1);
-    const bool full = g.w == WMAX;
-    if ((h & 1) == 0) {
-        if (full) group_right<T, WMAX, true>(cb, g, slot, vb, taub);
-        else group_right<T, WMAX, false>(cb, g, slot, vb, taub);
-    } else {
-        if (full) group_left<T, WMAX, true>(cb, g, slot, vb, taub);
-        else group_left<T, WMAX, false>(cb, g, slot, vb, taub);
+// The chase a group kernel runs.  A sweep is a sequence of units, kUnits
+// per step; the lockstep lag (PassArgs::lagh) and the loader's and storer's
+// column bookkeeping count units.  A chase provides the first and last band
+// column unit h of sweep r touches (columns only move right as h grows), the
+// unit itself on the buffered band by one warp, and kVecs, the reflector-sized
+// vectors of shared scratch each warp needs.
+//
+// The bidiagonal chase: two units per step, the right half-step (rows p..ce
+// of columns c..ce) and the left one (rows c..ce of columns c..cend).
+struct BidiagChase {
+    static constexpr int kUnits = 2;
+    static constexpr int kVecs = 1;
+    __device__ static long long max_col(const PassArgs& P, int r, int h) { return half_max_col(P, r, h); }
+    __device__ static long long min_col(const PassArgs& P, int r, int h) { return half_min_col(P, r, h); }
+    // slot: the buffer slot of column c of this half-step's step (the caller
+    // carries it from step to step, sparing a modulo on the critical path).
+    template <typename T, int WMAX>
+    __device__ static void unit(const PassArgs& P, const ColBuf<T>& cb, int r, int h, int slot, T* vb, T* taub) {
+        const GGeom g = gstep(P, r, h >> 1);
+        const bool full = g.w == WMAX;
+        if ((h & 1) == 0) {
+            if (full) group_right<T, WMAX, true>(cb, g, slot, vb, taub);
+            else group_right<T, WMAX, false>(cb, g, slot, vb, taub);
+        } else {
+            if (full) group_left<T, WMAX, true>(cb, g, slot, vb, taub);
+            else group_left<T, WMAX, false>(cb, g, slot, vb, taub);
+        }
     }
-}
+};
 
 // Warps a group CTA may have (its sweeps plus the loader, the storer and the
 // publisher): a
@@ -375,25 +389,27 @@ __device__ __forceinline__ bool warp_wait(const int* flag, int target, int* stat
 }
 
 // Last column ticks <= ... touch, one sweep per lane: max over the group's
-// sweeps active at tick u of the last column of their half-step.
+// sweeps active at tick u of the last column of their unit.
+template <class Chase>
 __device__ __forceinline__ long long tick_max_col(const PassArgs& P, int r0, int ng, int L, const int* nsteps,
                                                   int u) {
     long long x = -1;
     for (int jj = threadIdx.x & 31; jj < ng; jj += 32) {
         const int h = u - L * jj;
-        if (h >= 0 && h < 2 * nsteps[jj]) x = max(x, half_max_col(P, r0 + jj, h));
+        if (h >= 0 && h < Chase::kUnits * nsteps[jj]) x = max(x, Chase::max_col(P, r0 + jj, h));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
     return x;
 }
 // First column any tick >= u touches (n when none does).
+template <class Chase>
 __device__ __forceinline__ long long tick_min_col(const PassArgs& P, int r0, int ng, int L, const int* nsteps,
                                                   int u) {
     long long a = P.n;
     for (int jj = threadIdx.x & 31; jj < ng; jj += 32) {
         const int h = u - L * jj;
-        if (h < 2 * nsteps[jj]) a = min(a, half_min_col(P, r0 + jj, max(h, 0)));
+        if (h < Chase::kUnits * nsteps[jj]) a = min(a, Chase::min_col(P, r0 + jj, max(h, 0)));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
@@ -402,17 +418,19 @@ __device__ __forceinline__ long long tick_min_col(const PassArgs& P, int r0, int
 
 constexpr int kMaxStages = 10;
 
-// Shared memory of the group kernel: per-sweep reflectors and scalars, then
-// (16-byte aligned) the circular column buffer.
-__host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem) {
-    const size_t head = elem * ((size_t)g * group_v_stride(wmax, (int)elem) + (size_t)((g + 1) & ~1));
+// Shared memory of the group kernel: per-sweep scratch (nvec reflector-sized
+// vectors) and scalars, then (16-byte aligned) the circular column buffer.
+__host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem, int nvec = 1) {
+    const size_t head =
+        elem * ((size_t)g * nvec * group_v_stride(wmax, (int)elem) + (size_t)((g + 1) & ~1));
     return (head + 15) & ~(size_t)15;
 }
 
 // Persistent group kernel: CTAs take groups G = blockIdx.x, + gridDim.x, ...
-// in order; blockDim.x = 32 * (g + 3).
-//   Warps jj < g run sweep r0 + jj, one half-step per tick, and meet at a
-//   named barrier after each tick.
+// in order; blockDim.x = 32 * (g + 3).  Chase: the chase it runs (units,
+// their columns and their arithmetic; BidiagChase above).
+//   Warps jj < g run sweep r0 + jj, one unit per tick, and meet at a named
+//   barrier after each tick.
 //   Warp g (the loader) copies in the columns tick u first needs, one bulk
 //   (TMA) copy per column, once group G - 1's watermark is beyond them and
 //   the storer has freed their slots; full[u mod S] completes when the bytes
@@ -432,7 +450,7 @@ __host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem
 // the same tick, the other roles leave theirs, and the CTA returns after one
 // last barrier.  Requires band, ldab * sizeof(T) and top * sizeof(T) 16-byte
 // aligned and n < 2^30 (32-bit geometry).
-template <typename T, int WMAX>
+template <typename T, int WMAX, class Chase = BidiagChase>
 __global__ void __launch_bounds__(32 * GroupMaxWarps<T, WMAX>::value)
 pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restrict__ wm,
                   int* __restrict__ status) {
@@ -445,11 +463,12 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     __shared__ int s_written;     // storer: columns < s_written are written back and complete
     __shared__ volatile int s_abort_tick;  // first tick the CTA does not run
     __shared__ volatile int s_dead;  // a warp gave up waiting on a signal that never came
-    constexpr int VS = group_v_stride(WMAX, (int)sizeof(T));
+    constexpr int U = Chase::kUnits;
+    constexpr int VS = Chase::kVecs * group_v_stride(WMAX, (int)sizeof(T));
     T* vbuf = reinterpret_cast<T*>(smem_raw);  // [g][VS], 16-byte aligned rows
     T* taubuf = vbuf + (size_t)GA.g * VS;      // [g]
     ColBuf<T> cb;
-    cb.cols = reinterpret_cast<T*>(smem_raw + group_cols_offset(GA.g, WMAX, sizeof(T)));
+    cb.cols = reinterpret_cast<T*>(smem_raw + group_cols_offset(GA.g, WMAX, sizeof(T), Chase::kVecs));
     cb.base = sh_addr(cb.cols);
     cb.nslot = GA.nslot;
     cb.lds = GA.lds;
@@ -479,16 +498,16 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
         __syncthreads();
         if ((int)threadIdx.x < ng) s_nsteps[threadIdx.x] = sweep_steps(P, r0 + threadIdx.x);
         if (threadIdx.x == 0) {
-            s_freed = r0 + P.bp;
+            s_freed = (int)Chase::min_col(P, r0, 0);  // the group's first column
             s_retired = -1;
             s_written = -1;
         }
         __syncthreads();
         int tend = 0;
-        for (int jj = 0; jj < ng; ++jj) tend = max(tend, L * jj + 2 * s_nsteps[jj]);
+        for (int jj = 0; jj < ng; ++jj) tend = max(tend, L * jj + U * s_nsteps[jj]);
         if (warp < GA.g) {
             // ---- compute warps ----
-            const int my_h_end = (warp < ng) ? 2 * s_nsteps[warp] : 0;
+            const int my_h_end = (warp < ng) ? U * s_nsteps[warp] : 0;
             // slot of column c of this warp's current step: one modulo per
             // group, then + b per step (one wrap when nslot > b, as the
             // footprint of a whole step gives; the loop keeps it exact anyway)
@@ -506,12 +525,13 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 const int h = tau - L * warp;
                 if (!s_dead && h >= 0 && h < my_h_end) {
                     if (my_slot < 0) {
-                        my_slot = cb.slot(r0 + warp + P.bp + (h >> 1) * P.b);
-                    } else if ((h & 1) == 0) {
+                        my_slot = cb.slot(r0 + warp + P.bp + (h / U) * P.b);
+                    } else if (h % U == 0) {
                         my_slot += P.b;
                         while (my_slot >= cb.nslot) my_slot -= cb.nslot;
                     }
-                    group_half<T, WMAX>(P, cb, r0 + warp, h, my_slot, vbuf + (size_t)warp * VS, taubuf + warp);
+                    Chase::template unit<T, WMAX>(P, cb, r0 + warp, h, my_slot, vbuf + (size_t)warp * VS,
+                                                  taubuf + warp);
                     // the storer's bulk copies read these columns through the async proxy
                     if (GA.bulk_store) fence_proxy_async_smem();
                 }
@@ -526,7 +546,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
             }
         } else if (warp == GA.g) {
             // ---- loader ----
-            long long B = (long long)r0 + P.bp - 1;  // last column copied in
+            long long B = Chase::min_col(P, r0, 0) - 1;  // last column copied in
             int seen = (G == 0) ? 0x7fffffff : -1;
             int stage = (int)(T0 % (unsigned)S);
             for (int u = 0; u < tend; ++u) {
@@ -546,7 +566,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                 };
                 // stay within `ahead` ticks of the storer (mbarrier phases)
                 if (u - GA.ahead - 1 >= 0) ok = storer_done(u - GA.ahead - 1);
-                const long long xn = ok ? tick_max_col(P, r0, ng, L, s_nsteps, u) : -1;
+                const long long xn = ok ? tick_max_col<Chase>(P, r0, ng, L, s_nsteps, u) : -1;
                 if (ok && xn > B) {
                     // slots of the columns xn - nslot + 1 .. xn must be free: wait
                     // for the storer's next ticks (at most up to tick u - 1)
@@ -586,7 +606,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
             }
         } else if (warp == GA.g + 1) {
             // ---- storer ----
-            long long A = (long long)r0 + P.bp;  // first column not yet written back
+            long long A = Chase::min_col(P, r0, 0);  // first column not yet written back
             long long xr = -1;                   // last column ticks <= v touch
             int a_prev = (int)A;                 // A before this iteration's write-backs
             bool stopped = false;
@@ -606,8 +626,9 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                     stage = 0;
                     phase ^= 1u;
                 }
-                xr = max(xr, tick_max_col(P, r0, ng, L, s_nsteps, v));
-                long long an = (v == tend - 1) ? (long long)P.n : tick_min_col(P, r0, ng, L, s_nsteps, v + 1);
+                xr = max(xr, tick_max_col<Chase>(P, r0, ng, L, s_nsteps, v));
+                long long an =
+                    (v == tend - 1) ? (long long)P.n : tick_min_col<Chase>(P, r0, ng, L, s_nsteps, v + 1);
                 an = min(an, xr + 1);
                 if (GA.bulk_store) {
                     if (an > A) {

@@ -37,17 +37,25 @@ struct LaunchStats {
     int group = 0;         // sweeps per group (group kernel)
 };
 
-// Shared memory of the group kernel: per-sweep reflectors and scalars, then
+// The chase a group kernel runs: the bidiagonal one (BidiagChase, two
+// half-steps per step) or the symmetric one (SymChase in bb_sym_group.cuh,
+// one two-sided step; lower band storage).
+enum class ChaseKind { kBidiag = 0, kSym = 1 };
+// Reflector-sized vectors of shared scratch per sweep (Chase::kVecs).
+inline int chase_vecs(ChaseKind kind) { return kind == ChaseKind::kSym ? 2 : 1; }
+
+// Shared memory of the group kernel: per-sweep scratch and scalars, then
 // the circular column buffer.
-inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem) {
-    return group_cols_offset(GA.g, wmax, elem) + elem * (size_t)GA.nslot * GA.lds;
+inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem, int nvec = 1) {
+    return group_cols_offset(GA.g, wmax, elem, nvec) + elem * (size_t)GA.nslot * GA.lds;
 }
 
 // Largest group (<= requested, or the most the kernel is compiled for when
 // requested == 0) whose column buffer fits in shared memory; false if not
 // even one sweep fits.  The kernel then needs the band and ldab * elem
 // 16-byte aligned (group_layout_ok).
-bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out);
+bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out,
+                ChaseKind kind = ChaseKind::kBidiag);
 
 // Whether the group kernel's bulk copies can address this band storage.
 inline bool group_layout_ok(const void* band, long long ldab, size_t elem) {
@@ -89,7 +97,7 @@ constexpr int kGroupAhead = 3;
 // Columns the group starting at sweep 0 holds at most when its loader runs
 // `ahead` ticks ahead (the buffer size the group kernel needs; groups further
 // down the matrix hold no more).
-int group_footprint(const PassArgs& P, int g, int ahead);
+int group_footprint(const PassArgs& P, int g, int ahead, ChaseKind kind = ChaseKind::kBidiag);
 
 // One pass of the reduction on `stream`.  scheduler 0: persistent kernel
 // (cooperative launch); 1: one launch per cycle.

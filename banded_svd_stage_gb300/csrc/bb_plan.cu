@@ -24,7 +24,7 @@ int pass_lag_half(int b, int t) {
 // R + n*BW > R + 1 + BW + TW holds for n = 2 when BW > 1 + TW, else n = 3.
 int pass_lag_cycle(int b, int t) { return (b > t + 1) ? 2 : 3; }
 
-int group_footprint(const PassArgs& P, int g, int ahead) {
+int group_footprint(const PassArgs& P, int g, int ahead, ChaseKind kind) {
     // Replays the group kernel's buffer bookkeeping for the group at sweep 0:
     // the loader copies in tick u's columns once the storer has written back
     // what ticks < u - ahead alone touch, so the buffer holds the columns from
@@ -33,27 +33,33 @@ int group_footprint(const PassArgs& P, int g, int ahead) {
     const int ng = (int)std::min<long long>(g, P.nsweeps);
     if (ng <= 0) return 0;
     const int L = P.lagh;
+    const bool sym = kind == ChaseKind::kSym;
+    const int U = sym ? 1 : 2;  // units per step
     auto steps = [&](long long r) -> long long {
         long long last = P.n - 2 - r - P.bp;
         return last < 0 ? 0 : last / P.b + 1;
     };
+    // the columns unit h of sweep r touches (BidiagChase / SymChase)
     auto maxcol = [&](long long r, long long h) -> long long {
-        const long long k = h >> 1;
+        const long long k = h / U;
         const long long c = r + P.bp + k * P.b;
         const long long ce = std::min(c + P.t, P.n - 1);
-        return (h & 1) ? std::min(ce + P.b, P.n - 1) : ce;
+        return (!sym && (h & 1)) ? std::min(ce + P.b, P.n - 1) : ce;
     };
-    auto mincol = [&](long long r, long long h) -> long long { return r + P.bp + (h >> 1) * P.b; };
+    auto mincol = [&](long long r, long long h) -> long long {
+        if (sym) return h == 0 ? r : r + P.bp + (h - 1) * P.b;
+        return r + P.bp + (h >> 1) * P.b;
+    };
     long long tend = 0;
-    for (int jj = 0; jj < ng; ++jj) tend = std::max(tend, (long long)L * jj + 2 * steps(jj));
+    for (int jj = 0; jj < ng; ++jj) tend = std::max(tend, (long long)L * jj + U * steps(jj));
     std::vector<long long> xrun(tend), amin(tend);
     long long x = -1;
     for (long long tau = 0; tau < tend; ++tau) {
         long long a = P.n;
         for (int jj = 0; jj < ng; ++jj) {
             const long long h = tau - (long long)L * jj;
-            if (h >= 0 && h < 2 * steps(jj)) x = std::max(x, maxcol(jj, h));
-            if (h < 2 * steps(jj)) a = std::min(a, mincol(jj, std::max(h, 0LL)));
+            if (h >= 0 && h < U * steps(jj)) x = std::max(x, maxcol(jj, h));
+            if (h < U * steps(jj)) a = std::min(a, mincol(jj, std::max(h, 0LL)));
         }
         xrun[tau] = x;
         amin[tau] = a;
@@ -67,8 +73,9 @@ int group_footprint(const PassArgs& P, int g, int ahead) {
     return (int)fp;
 }
 
-bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out) {
+bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out, ChaseKind kind) {
     const size_t budget = 220 * 1024;
+    const int nvec = chase_vecs(kind);
     GroupArgs best{};
     const int gcap = group_max_warps(wmax, elem);
     const int gmax = requested > 0 ? std::min(requested, gcap) : gcap;
@@ -76,19 +83,22 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
         GroupArgs ga;
         ga.g = g;
         ga.ngroups = (int)((P.nsweeps + g - 1) / g);
-        // rows top .. top + lds - 1 hold the pass's rows ku-b-t .. ku+t, both
+        // rows top .. top + lds - 1 hold the pass's rows (ku-b-t .. ku+t of
+        // the upper band; ku .. ku+b+t of the lower, symmetric band), both
         // ends rounded out to 16 bytes (the extra rows are ones the pass
         // leaves alone: copied in and written back unchanged)
         const int q = (int)(16 / elem);
-        ga.top = (P.ku - P.b - P.t) / q * q;
-        ga.lds = (P.ku + P.t + 1 - ga.top + q - 1) / q * q;
+        const int lo = (kind == ChaseKind::kSym) ? P.ku : P.ku - P.b - P.t;
+        const int hi = (kind == ChaseKind::kSym) ? P.ku + P.b + P.t : P.ku + P.t;
+        ga.top = lo / q * q;
+        ga.lds = (hi + 1 - ga.top + q - 1) / q * q;
         ga.ahead = kGroupAhead;
         // wide columns go back with bulk copies (one instruction a column);
         // narrow ones with plain copies, which spare the compute warps a
         // proxy fence every tick
         ga.bulk_store = ((size_t)ga.lds * elem >= 256) ? 1 : 0;
-        ga.nslot = std::max(1, group_footprint(P, g, ga.ahead));
-        if (group_smem_bytes(ga, wmax, elem) > budget) break;
+        ga.nslot = std::max(1, group_footprint(P, g, ga.ahead, kind));
+        if (group_smem_bytes(ga, wmax, elem, nvec) > budget) break;
         best = ga;
         if (requested > 0 && g == requested) break;
     }
@@ -100,8 +110,8 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
     for (int a = best.ahead + 1; a <= kMaxStages - 2; ++a) {
         GroupArgs ga = best;
         ga.ahead = a;
-        ga.nslot = std::max(1, group_footprint(P, ga.g, a));
-        if (group_smem_bytes(ga, wmax, elem) > budget) break;
+        ga.nslot = std::max(1, group_footprint(P, ga.g, a, kind));
+        if (group_smem_bytes(ga, wmax, elem, nvec) > budget) break;
         best = ga;
     }
     *out = best;

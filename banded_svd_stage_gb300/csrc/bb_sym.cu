@@ -16,11 +16,19 @@
 //   from the right to rows ce+1 .. cend, columns c..ce.
 // Storage: A(i, j), i >= j, at band[(i - j) + j * ldab], ldab >= bw + tw + 1.
 //
-// Scheduler: one CTA per sweep (persistent, cooperative launch), sweep r
-// taking step k once sweep r-1 has finished min(k + L, K_{r-1}) steps, the
-// last step once all of sweep r-1 is done; L = 2, or 3 when b - t = 1, the
-// least lag for which overlapping steps of consecutive sweeps stay in sweep
-// order.  Band data another CTA wrote is read through L2 (ld.global.cg).
+// Schedulers, per pass:
+// - the flag kernel here: one CTA per sweep (persistent, cooperative
+//   launch), sweep r taking step k once sweep r-1 has finished
+//   min(k + L, K_{r-1}) steps, the last step once all of sweep r-1 is done;
+//   L = 2, or 3 when b - t = 1, the least lag for which overlapping steps of
+//   consecutive sweeps stay in sweep order.  Band data another CTA wrote is
+//   read through L2 (ld.global.cg);
+// - the group kernel (bb_sym_group.cuh): g sweeps per CTA in lockstep with
+//   the same lag, their columns in shared memory, whole columns handed from
+//   group to group.  Chosen where at least kAutoGroupMin sweeps fit shared
+//   memory (or wherever one fits, on request), for reflectors of up to 33
+//   elements.
+// Both give bitwise equal results.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -28,13 +36,29 @@
 #include "bb_device.cuh"
 #include "bb_internal.h"
 #include "bb_sym.h"
+#include "bb_sym_group.cuh"
 
 namespace bb {
+
+BB_SYM_GROUP_EXTERN(float, 9) BB_SYM_GROUP_EXTERN(float, 17) BB_SYM_GROUP_EXTERN(float, 33)
+BB_SYM_GROUP_EXTERN(double, 9) BB_SYM_GROUP_EXTERN(double, 17) BB_SYM_GROUP_EXTERN(double, 33)
 
 constexpr int kSymThreads = 256;
 
 // Step lag of the symmetric variant in pass (b, t).
 int sym_pass_lag(int b, int t) { return (b - t >= 2) ? 2 : 3; }
+
+bool sym_choose_group(const PassArgs& P, int scheduler, int group_size, size_t elem, GroupArgs* out) {
+    if (scheduler != 0 && scheduler != 3) return false;
+    if (P.nsweeps <= 0 || P.n >= kGroupMaxN) return false;
+    const int wmax = sym_group_wmax(P.t + 1);
+    if (wmax == 0) return false;
+    GroupArgs ga;
+    if (!plan_group(P, wmax, elem, group_size, &ga, ChaseKind::kSym)) return false;
+    if (scheduler == 0 && ga.g < kAutoGroupMin) return false;
+    if (out) *out = ga;
+    return true;
+}
 
 template <typename T>
 __device__ __forceinline__ T sym_ld(const T* band, long long ld, long long i, long long j) {
@@ -134,12 +158,10 @@ __device__ __forceinline__ void sym_step(T* __restrict__ band, const PassArgs& P
     // 0 <= q <= u < w, entry e = u (u + 1) / 2 + q
     const int npairs = w * (w + 1) / 2;
     for (int e = threadIdx.x; e < npairs; e += blockDim.x) {
-        int u = (int)((sqrtf(8.f * (float)e + 1.f) - 1.f) * 0.5f);
-        while (u * (u + 1) / 2 > e) --u;
-        while ((u + 1) * (u + 2) / 2 <= e) ++u;
-        const int q = e - u * (u + 1) / 2;
+        int u, q;
+        sym_pair(e, u, q);
         const T a = sym_ld(band, ld, c + u, c + q);
-        sym_st(band, ld, c + u, c + q, a - s_v[u] * s_x[q] - s_x[u] * s_v[q]);
+        sym_st(band, ld, c + u, c + q, sym_rank2(a, s_v[u], s_x[q], s_x[u], s_v[q]));
     }
 }
 
@@ -215,11 +237,42 @@ static cudaError_t run_sym_pass(T* band, const PassArgs& P, int num_sms, int max
     return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(kSymThreads), args, 0, s);
 }
 
+// The pass arguments of pass (b, t) of the symmetric chase.
+static PassArgs sym_pass_args(long long n, long long ldab, int b, int t, const SymLaunch& L) {
+    PassArgs P{};
+    P.n = n;
+    P.ldab = ldab;
+    P.b = b;
+    P.t = t;
+    P.bp = b - t;
+    P.ku = 0;
+    P.nsweeps = (int)std::max<long long>(0, n - (b - t) - 1);
+    P.lag = sym_pass_lag(b, t);
+    P.lagh = P.lag;
+    P.stall_sweep = L.stall_sweep;
+    P.wait_budget = L.wait_budget;
+    return P;
+}
+
+bool sym_any_group(long long n, int bw, int tw, const SymLaunch& L, size_t elem) {
+    for (int b = bw; b > 1;) {
+        const int t = std::min(tw, b - 1);
+        if (sym_choose_group(sym_pass_args(n, 0, b, t, L), L.scheduler, L.group_size, elem, nullptr)) return true;
+        b -= t;
+    }
+    return false;
+}
+
 template <typename T>
 cudaError_t run_sym(T* band, long long n, long long ldab, int bw, int tw, T* d, T* e, const SymLaunch& L,
-                    cudaStream_t s, long long* launches) {
+                    cudaStream_t s, long long* launches, SymPassStats* stats) {
     cudaError_t err = cudaSuccess;
     long long nl = 0;
+    if (stats) {
+        stats->kernel.clear();
+        stats->group.clear();
+    }
+    const bool layout_ok = group_layout_ok(band, ldab, sizeof(T));
     if (n * (long long)tw > 0) {
         const long long total = n * (long long)tw;
         const unsigned grid = (unsigned)std::min<long long>((total + 255) / 256, 4LL * L.num_sms);
@@ -230,23 +283,27 @@ cudaError_t run_sym(T* band, long long n, long long ldab, int bw, int tw, T* d, 
     int b = bw;
     while (err == cudaSuccess && b > 1) {
         const int t = std::min(tw, b - 1);
-        PassArgs P{};
-        P.n = n;
-        P.ldab = ldab;
-        P.b = b;
-        P.t = t;
-        P.bp = b - t;
-        P.ku = 0;
-        P.nsweeps = (int)std::max<long long>(0, n - (b - t) - 1);
-        P.lag = sym_pass_lag(b, t);
-        P.lagh = P.lag;
-        P.stall_sweep = L.stall_sweep;
-        P.wait_budget = L.wait_budget;
+        const PassArgs P = sym_pass_args(n, ldab, b, t, L);
         const int w = t + 1;
-        if (w <= 32) err = run_sym_pass<T, 32>(band, P, L.num_sms, L.max_ctas, L.progress, L.status, s);
-        else if (w <= 64) err = run_sym_pass<T, 64>(band, P, L.num_sms, L.max_ctas, L.progress, L.status, s);
-        else err = run_sym_pass<T, 96>(band, P, L.num_sms, L.max_ctas, L.progress, L.status, s);
+        GroupArgs ga{};
+        const bool grp = layout_ok && sym_choose_group(P, L.scheduler, L.group_size, sizeof(T), &ga);
+        if (grp) {
+            const int wmax = sym_group_wmax(w);
+            auto launch = (wmax == 9) ? run_sym_group_pass<T, 9>
+                                      : (wmax == 17) ? run_sym_group_pass<T, 17> : run_sym_group_pass<T, 33>;
+            err = launch(band, P, ga, L.num_sms, L.max_ctas, L.progress, L.status, s);
+        } else if (w <= 32) {
+            err = run_sym_pass<T, 32>(band, P, L.num_sms, L.max_ctas, L.progress, L.status, s);
+        } else if (w <= 64) {
+            err = run_sym_pass<T, 64>(band, P, L.num_sms, L.max_ctas, L.progress, L.status, s);
+        } else {
+            err = run_sym_pass<T, 96>(band, P, L.num_sms, L.max_ctas, L.progress, L.status, s);
+        }
         if (P.nsweeps > 0) ++nl;
+        if (stats) {
+            stats->kernel.push_back(grp ? 3 : 2);
+            stats->group.push_back(grp ? ga.g : 0);
+        }
         b -= t;
     }
     if (err == cudaSuccess) {
@@ -260,8 +317,8 @@ cudaError_t run_sym(T* band, long long n, long long ldab, int bw, int tw, T* d, 
 }
 
 template cudaError_t run_sym<float>(float*, long long, long long, int, int, float*, float*, const SymLaunch&,
-                                    cudaStream_t, long long*);
+                                    cudaStream_t, long long*, SymPassStats*);
 template cudaError_t run_sym<double>(double*, long long, long long, int, int, double*, double*,
-                                     const SymLaunch&, cudaStream_t, long long*);
+                                     const SymLaunch&, cudaStream_t, long long*, SymPassStats*);
 
 }  // namespace bb

@@ -171,10 +171,22 @@ int64_t bb_get_param(const bb_handle* h, int param);
  *   tw       1 <= tw <= max(1, bw - 1), tw <= 64
  *   d_out    device, n entries: the diagonal; e_out device, n - 1 entries:
  *            the subdiagonal (may be null when n == 1)
- * Stream-ordered and asynchronous like bb_reduce; one CTA per sweep with the
- * handle's progress counters (step k of sweep r after sweep r-1 finished
- * min(k + L, its steps), L = 2, or 3 when b - t = 1); device-side failures
- * are reported by bb_status_sync. */
+ * Stream-ordered and asynchronous like bb_reduce.  Schedulers, per pass
+ * (BB_PARAM_SCHEDULER; BB_PARAM_GROUP_SIZE, BB_PARAM_MAX_CTAS,
+ * BB_PARAM_WAIT_BUDGET_MS and BB_PARAM_STALL_SWEEP apply as for bb_reduce):
+ *   flag kernel: one CTA per sweep with the handle's progress counters (step
+ *     k of sweep r after sweep r-1 finished min(k + L, its steps), L = 2, or
+ *     3 when b - t = 1);
+ *   group kernel: g sweeps per CTA in lockstep with the same lag, their
+ *     columns in shared memory (bb_sym_group_plan); it takes a pass with a
+ *     reflector of at most 33 elements on a band whose base and ldab *
+ *     element size are multiples of 16 bytes: under scheduler 0 (default)
+ *     where at least 5 sweeps fit, under 3 wherever one fits; every other
+ *     pass, and every pass under schedulers 1, 2 and 4, runs on the flag
+ *     kernel.
+ * Both give bitwise equal results; bb_last_pass_kernel / bb_last_pass_group
+ * report the choice (2 or 3) per pass.  Device-side failures are reported
+ * by bb_status_sync. */
 bb_status bb_sym_reduce(bb_handle* h, void* band_ptr, int64_t ldab, int64_t tw, void* d_out, void* e_out,
                         bb_stream_t stream);
 int64_t bb_sym_required_ldab(int64_t bw, int64_t tw);
@@ -208,6 +220,13 @@ bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t
  * plan, elem_bytes is 4 or 8 and group_size >= 0. */
 bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
                         int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds);
+
+/* As bb_group_plan, for the symmetric chase of bb_sym_reduce (lower band
+ * storage, one two-sided step per tick): g = 0 when its group kernel cannot
+ * take the pass (no group fits shared memory, or a reflector of more than 33
+ * elements).  Same arguments and errors. */
+bb_status bb_sym_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass,
+                            int64_t group_size, int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds);
 
 /* Algorithmic bytes of pass i (or of all passes when i < 0) of an n x n
  * reduction with element size elem_bytes: every element of each step's right

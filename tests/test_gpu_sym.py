@@ -34,7 +34,9 @@ def sym_fro(sb, n):
     return float(np.sqrt((a[:, 0] ** 2).sum() + 2 * (a[:, 1:] ** 2).sum()))
 
 
-def gpu_sym(sb, n, bw, tw, dt, params=None, return_band=False):
+def gpu_sym(sb, n, bw, tw, dt, params=None, return_band=False, kernels=None):
+    """bb_sym_reduce of the lower band sb on cuda:0: (d, e[, band after]).
+    kernels: a list that receives (kernel, group size) of every pass."""
     dev = torch.device("cuda:0")
     x = torch.from_numpy(np.ascontiguousarray(sb)).to(dev)
     d = torch.empty(n, dtype=x.dtype, device=dev)
@@ -47,6 +49,9 @@ def gpu_sym(sb, n, bw, tw, dt, params=None, return_band=False):
         bb.bb_sym_reduce(h, x, sb.shape[1], tw, d, e, s)
         st = bb.bb_status_sync(h, s)
         assert st == bb.BB_OK, f"device status {st}: {bb.bb_last_error()}"
+        if kernels is not None:
+            kernels.extend((bb.bb_last_pass_kernel(h, i), bb.bb_last_pass_group(h, i))
+                           for i in range(bb.bb_last_num_passes(h)))
     finally:
         bb.bb_destroy(h)
     out = (d.cpu().numpy(), e[: max(n - 1, 0)].cpu().numpy())
@@ -94,6 +99,64 @@ def test_larger_bands(n, bw, tw, dt):
     check(bi.make_sym_band(n, bw, tw, dt, "uniform", seed=n + bw), n, bw, tw, dt)
 
 
+# Shapes for the group kernel: one and several groups, ragged last groups,
+# reflectors of 8, 9, 17 and 33 elements (the compiled widths and a
+# predicated one), passes with b - t = 1 (lag 3), float and double.
+GROUP_CASES = [(40, 8, 7, "f64"), (64, 16, 8, "f32"), (129, 9, 8, "f64"), (257, 8, 7, "f32"),
+               (300, 40, 12, "f64"), (500, 24, 7, "f32"), (1000, 64, 16, "f32"), (700, 48, 16, "f64"),
+               (600, 96, 32, "f32"), (400, 66, 32, "f64"), (2000, 16, 8, "f32"), (1500, 32, 8, "f64")]
+
+
+@pytest.mark.parametrize("n,bw,tw,dt", GROUP_CASES)
+def test_group_kernel_bitwise_equals_flag_kernel(n, bw, tw, dt):
+    """The two schedulers run the same arithmetic in the same order per
+    entry: any difference is a race or a lost update."""
+    sb = bi.make_sym_band(n, bw, tw, dt, seed=7 * n + bw)
+    kf, kg = [], []
+    d2, e2, b2 = gpu_sym(sb, n, bw, tw, dt, {bb.BB_PARAM_SCHEDULER: 2}, return_band=True, kernels=kf)
+    d3, e3, b3 = gpu_sym(sb, n, bw, tw, dt, {bb.BB_PARAM_SCHEDULER: 3}, return_band=True, kernels=kg)
+    assert all(k == 2 for k, _ in kf)
+    planned = [bb.bb_sym_group_plan(n, bw, tw, 4 if dt == "f32" else 8, p)[0] for p in range(len(kg))]
+    assert [k for k, _ in kg] == [3 if g > 0 else 2 for g in planned]
+    assert any(k == 3 for k, _ in kg)
+    record("sym_group_vs_flag", n=n, bw=bw, tw=tw, dt=dt, kernels=kg)
+    assert np.array_equal(d2, d3) and np.array_equal(e2, e3)
+    assert np.array_equal(b2, b3)
+
+
+@pytest.mark.parametrize("group_size,max_ctas", [(1, 0), (2, 3), (5, 1), (13, 2), (7, 0)])
+def test_group_kernel_group_sizes_and_grid_caps(group_size, max_ctas):
+    """Groups of any size, and fewer CTAs than groups (each CTA then runs
+    several groups in turn and waits on other CTAs' watermarks)."""
+    n, bw, tw, dt = 700, 16, 8, "f32"
+    sb = bi.make_sym_band(n, bw, tw, dt, seed=11)
+    ref = gpu_sym(sb, n, bw, tw, dt, {bb.BB_PARAM_SCHEDULER: 2}, return_band=True)
+    ks = []
+    got = gpu_sym(sb, n, bw, tw, dt, {bb.BB_PARAM_SCHEDULER: 3, bb.BB_PARAM_GROUP_SIZE: group_size,
+                                      bb.BB_PARAM_MAX_CTAS: max_ctas}, return_band=True, kernels=ks)
+    assert ks == [(3, group_size)] * len(ks)
+    for a, b in zip(ref, got):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("n,bw,tw,dt", [(1000, 64, 16, "f32"), (700, 48, 16, "f64"), (2000, 16, 8, "f32")])
+def test_group_kernel_parity(n, bw, tw, dt):
+    check(bi.make_sym_band(n, bw, tw, dt, seed=n + 3 * bw), n, bw, tw, dt, {bb.BB_PARAM_SCHEDULER: 3})
+
+
+def test_automatic_scheduler_takes_the_group_kernel():
+    # the main workload's shape: both passes on the group kernel, 13 sweeps
+    # per group; ldab = bw + tw + 1 is not a multiple of 16 bytes, so the
+    # handle's aligned working copy is used (and the band is copied back)
+    n, bw, tw, dt = 4096, 16, 8, "f32"
+    sb = bi.make_sym_band(n, bw, tw, dt, seed=5)
+    ks = []
+    d, e, after = gpu_sym(sb, n, bw, tw, dt, return_band=True, kernels=ks)
+    assert ks == [(3, 13), (3, 13)]
+    d2, e2, after2 = gpu_sym(sb, n, bw, tw, dt, {bb.BB_PARAM_SCHEDULER: 2}, return_band=True)
+    assert np.array_equal(d, d2) and np.array_equal(e, e2) and np.array_equal(after, after2)
+
+
 @pytest.mark.parametrize("max_ctas", [1, 3, 17])
 def test_fewer_ctas_than_sweeps(max_ctas):
     # CTAs take several sweeps each and wait on sweeps of other CTAs
@@ -118,7 +181,11 @@ def test_prescribed_eigenvalues(kind, dt):
     assert np.abs(got - np.sort(lam)).max() <= TOL[dt] * np.abs(lam).max()
 
 
-def test_stalled_sweep_times_out_and_context_survives():
+@pytest.mark.parametrize("scheduler", [2, 3])
+def test_stalled_sweep_times_out_and_context_survives(scheduler):
+    """A sweep (flag kernel) or the group holding it (group kernel) that
+    never reports progress: the waits give up, the status says so, and the
+    context runs the next reduction."""
     n, bw, tw = 800, 16, 8
     sb = bi.make_sym_band(n, bw, tw, "f32", seed=2)
     dev = torch.device("cuda:0")
@@ -127,11 +194,13 @@ def test_stalled_sweep_times_out_and_context_survives():
     e = torch.empty(n - 1, dtype=torch.float32, device=dev)
     h = bb.bb_create(n, bw, bb.BB_F32)
     try:
+        bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, scheduler)
         bb.bb_set_param(h, bb.BB_PARAM_WAIT_BUDGET_MS, 50)
         bb.bb_set_param(h, bb.BB_PARAM_STALL_SWEEP, 5)
         s = torch.cuda.current_stream(dev)
         bb.bb_sym_reduce(h, x, sb.shape[1], tw, d, e, s)
         assert bb.bb_status_sync(h, s) == bb.BB_ERR_TIMEOUT
+        assert bb.bb_last_pass_kernel(h, 0) == scheduler
         bb.bb_set_param(h, bb.BB_PARAM_STALL_SWEEP, -1)
         x.copy_(torch.from_numpy(sb).to(dev))
         bb.bb_sym_reduce(h, x, sb.shape[1], tw, d, e, s)
