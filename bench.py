@@ -291,10 +291,16 @@ def run_sym(w: bi.Workload, steps: int, warmup: int):
                 raise RuntimeError("symmetric reduction failed: " + bb.bb_last_error())
             if i >= warmup:
                 times.append(ev0.elapsed_time(ev1))
+        # per pass: the group kernel (its sweeps per CTA) or the flag kernel
+        names = {2: "sym_pass_kernel", 3: "pass_group_kernel<SymChase>"}
+        kernels = [f"{names.get(bb.bb_last_pass_kernel(h, i), '?')}"
+                   + (f" g={bb.bb_last_pass_group(h, i)}" if bb.bb_last_pass_kernel(h, i) == 3 else "")
+                   for i in range(bb.bb_last_num_passes(h))]
+        launches = int(bb.bb_last_launches(h))
     finally:
         bb.bb_destroy(h)
     out = {"ms": statistics.median(times), "n": w.n, "bw": w.bw, "tw": w.tw, "dtype": w.dtype,
-           "kernel": "sym_pass_kernel", "launches": int(bb.bb_num_passes(w.bw, w.tw)) + 2}
+           "kernels": kernels, "launches": launches}
     try:
         import oracle
         cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
