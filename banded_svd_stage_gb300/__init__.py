@@ -78,7 +78,7 @@ def lib() -> ctypes.CDLL:
             "bb_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
             "bb_sym_group_plan": ([i64, i64, i64, i64, i64, i64] + [ctypes.POINTER(i64)] * 4, ci),
             "bb_sym_reduce": ([p, p, i64, i64, p, p, p], ci),
-            "bb_dense_to_band_workspace": ([i64, ci], i64),
+            "bb_dense_to_band_workspace": ([i64, i64, ci], i64),
             "bb_dense_to_band": ([ci, i64, i64, p, i64, p, i64, p], ci),
             "bb_pack_band": ([ci, i64, i64, i64, p, i64, p, i64, p], ci),
             "bb_sym_required_ldab": ([i64, i64], i64),
@@ -239,8 +239,9 @@ def bb_sym_reduce(h, band, ldab: int, tw: int, d, e, stream=None) -> None:
     _check(lib().bb_sym_reduce(h, _addr(band), ldab, tw, _addr(d), _addr(e), _stream(stream)))
 
 
-def bb_dense_to_band_workspace(n: int, dtype: int) -> int:
-    return lib().bb_dense_to_band_workspace(n, dtype)
+def bb_dense_to_band_workspace(n: int, bw: int, dtype: int) -> int:
+    """Bytes of device workspace bb_dense_to_band needs (-1: invalid)."""
+    return lib().bb_dense_to_band_workspace(n, bw, dtype)
 
 
 def bb_dense_to_band(dtype: int, n: int, bw: int, a, lda: int, workspace, workspace_bytes: int, stream=None) -> None:

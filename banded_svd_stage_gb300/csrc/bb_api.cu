@@ -147,7 +147,7 @@ bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, i
                         int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds) {
     if (n < 1 || n >= bb::kGroupMaxN || bw < 0 || bw >= n || tw < 1 || tw > std::max<int64_t>(1, bw - 1) ||
         pass < 0 || pass >= count_passes(bw, tw) || !g || !nslot || !ahead || !lds ||
-        (elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
+        (elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
         return fail(BB_ERR_INVALID_ARG, "bb_group_plan: argument out of range");
     try {
         const PassPlan ps = pass_at(bw, tw, pass);
@@ -160,8 +160,12 @@ bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, i
         P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
         P.lagh = bb::pass_lag_half(P.b, P.t);
         bb::GroupArgs ga{};
-        const bool ok = P.nsweeps > 0 &&
-                        bb::plan_group(P, bb::wmax_bucket(P.t + 1), (size_t)elem_bytes, (int)group_size, &ga);
+        bool ok;
+        if (elem_bytes == 2)  // binary16 storage, float arithmetic
+            ok = bb::half_choose_group(P, 3, (int)group_size, &ga);
+        else
+            ok = P.nsweeps > 0 &&
+                 bb::plan_group(P, bb::wmax_bucket(P.t + 1), (size_t)elem_bytes, (int)group_size, &ga);
         *g = ok ? ga.g : 0;
         *nslot = ok ? ga.nslot : 0;
         *ahead = ok ? ga.ahead : 0;
@@ -616,10 +620,10 @@ static bb_status reduce_impl(bb_handle* h, T* band, int64_t ldab, int64_t tw, T*
     return BB_OK;
 }
 
-// Binary16 storage (float arithmetic): one persistent kernel per pass, the
-// flag kernel's progress protocol (bb_half.cu).  The scheduler parameter
-// does not apply; the pass range, timing, grid cap, wait budget and fault
-// injection do.
+// Binary16 storage (float arithmetic), per pass the group kernel with
+// binary16 columns (where the scheduler rule of bb_reduce picks it) or the
+// binary16 flag kernel (bb_half.cu).  The pass range, timing, grid cap, wait
+// budget, group size and fault injection apply.
 static bb_status half_reduce(bb_handle* h, void* band, int64_t ldab, int64_t tw, void* d, void* e,
                              cudaStream_t s) {
     const int64_t n = h->n;
@@ -633,8 +637,51 @@ static bb_status half_reduce(bb_handle* h, void* band, int64_t ldab, int64_t tw,
     const int64_t np = count_passes(h->bw, tw);
     const int64_t lo = std::max<int64_t>(0, h->pass_lo);
     const int64_t hi = std::min<int64_t>(np, h->pass_hi);
+    const int sched = h->scheduler;
+    auto pass_args = [&](int64_t pi, int64_t ld) {
+        const PassPlan ps = pass_at(h->bw, tw, pi);
+        bb::PassArgs P;
+        P.n = n;
+        P.ldab = ld;
+        P.b = ps.b;
+        P.t = ps.t;
+        P.bp = ps.b - ps.t;
+        P.ku = ku;
+        P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
+        P.lag = bb::pass_lag_cycle(P.b, P.t);
+        P.lagh = bb::pass_lag_half(P.b, P.t);
+        P.stall_sweep = h->stall_sweep;
+        P.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+        return P;
+    };
+    // The group kernel moves whole columns with bulk copies, which need a
+    // 16-byte aligned column stride: on any other layout the reduction runs
+    // on an aligned working copy (one strided copy in, one out).
+    void* wb = band;
+    int64_t ldw = ldab;
+    bool any_group = false;
+    for (int64_t pi = lo; pi < hi; ++pi)
+        any_group = any_group || bb::half_choose_group(pass_args(pi, ldab), sched, h->group_size, nullptr);
+    const size_t elem = 2;
+    if (any_group && !bb::group_layout_ok(band, ldab, elem)) {
+        const int64_t q = 16 / (int64_t)elem;
+        ldw = (ldab + q - 1) / q * q;
+        const size_t bytes = elem * (size_t)ldw * (size_t)n;
+        if (h->work_bytes < bytes) {
+            if (h->work) cudaFree(h->work);
+            h->work = nullptr;
+            h->work_bytes = 0;
+            err = cudaMalloc(&h->work, bytes);
+            if (err != cudaSuccess) return fail(BB_ERR_NOMEM, "working band allocation failed");
+            h->work_bytes = bytes;
+        }
+        wb = h->work;
+        err = cudaMemcpy2DAsync(wb, elem * ldw, band, elem * ldab, elem * ldab, (size_t)n, cudaMemcpyDeviceToDevice,
+                                s);
+        if (err != cudaSuccess) return cuda_fail(err, "copy to the working band");
+    }
     if (lo == 0) {
-        err = bb::run_half_zero_fill(band, n, ldab, (int)tw, ku, h->num_sms, s);
+        err = bb::run_half_zero_fill(wb, n, ldw, (int)tw, ku, h->num_sms, s);
         if (err != cudaSuccess) return cuda_fail(err, "zero fill launch");
         h->last_launches += 1;
     }
@@ -650,34 +697,31 @@ static bb_status half_reduce(bb_handle* h, void* band, int64_t ldab, int64_t tw,
     bb::HalfLaunch L;
     L.num_sms = h->num_sms;
     L.max_ctas = h->max_ctas;
+    L.scheduler = sched;
+    L.group_size = h->group_size;
     L.progress = h->d_progress;
     L.status = h->d_status;
     for (int64_t pi = lo; pi < hi; ++pi) {
-        const PassPlan ps = pass_at(h->bw, tw, pi);
-        bb::PassArgs P;
-        P.n = n;
-        P.ldab = ldab;
-        P.b = ps.b;
-        P.t = ps.t;
-        P.bp = ps.b - ps.t;
-        P.ku = ku;
-        P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
-        P.lag = bb::pass_lag_cycle(P.b, P.t);
-        P.lagh = bb::pass_lag_half(P.b, P.t);
-        P.stall_sweep = h->stall_sweep;
-        P.wait_budget = (unsigned long long)h->wait_ms * (unsigned long long)h->clock_khz;
+        const bb::PassArgs P = pass_args(pi, ldw);
+        bb::GroupArgs ga{};
+        const bool grp = bb::group_layout_ok(wb, ldw, elem) && bb::half_choose_group(P, sched, h->group_size, &ga);
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo)], s);
-        err = bb::run_half_pass(band, P, L, s);
+        err = bb::run_half_pass(wb, P, L, grp ? &ga : nullptr, s);
         if (h->timing) cudaEventRecord(h->ev[2 * (pi - lo) + 1], s);
         if (err != cudaSuccess) return cuda_fail(err, "pass launch");
         h->last_launches += (P.nsweeps > 0) ? 1 : 0;
         h->last_passes += 1;
-        h->pass_kernel.push_back(5);
-        h->pass_group.push_back(0);
+        h->pass_kernel.push_back(grp ? 3 : 5);
+        h->pass_group.push_back(grp ? ga.g : 0);
     }
-    err = bb::run_half_extract(band, n, ldab, ku, d, e, h->num_sms, s);
+    err = bb::run_half_extract(wb, n, ldw, ku, d, e, h->num_sms, s);
     if (err != cudaSuccess) return cuda_fail(err, "extract launch");
     h->last_launches += 1;
+    if (wb != band) {
+        err = cudaMemcpy2DAsync(band, elem * ldab, wb, elem * ldw, elem * ldab, (size_t)n, cudaMemcpyDeviceToDevice,
+                                s);
+        if (err != cudaSuccess) return cuda_fail(err, "copy back from the working band");
+    }
     return BB_OK;
 }
 

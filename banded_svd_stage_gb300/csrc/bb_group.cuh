@@ -25,6 +25,10 @@
 // the grouping of sweeps per CTA and the column hand-over are this library's.
 #pragma once
 
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "bb_device.cuh"
 
 namespace bb {
@@ -66,6 +70,31 @@ struct ColBuf {
     __device__ __forceinline__ T* col(int j) const { return cols + slot(j) * lds; }
     __device__ __forceinline__ unsigned at(int idx) const { return base + (unsigned)idx * (unsigned)sizeof(T); }
 };
+
+// A buffered entry of storage type ST read as the arithmetic type T, and a
+// T value rounded to ST and stored (ST = T, or binary16 with float
+// arithmetic: round to nearest even).
+template <typename T, typename ST>
+__device__ __forceinline__ T sh_ld_as(unsigned a) {
+    if constexpr (std::is_same<T, ST>::value) {
+        return sh_ld<T>(a);
+    } else {
+        static_assert(std::is_same<ST, __half>::value && std::is_same<T, float>::value, "binary16 storage: float");
+        unsigned short h;
+        asm volatile("ld.shared.b16 %0, [%1];" : "=h"(h) : "r"(a));
+        return __half2float(__ushort_as_half(h));
+    }
+}
+template <typename ST, typename T>
+__device__ __forceinline__ void sh_st_as(unsigned a, T v) {
+    if constexpr (std::is_same<T, ST>::value) {
+        sh_st(a, v);
+    } else {
+        static_assert(std::is_same<ST, __half>::value && std::is_same<T, float>::value, "binary16 storage: float");
+        const unsigned short h = __half_as_ushort(__float2half_rn(v));
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(h) : "memory");
+    }
+}
 
 // Geometry of step k of sweep r in 32-bit arithmetic (the group kernel runs
 // only for n < 2^30): c, p, ce, cend and w as in step_geom.
@@ -123,11 +152,11 @@ __host__ __device__ constexpr bool group_v_in_registers() {
 // Right half-step (rows p..ce of columns c..ce) on the buffered band, by one
 // warp: reflector from row p, then lane i applies it to rows p+1+i, +32, ...
 // The half-step's columns span fewer than nslot slots, so a slot index past
-// the end wraps with one subtraction.
-template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
+// the end wraps with one subtraction.  T: arithmetic, ST: storage.
+template <typename T, typename ST, int WMAX, bool FULL>
+__device__ __forceinline__ void group_right(const ColBuf<ST>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
-    constexpr unsigned S = sizeof(T);
+    constexpr unsigned S = sizeof(T), SB = sizeof(ST);
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
     // A(p + i, c + m) is element a0 + i + m (lds - 1) - (m >= mwrap ? nslot lds : 0):
@@ -142,13 +171,13 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
         xa[q] = cb.at(a0 + m * dm - ((m >= mwrap) ? wrap : 0));
-        xp[q] = (m < W) ? sh_ld<T>(xa[q]) : T(0);
+        xp[q] = (m < W) ? sh_ld_as<T, ST>(xa[q]) : T(0);
     }
     T beta = warp_larfg<T, NPL>(xp, W, lane, vb, taub);
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        if (m < W) sh_st(xa[q], (m == 0) ? beta : T(0));
+        if (m < W) sh_st_as<ST>(xa[q], (m == 0) ? beta : T(0));
     }
     __syncwarp();
     const T tau = sh_ld<T>(sh_addr(taub));
@@ -166,7 +195,7 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
     // byte offset of column c + m from column c, wrap included
     unsigned om[WMAX];
 #pragma unroll
-    for (int m = 0; m < WMAX; ++m) om[m] = S * (unsigned)(m * dm - ((m >= mwrap) ? wrap : 0));
+    for (int m = 0; m < WMAX; ++m) om[m] = SB * (unsigned)(m * dm - ((m >= mwrap) ? wrap : 0));
     const int nrows = g.ce - g.p;
     for (int i = 1 + lane; i <= nrows; i += 32) {
         const unsigned ra = cb.at(a0 + i);
@@ -175,37 +204,37 @@ __device__ __forceinline__ void group_right(const ColBuf<T>& cb, const GGeom& g,
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
-                x[m] = sh_ld<T>(ra + om[m]);
+                x[m] = sh_ld_as<T, ST>(ra + om[m]);
                 y = fma(x[m], v(m), y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) sh_st(ra + om[m], fma(-s, v(m), x[m]));
+            if (m < W) sh_st_as<ST>(ra + om[m], fma(-s, v(m), x[m]));
     }
 }
 
 // Left half-step (rows c..ce of columns c..cend) on the buffered band, by
 // one warp: reflector from column c, then lane i applies it to columns
 // c+1+i, +32, ...
-template <typename T, int WMAX, bool FULL>
-__device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, int s0, T* vb, T* taub) {
+template <typename T, typename ST, int WMAX, bool FULL>
+__device__ __forceinline__ void group_left(const ColBuf<ST>& cb, const GGeom& g, int s0, T* vb, T* taub) {
     constexpr int NPL = (WMAX + 31) / 32;
-    constexpr unsigned S = sizeof(T);
+    constexpr unsigned S = sizeof(T), SB = sizeof(ST);
     const int W = FULL ? WMAX : g.w;
     const int lane = threadIdx.x & 31;
-    const unsigned colc = cb.at(s0 * cb.lds + cb.off);  // colc + S m = A(c + m, c)
+    const unsigned colc = cb.at(s0 * cb.lds + cb.off);  // colc + SB m = A(c + m, c)
     T xc[NPL];
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        xc[q] = (m < W) ? sh_ld<T>(colc + S * (unsigned)m) : T(0);
+        xc[q] = (m < W) ? sh_ld_as<T, ST>(colc + SB * (unsigned)m) : T(0);
     }
     T beta = warp_larfg<T, NPL>(xc, W, lane, vb, taub);
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
         const int m = lane + 32 * q;
-        if (m < W) sh_st(colc + S * (unsigned)m, (m == 0) ? beta : T(0));
+        if (m < W) sh_st_as<ST>(colc + SB * (unsigned)m, (m == 0) ? beta : T(0));
     }
     __syncwarp();
     const T tau = sh_ld<T>(sh_addr(taub));
@@ -221,19 +250,19 @@ __device__ __forceinline__ void group_left(const ColBuf<T>& cb, const GGeom& g, 
     for (int dj = 1 + lane; dj <= g.cend - g.c; dj += 32) {
         int sl = s0 + dj;
         if (sl >= cb.nslot) sl -= cb.nslot;
-        const unsigned cj = cb.at(sl * cb.lds + cb.off - dj);  // cj + S m = A(c + m, c + dj)
+        const unsigned cj = cb.at(sl * cb.lds + cb.off - dj);  // cj + SB m = A(c + m, c + dj)
         T x[WMAX];
         T y = 0;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
             if (m < W) {
-                x[m] = sh_ld<T>(cj + S * (unsigned)m);
+                x[m] = sh_ld_as<T, ST>(cj + SB * (unsigned)m);
                 y = fma(v(m), x[m], y);
             }
         const T s = tau * y;
 #pragma unroll
         for (int m = 0; m < WMAX; ++m)
-            if (m < W) sh_st(cj + S * (unsigned)m, fma(-s, v(m), x[m]));
+            if (m < W) sh_st_as<ST>(cj + SB * (unsigned)m, fma(-s, v(m), x[m]));
     }
 }
 
@@ -253,16 +282,16 @@ struct BidiagChase {
     __device__ static long long min_col(const PassArgs& P, int r, int h) { return half_min_col(P, r, h); }
     // slot: the buffer slot of column c of this half-step's step (the caller
     // carries it from step to step, sparing a modulo on the critical path).
-    template <typename T, int WMAX>
-    __device__ static void unit(const PassArgs& P, const ColBuf<T>& cb, int r, int h, int slot, T* vb, T* taub) {
+    template <typename T, typename ST, int WMAX>
+    __device__ static void unit(const PassArgs& P, const ColBuf<ST>& cb, int r, int h, int slot, T* vb, T* taub) {
         const GGeom g = gstep(P, r, h >> 1);
         const bool full = g.w == WMAX;
         if ((h & 1) == 0) {
-            if (full) group_right<T, WMAX, true>(cb, g, slot, vb, taub);
-            else group_right<T, WMAX, false>(cb, g, slot, vb, taub);
+            if (full) group_right<T, ST, WMAX, true>(cb, g, slot, vb, taub);
+            else group_right<T, ST, WMAX, false>(cb, g, slot, vb, taub);
         } else {
-            if (full) group_left<T, WMAX, true>(cb, g, slot, vb, taub);
-            else group_left<T, WMAX, false>(cb, g, slot, vb, taub);
+            if (full) group_left<T, ST, WMAX, true>(cb, g, slot, vb, taub);
+            else group_left<T, ST, WMAX, false>(cb, g, slot, vb, taub);
         }
     }
 };
@@ -428,7 +457,9 @@ __host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem
 
 // Persistent group kernel: CTAs take groups G = blockIdx.x, + gridDim.x, ...
 // in order; blockDim.x = 32 * (g + 3).  Chase: the chase it runs (units,
-// their columns and their arithmetic; BidiagChase above).
+// their columns and their arithmetic; BidiagChase above).  T: the arithmetic
+// type, ST: the band's storage type (T, or binary16 with float arithmetic;
+// columns are buffered as stored).
 //   Warps jj < g run sweep r0 + jj, one unit per tick, and meet at a named
 //   barrier after each tick.
 //   Warp g (the loader) copies in the columns tick u first needs, one bulk
@@ -448,11 +479,11 @@ __host__ __device__ inline size_t group_cols_offset(int g, int wmax, size_t elem
 // publication thus overlap the computation.  Every wait is bounded; on
 // giving up the CTA latches an error, the compute warps leave their loop at
 // the same tick, the other roles leave theirs, and the CTA returns after one
-// last barrier.  Requires band, ldab * sizeof(T) and top * sizeof(T) 16-byte
-// aligned and n < 2^30 (32-bit geometry).
-template <typename T, int WMAX, class Chase = BidiagChase>
+// last barrier.  Requires band, ldab * sizeof(ST) and top * sizeof(ST)
+// 16-byte aligned and n < 2^30 (32-bit geometry).
+template <typename T, int WMAX, class Chase = BidiagChase, typename ST = T>
 __global__ void __launch_bounds__(32 * GroupMaxWarps<T, WMAX>::value)
-pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restrict__ wm,
+pass_group_kernel(ST* __restrict__ band, PassArgs P, GroupArgs GA, int* __restrict__ wm,
                   int* __restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_flag;
@@ -467,8 +498,8 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     constexpr int VS = Chase::kVecs * group_v_stride(WMAX, (int)sizeof(T));
     T* vbuf = reinterpret_cast<T*>(smem_raw);  // [g][VS], 16-byte aligned rows
     T* taubuf = vbuf + (size_t)GA.g * VS;      // [g]
-    ColBuf<T> cb;
-    cb.cols = reinterpret_cast<T*>(smem_raw + group_cols_offset(GA.g, WMAX, sizeof(T), Chase::kVecs));
+    ColBuf<ST> cb;
+    cb.cols = reinterpret_cast<ST*>(smem_raw + group_cols_offset(GA.g, WMAX, sizeof(T), Chase::kVecs));
     cb.base = sh_addr(cb.cols);
     cb.nslot = GA.nslot;
     cb.lds = GA.lds;
@@ -477,7 +508,7 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
     const int lane = threadIdx.x & 31;
     const int L = P.lagh;
     const int S = GA.ahead + 2;
-    const unsigned col_bytes = (unsigned)(GA.lds * sizeof(T));
+    const unsigned col_bytes = (unsigned)(GA.lds * sizeof(ST));
     const unsigned long long inner_budget = 2 * P.wait_budget + (1ull << 24);
     if (threadIdx.x == 0) {
         s_flag = ld_relaxed_gpu(status);
@@ -530,8 +561,8 @@ pass_group_kernel(T* __restrict__ band, PassArgs P, GroupArgs GA, int* __restric
                         my_slot += P.b;
                         while (my_slot >= cb.nslot) my_slot -= cb.nslot;
                     }
-                    Chase::template unit<T, WMAX>(P, cb, r0 + warp, h, my_slot, vbuf + (size_t)warp * VS,
-                                                  taubuf + warp);
+                    Chase::template unit<T, ST, WMAX>(P, cb, r0 + warp, h, my_slot, vbuf + (size_t)warp * VS,
+                                                      taubuf + warp);
                     // the storer's bulk copies read these columns through the async proxy
                     if (GA.bulk_store) fence_proxy_async_smem();
                 }

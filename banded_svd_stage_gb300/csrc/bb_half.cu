@@ -10,20 +10,25 @@
 // Entries of one half-step are therefore rounded exactly once per write, as
 // in a run on binary16 storage.
 //
-// Scheduler: the flag kernel's progress protocol (one CTA per sweep,
-// persistent, cooperative launch): half-step h of sweep r starts once sweep
-// r-1 has completed min(h + lagh, H_{r-1}) half-steps, and a sweep reports
-// its last half-step only after its predecessor reported all of its own.
-// Every half-step reads its whole window after its wait, through L2
-// (ld.global.cg), so the data a neighbouring CTA wrote is never read from a
-// stale L1 line; no shared-memory tiles are needed (a 2-byte element cannot
-// be copied with cp.async).
+// Schedulers, per pass:
+// - the flag kernel here: the flag kernel's progress protocol (one CTA per
+//   sweep, persistent, cooperative launch): half-step h of sweep r starts
+//   once sweep r-1 has completed min(h + lagh, H_{r-1}) half-steps, and a
+//   sweep reports its last half-step only after its predecessor reported all
+//   of its own.  Every half-step reads its whole window after its wait,
+//   through L2 (ld.global.cg), so the data a neighbouring CTA wrote is never
+//   read from a stale L1 line;
+// - the group kernel (bb_group.cuh) with binary16 storage: the columns are
+//   buffered in shared memory as stored, and each half-step converts the
+//   entries it reads to float and rounds the ones it writes, exactly as
+//   here.  Both kernels give bitwise equal results.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 
 #include "bb_device.cuh"
+#include "bb_group.cuh"
 #include "bb_half.h"
 
 namespace bb {
@@ -195,10 +200,59 @@ static cudaError_t run_half_pass_w(__half* band, const PassArgs& P, const HalfLa
     return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(kHalfThreads), args, 0, s);
 }
 
-cudaError_t run_half_pass(void* band, const PassArgs& P, const HalfLaunch& L, cudaStream_t s) {
+// Reflector lengths the binary16 group kernel is compiled for (0: none).
+static int half_group_wmax(int w) { return w <= 9 ? 9 : (w <= 17 ? 17 : (w <= 33 ? 33 : 0)); }
+
+bool half_choose_group(const PassArgs& P, int scheduler, int group_size, GroupArgs* out) {
+    if (scheduler != 0 && scheduler != 3) return false;
+    if (P.nsweeps <= 0 || P.n >= kGroupMaxN) return false;
+    const int wmax = half_group_wmax(P.t + 1);
+    if (wmax == 0) return false;
+    GroupArgs ga;
+    if (!plan_group(P, wmax, sizeof(float), group_size, &ga, ChaseKind::kBidiag, sizeof(__half))) return false;
+    if (scheduler == 0 && ga.g < kAutoGroupMin) return false;
+    if (out) *out = ga;
+    return true;
+}
+
+template <int WMAX>
+static cudaError_t run_half_group_w(__half* band, const PassArgs& P, const GroupArgs& GA, const HalfLaunch& L,
+                                    cudaStream_t s) {
+    auto kern = pass_group_kernel<float, WMAX, BidiagChase, __half>;
+    const size_t smem = group_smem_bytes(GA, WMAX, sizeof(float), BidiagChase::kVecs, sizeof(__half));
+    // always raise the dynamic limit: static shared memory counts against 48 KB too
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 3), smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    long long grid = std::min<long long>((long long)per_sm * L.num_sms, GA.ngroups);
+    if (L.max_ctas > 0) grid = std::min<long long>(grid, L.max_ctas);
+    err = cudaMemsetAsync(L.progress, 0, sizeof(int) * (size_t)GA.ngroups, s);
+    if (err != cudaSuccess) return err;
+    __half* band_arg = band;
+    PassArgs p_arg = P;
+    GroupArgs g_arg = GA;
+    int* wm_arg = L.progress;
+    int* stat_arg = L.status;
+    void* args[] = {&band_arg, &p_arg, &g_arg, &wm_arg, &stat_arg};
+    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 3)), args, smem,
+                                       s);
+}
+
+cudaError_t run_half_pass(void* band, const PassArgs& P, const HalfLaunch& L, const GroupArgs* GA,
+                          cudaStream_t s) {
     if (P.nsweeps <= 0) return cudaSuccess;
     __half* b = static_cast<__half*>(band);
     const int w = P.t + 1;
+    if (GA) {
+        const int wmax = half_group_wmax(w);
+        if (wmax == 9) return run_half_group_w<9>(b, P, *GA, L, s);
+        if (wmax == 17) return run_half_group_w<17>(b, P, *GA, L, s);
+        if (wmax == 33) return run_half_group_w<33>(b, P, *GA, L, s);
+        return cudaErrorInvalidValue;
+    }
     if (w <= 9) return run_half_pass_w<9>(b, P, L, s, nullptr);
     if (w <= 17) return run_half_pass_w<17>(b, P, L, s, nullptr);
     if (w <= 33) return run_half_pass_w<33>(b, P, L, s, nullptr);

@@ -44,18 +44,20 @@ enum class ChaseKind { kBidiag = 0, kSym = 1 };
 // Reflector-sized vectors of shared scratch per sweep (Chase::kVecs).
 inline int chase_vecs(ChaseKind kind) { return kind == ChaseKind::kSym ? 2 : 1; }
 
-// Shared memory of the group kernel: per-sweep scratch and scalars, then
-// the circular column buffer.
-inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem, int nvec = 1) {
-    return group_cols_offset(GA.g, wmax, elem, nvec) + elem * (size_t)GA.nslot * GA.lds;
+// Shared memory of the group kernel: per-sweep scratch and scalars (elem:
+// the arithmetic type's size), then the circular column buffer (selem: the
+// storage type's size; 0 = elem).
+inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem, int nvec = 1, size_t selem = 0) {
+    return group_cols_offset(GA.g, wmax, elem, nvec) + (selem ? selem : elem) * (size_t)GA.nslot * GA.lds;
 }
 
 // Largest group (<= requested, or the most the kernel is compiled for when
 // requested == 0) whose column buffer fits in shared memory; false if not
-// even one sweep fits.  The kernel then needs the band and ldab * elem
-// 16-byte aligned (group_layout_ok).
+// even one sweep fits.  elem: the arithmetic type's size; selem: the
+// storage type's size (0 = elem; 2 for binary16 storage).  The kernel then
+// needs the band and ldab * selem 16-byte aligned (group_layout_ok).
 bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out,
-                ChaseKind kind = ChaseKind::kBidiag);
+                ChaseKind kind = ChaseKind::kBidiag, size_t selem = 0);
 
 // Whether the group kernel's bulk copies can address this band storage.
 inline bool group_layout_ok(const void* band, long long ldab, size_t elem) {

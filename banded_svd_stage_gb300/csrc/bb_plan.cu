@@ -73,9 +73,11 @@ int group_footprint(const PassArgs& P, int g, int ahead, ChaseKind kind) {
     return (int)fp;
 }
 
-bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out, ChaseKind kind) {
+bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupArgs* out, ChaseKind kind,
+                size_t selem) {
     const size_t budget = 220 * 1024;
     const int nvec = chase_vecs(kind);
+    if (selem == 0) selem = elem;
     GroupArgs best{};
     const int gcap = group_max_warps(wmax, elem);
     const int gmax = requested > 0 ? std::min(requested, gcap) : gcap;
@@ -87,7 +89,7 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
         // the upper band; ku .. ku+b+t of the lower, symmetric band), both
         // ends rounded out to 16 bytes (the extra rows are ones the pass
         // leaves alone: copied in and written back unchanged)
-        const int q = (int)(16 / elem);
+        const int q = (int)(16 / selem);
         const int lo = (kind == ChaseKind::kSym) ? P.ku : P.ku - P.b - P.t;
         const int hi = (kind == ChaseKind::kSym) ? P.ku + P.b + P.t : P.ku + P.t;
         ga.top = lo / q * q;
@@ -96,9 +98,9 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
         // wide columns go back with bulk copies (one instruction a column);
         // narrow ones with plain copies, which spare the compute warps a
         // proxy fence every tick
-        ga.bulk_store = ((size_t)ga.lds * elem >= 256) ? 1 : 0;
+        ga.bulk_store = ((size_t)ga.lds * selem >= 256) ? 1 : 0;
         ga.nslot = std::max(1, group_footprint(P, g, ga.ahead, kind));
-        if (group_smem_bytes(ga, wmax, elem, nvec) > budget) break;
+        if (group_smem_bytes(ga, wmax, elem, nvec, selem) > budget) break;
         best = ga;
         if (requested > 0 && g == requested) break;
     }
@@ -111,7 +113,7 @@ bool plan_group(const PassArgs& P, int wmax, size_t elem, int requested, GroupAr
         GroupArgs ga = best;
         ga.ahead = a;
         ga.nslot = std::max(1, group_footprint(P, ga.g, a, kind));
-        if (group_smem_bytes(ga, wmax, elem, nvec) > budget) break;
+        if (group_smem_bytes(ga, wmax, elem, nvec, selem) > budget) break;
         best = ga;
     }
     *out = best;

@@ -4,20 +4,33 @@
 // Memory-Aware Bulge-Chasing on GPUs", Section V, the "classical block
 // Householder reduction" its accuracy protocol runs before the band stage;
 // the GPU stage 1 of "A two-stage reduction on an Apple M5 Pro" uses the same
-// panels).
+// panels, with the trailing updates as matrix products).
 //
-// For each panel of bw columns k .. k+bw-1:
+// For each panel of bw columns k .. kb-1 (kb = min(k + bw, n)):
 //   QR of the panel, column by column: the reflector of A(j.., j) (LAPACK
 //   xLARFG convention) is applied from the left to every later column;
 //   LQ of the panel's rows right of the band, row by row: the reflector of
 //   A(i, i+bw ..) is applied from the right to every later row.
-// Annihilated entries are set to exactly zero.  One reflector is built by one
-// block (block-wide scaled norm) and applied as a rank-one update: one block
-// per trailing column for a left reflector (its column is contiguous), a
-// row-parallel product then a rank-one update for a right reflector.  The
-// arithmetic is in the matrix's own precision; these are SIMT kernels (the
-// tensor cores of this GPU have no float64 rate worth using, and TF32 would
-// lose float32 accuracy).
+// Annihilated entries are set to exactly zero.
+//
+// Blocked (compact WY) form of that sequence, kInner reflectors at a time
+// (the QR reflectors of a panel in order, then its LQ reflectors in order):
+//   1. s1_panel_kernel (one CTA) factorizes a block of kInner columns:
+//      reflector j is built from P(j.., j) and applied to the block's later
+//      columns only; it writes V (unit lower trapezoidal), tau and the upper
+//      triangular T with H_0 H_1 ... = I - V T V^T (LAPACK xLARFT, forward,
+//      columnwise);
+//   2. the rest of the matrix is updated with matrix products:
+//        QR: rows of the block's reflectors, later columns:  A -= V T^T (V^T A);
+//        LQ: rows below the block's rows, their columns:     A -= (A U) T U^T;
+//      the long inner products (V^T A, A U) are split over several CTAs and
+//      their partial sums added in a fixed order (s1_reduce_tri_kernel, which
+//      also applies T).
+// The LQ panel is the QR panel kernel on the transposed view of the rows
+// (P(i, c) = A(k + c, k + bw + i)).  The products are SIMT tiled GEMMs in
+// the matrix's own precision (the tensor cores of this GPU have no float64
+// rate worth using, and TF32 would lose float32 accuracy).  The arithmetic
+// differs from the reflector-by-reflector sequence only in rounding order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -28,146 +41,312 @@
 
 namespace bb {
 
-constexpr int kS1Threads = 256;
+constexpr int kPanelThreads = 512;
+constexpr int kPanelWarps = kPanelThreads / 32;
+constexpr int kDotChunk = 16;  // dot products are reduced kDotChunk at a time
 
+// Sum over the block of one value per thread; every thread gets the result.
 template <typename T>
-__device__ __forceinline__ T block_reduce_sum(T v, T* red) {
+__device__ __forceinline__ T s1_block_sum(T v, T* red) {
     v = warp_sum(v);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __syncthreads();
     if (lane == 0) red[warp] = v;
     __syncthreads();
     T s = 0;
-    if (threadIdx.x < 32) {
-        s = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : T(0);
-        s = warp_sum(s);
-        if (threadIdx.x == 0) red[32] = s;
-    }
-    __syncthreads();
-    return red[32];
+#pragma unroll
+    for (int w = 0; w < kPanelWarps; ++w) s += red[w];
+    return s;
 }
 template <typename T>
-__device__ __forceinline__ T block_reduce_max(T v, T* red) {
+__device__ __forceinline__ T s1_block_max(T v, T* red) {
     v = warp_max(v);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __syncthreads();
     if (lane == 0) red[warp] = v;
     __syncthreads();
     T s = 0;
-    if (threadIdx.x < 32) {
-        s = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : T(0);
-        s = warp_max(s);
-        if (threadIdx.x == 0) red[32] = s;
-    }
-    __syncthreads();
-    return red[32];
+#pragma unroll
+    for (int w = 0; w < kPanelWarps; ++w) s = fmax(s, red[w]);
+    return s;
 }
 
-// Reflector of x[0], x[inc], ..., x[(m-1) inc] (m >= 2), one block: on
-// return v[0 .. m-1] holds v (v[0] = 1), *tau_out tau, x[0] = beta and the
-// other entries of x are exactly zero.  Norm of the tail: the largest
-// magnitude first, then the sum of squares of the scaled entries; tiny
-// results are rescaled by safmin as LAPACK does.
+// Panel factorization, one CTA.  The panel P (m x nc) is P(i, c) =
+// p[i * si + c * sc]; reflectors j = 0 .. nq-1 (nq <= nc, nq <= m - 1), the
+// reflector of P(j .. m-1, j) applied to columns j+1 .. nc-1.  Outputs:
+//   P(j, j) = beta, P(j+1.., j) = 0;
+//   V (m x nq, column-major, ld m): column j is v_j (zeros above row j, 1 at
+//   row j);  tau[j];  Tm (nq x nq, column-major): T(l, j) for l <= j;
+//   dots (nc entries): scratch.
+// Norm as the oracle: the plain sum of squares of the tail; when it under-
+// or overflows, the largest magnitude first and the sum of squares of the
+// scaled entries; then LAPACK's safmin rescaling for a tiny beta.
 template <typename T>
-__global__ void __launch_bounds__(kS1Threads) s1_larfg_kernel(T* __restrict__ x, long long inc, int m,
-                                                               T* __restrict__ v, T* __restrict__ tau_out) {
-    __shared__ T red[33];
-    T amax = 0;
-    for (int i = 1 + threadIdx.x; i < m; i += blockDim.x) amax = fmax(amax, fabs(x[(long long)i * inc]));
-    const T scale = block_reduce_max(amax, red);
-    T alpha = x[0];
-    if (scale == T(0)) {
-        for (int i = threadIdx.x; i < m; i += blockDim.x) v[i] = (i == 0) ? T(1) : T(0);
-        if (threadIdx.x == 0) *tau_out = T(0);
-        return;
-    }
-    T ss = 0;
-    for (int i = 1 + threadIdx.x; i < m; i += blockDim.x) {
-        const T u = x[(long long)i * inc] / scale;
-        ss = fma(u, u, ss);
-    }
-    ss = block_reduce_sum(ss, red);
-    T xnorm = scale * dev_sqrt(ss);
-    T beta = (alpha >= T(0)) ? -dev_hypot(alpha, xnorm) : dev_hypot(alpha, xnorm);
-    const T safmin = Lim<T>::safmin();
-    int knt = 0;
-    T mult = T(1);  // the scaling applied to x's tail
-    if (fabs(beta) < safmin) {
-        const T rsafmn = T(1) / safmin;
-        do {
-            ++knt;
-            mult = mult * rsafmn;
-            beta = beta * rsafmn;
-            alpha = alpha * rsafmn;
-        } while (fabs(beta) < safmin && knt < 20);
-        xnorm = xnorm * mult;
-        beta = (alpha >= T(0)) ? -dev_hypot(alpha, xnorm) : dev_hypot(alpha, xnorm);
-    }
-    const T tau = (beta - alpha) / beta;
-    const T scal = T(1) / (alpha - beta);
-    for (int i = threadIdx.x; i < m; i += blockDim.x) {
-        if (i == 0) {
-            v[0] = T(1);
-        } else {
-            T* xi = x + (long long)i * inc;
-            v[i] = (*xi * mult) * scal;
-            *xi = T(0);
+__global__ void __launch_bounds__(kPanelThreads)
+s1_panel_kernel(T* __restrict__ p, long long si, long long sc, int m, int nc, int nq, T* __restrict__ V,
+                T* __restrict__ tau_out, T* __restrict__ Tm, T* __restrict__ dots) {
+    __shared__ T red[kPanelWarps];
+    __shared__ T part[kPanelWarps][kDotChunk];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    auto P = [&](int i, int c) -> T& { return p[(long long)i * si + (long long)c * sc]; };
+    for (int j = 0; j < nq; ++j) {
+        T* vj = V + (long long)j * m;
+        const T alpha = P(j, j);
+        T ss = 0;
+        for (int i = j + 1 + tid; i < m; i += kPanelThreads) {
+            const T x = P(i, j);
+            ss = fma(x, x, ss);
         }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int j = 0; j < knt; ++j) beta = beta * safmin;
-        x[0] = beta;
-        *tau_out = tau;
-    }
-}
-
-// Left application: columns c0 + blockIdx.x (+ gridDim.x ...), rows r0 ..
-// r0+m-1 of the column-major matrix: y = v^T A(r0.., c), A(r0.., c) -= tau v y.
-template <typename T>
-__global__ void __launch_bounds__(kS1Threads) s1_apply_left_kernel(T* __restrict__ a, long long lda, int r0,
-                                                                    int m, int c0, int c1,
-                                                                    const T* __restrict__ v,
-                                                                    const T* __restrict__ tau_p) {
-    __shared__ T red[33];
-    const T tau = *tau_p;
-    if (tau == T(0)) return;
-    for (int c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        T* col = a + (long long)c * lda + r0;
-        T y = 0;
-        for (int i = threadIdx.x; i < m; i += blockDim.x) y = fma(v[i], col[i], y);
-        y = block_reduce_sum(y, red);
-        const T s = tau * y;
-        for (int i = threadIdx.x; i < m; i += blockDim.x) col[i] = fma(-s, v[i], col[i]);
+        ss = s1_block_sum(ss, red);
+        T beta, tau, scal, mult = T(1);
+        int knt = 0;
+        bool identity = false;
+        if (isfinite(ss) && ss >= Lim<T>::min_normal()) {
+            const T nrm = dev_sqrt(fma(alpha, alpha, ss));
+            beta = (alpha >= T(0)) ? -nrm : nrm;
+        } else {
+            T amax = 0;
+            for (int i = j + 1 + tid; i < m; i += kPanelThreads) amax = fmax(amax, fabs(P(i, j)));
+            const T scale = s1_block_max(amax, red);
+            if (scale == T(0)) {
+                identity = true;
+                beta = alpha;
+            } else {
+                T s2 = 0;
+                for (int i = j + 1 + tid; i < m; i += kPanelThreads) {
+                    const T u = P(i, j) / scale;
+                    s2 = fma(u, u, s2);
+                }
+                s2 = s1_block_sum(s2, red);
+                const T xnorm = scale * dev_sqrt(s2);
+                beta = (alpha >= T(0)) ? -dev_hypot(alpha, xnorm) : dev_hypot(alpha, xnorm);
+                const T safmin = Lim<T>::safmin();
+                if (fabs(beta) < safmin) {
+                    const T rsafmn = T(1) / safmin;
+                    T a2 = alpha;
+                    do {
+                        ++knt;
+                        mult = mult * rsafmn;
+                        beta = beta * rsafmn;
+                        a2 = a2 * rsafmn;
+                    } while (fabs(beta) < safmin && knt < 20);
+                    const T xn2 = xnorm * mult;
+                    beta = (a2 >= T(0)) ? -dev_hypot(a2, xn2) : dev_hypot(a2, xn2);
+                    tau = (beta - a2) / beta;
+                    scal = T(1) / (a2 - beta);
+                }
+            }
+        }
+        if (!identity && knt == 0) {
+            tau = (beta - alpha) / beta;
+            scal = T(1) / (alpha - beta);
+        }
+        if (identity) {
+            tau = T(0);
+            scal = T(0);
+        }
+        // v_j, the annihilated entries, beta
+        for (int i = tid; i < m; i += kPanelThreads) {
+            if (i < j) {
+                vj[i] = T(0);
+            } else if (i == j) {
+                vj[i] = T(1);
+            } else {
+                T& x = P(i, j);
+                vj[i] = identity ? T(0) : (x * mult) * scal;
+                x = T(0);
+            }
+        }
+        if (tid == 0) {
+            T b = beta;
+            for (int q = 0; q < knt; ++q) b = b * Lim<T>::safmin();
+            P(j, j) = b;
+            tau_out[j] = tau;
+        }
+        __syncthreads();
+        // dot products of v_j (rows j..m-1) with the panel's later columns
+        // (dots[c], c > j) and with the earlier reflectors (dots[l], l < j),
+        // kDotChunk values at a time: each thread walks its rows once per
+        // chunk with the partial sums in registers
+        const int R = (tau != T(0)) ? nc - 1 : j;  // values c != j, c < nc
+        for (int c0 = 0; c0 < R; c0 += kDotChunk) {
+            const int cn = min(kDotChunk, R - c0);
+            T d[kDotChunk];
+#pragma unroll
+            for (int q = 0; q < kDotChunk; ++q) d[q] = T(0);
+            if (tau != T(0)) {
+                for (int i = j + tid; i < m; i += kPanelThreads) {
+                    const T vi = vj[i];
+#pragma unroll
+                    for (int q = 0; q < kDotChunk; ++q) {
+                        if (q < cn) {
+                            const int c = (c0 + q < j) ? c0 + q : c0 + q + 1;
+                            const T x = (c > j) ? P(i, c) : V[(long long)c * m + i];
+                            d[q] = fma(vi, x, d[q]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kDotChunk; ++q) {
+                const T w = warp_sum(d[q]);
+                if (lane == 0) part[warp][q] = w;
+            }
+            __syncthreads();
+            for (int q = tid; q < cn; q += kPanelThreads) {
+                T sum = 0;
+#pragma unroll
+                for (int w = 0; w < kPanelWarps; ++w) sum += part[w][q];
+                dots[(c0 + q < j) ? c0 + q : c0 + q + 1] = sum;
+            }
+            __syncthreads();
+        }
+        // P(i, c) -= (tau (v_j . P(:, c))) v_j(i), c > j
+        if (tau != T(0)) {
+            for (int i = j + tid; i < m; i += kPanelThreads) {
+                const T vi = vj[i];
+                for (int c = j + 1; c < nc; ++c) P(i, c) = fma(-(tau * dots[c]), vi, P(i, c));
+            }
+        }
+        // T(j, j) = tau_j; T(l, j) = -tau_j sum_{q = l}^{j-1} T(l, q) (v_q . v_j)
+        for (int l = tid; l <= j; l += kPanelThreads) {
+            T t = tau;
+            if (l < j) {
+                T s = 0;
+                for (int q = l; q < j; ++q) s = fma(Tm[l + (long long)q * nq], dots[q], s);
+                t = -tau * s;
+            }
+            Tm[l + (long long)j * nq] = t;
+        }
         __syncthreads();
     }
 }
 
-// Right application, part one: y[r] = sum_c A(r0 + r, c0 + c) u[c], one
-// thread per row (consecutive threads, consecutive rows of a column).
-template <typename T>
-__global__ void s1_gemv_rows_kernel(const T* __restrict__ a, long long lda, int r0, int mr, int c0, int mc,
-                                    const T* __restrict__ u, T* __restrict__ y, const T* __restrict__ tau_p) {
-    if (*tau_p == T(0)) return;
-    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < mr; r += gridDim.x * blockDim.x) {
-        const T* row = a + (long long)c0 * lda + r0 + r;
-        T s = 0;
-        for (int c = 0; c < mc; ++c) s = fma(row[(long long)c * lda], u[c], s);
-        y[r] = s;
+// C = alpha op(A) op(B) + beta C, column-major (M x N, inner dimension K):
+// op(A)(i, l) = TA ? A[l + i lda] : A[i + l lda], op(B)(l, j) = TB ?
+// B[j + l ldb] : B[l + j ldb].  64 x 64 tiles of C per CTA, 16 x 16 threads
+// with 4 x 4 entries each (rows tx + 16 p, columns ty + 16 q), the inner
+// dimension in steps of 16 through shared memory.  beta is 0 (C is not
+// read) or 1.  Split inner dimension: CTA z sums l in [z kchunk, (z + 1)
+// kchunk) into C + z cz (partial products, reduced by the caller).
+constexpr int kGemmBM = 64, kGemmBN = 64, kGemmBK = 16;
+template <typename T, bool TA, bool TB>
+__global__ void __launch_bounds__(256)
+s1_gemm_kernel(int M, int N, int K, T alpha, const T* __restrict__ A, long long lda, const T* __restrict__ B,
+               long long ldb, T beta, T* __restrict__ C, long long ldc, int kchunk, long long cz) {
+    __shared__ T As[kGemmBK][kGemmBM + 1];
+    __shared__ T Bs[kGemmBK][kGemmBN + 1];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;
+    const int i0 = blockIdx.x * kGemmBM, j0 = blockIdx.y * kGemmBN;
+    const int lbeg = blockIdx.z * kchunk, lend = min(K, lbeg + kchunk);
+    C += blockIdx.z * cz;
+    T acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = T(0);
+    for (int l0 = lbeg; l0 < lend; l0 += kGemmBK) {
+        for (int e = tid; e < kGemmBK * kGemmBM; e += 256) {
+            // consecutive threads on the contiguous index of A
+            const int ii = TA ? e / kGemmBK : e % kGemmBM;
+            const int ll = TA ? e % kGemmBK : e / kGemmBM;
+            const int gi = i0 + ii, gl = l0 + ll;
+            T x = T(0);
+            if (gi < M && gl < lend) x = TA ? A[gl + (long long)gi * lda] : A[gi + (long long)gl * lda];
+            As[ll][ii] = x;
+        }
+        for (int e = tid; e < kGemmBK * kGemmBN; e += 256) {
+            const int jj = TB ? e % kGemmBN : e / kGemmBK;
+            const int ll = TB ? e / kGemmBN : e % kGemmBK;
+            const int gj = j0 + jj, gl = l0 + ll;
+            T x = T(0);
+            if (gj < N && gl < lend) x = TB ? B[gj + (long long)gl * ldb] : B[gl + (long long)gj * ldb];
+            Bs[ll][jj] = x;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int l = 0; l < kGemmBK; ++l) {
+            T a[4], b[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                a[q] = As[l][tx + 16 * q];
+                b[q] = Bs[l][ty + 16 * q];
+            }
+#pragma unroll
+            for (int pa = 0; pa < 4; ++pa)
+#pragma unroll
+                for (int pb = 0; pb < 4; ++pb) acc[pa][pb] = fma(a[pa], b[pb], acc[pa][pb]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int pb = 0; pb < 4; ++pb) {
+        const int gj = j0 + ty + 16 * pb;
+        if (gj >= N) continue;
+#pragma unroll
+        for (int pa = 0; pa < 4; ++pa) {
+            const int gi = i0 + tx + 16 * pa;
+            if (gi >= M) continue;
+            T* c = C + gi + (long long)gj * ldc;
+            *c = (beta == T(0)) ? alpha * acc[pa][pb] : fma(alpha, acc[pa][pb], *c);
+        }
     }
 }
 
-// Right application, part two: A(r0 + r, c0 + c) -= tau y[r] u[c].
+// nsplit > 1: nsplit partial products of the inner dimension into C + z cz
+// (beta must be 0).
+template <typename T, bool TA, bool TB>
+static cudaError_t s1_gemm(int M, int N, int K, T alpha, const T* A, long long lda, const T* B, long long ldb,
+                           T beta, T* C, long long ldc, cudaStream_t s, int nsplit = 1, long long cz = 0) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    const int kchunk = (nsplit > 1) ? ((K + nsplit - 1) / nsplit + kGemmBK - 1) / kGemmBK * kGemmBK : K;
+    // column blocks of C within the grid's y limit
+    const int nmax = 65535 * kGemmBN;
+    for (int j0 = 0; j0 < N; j0 += nmax) {
+        const int nb = std::min(nmax, N - j0);
+        const T* Bj = TB ? B + j0 : B + (long long)j0 * ldb;
+        const dim3 grid((unsigned)((M + kGemmBM - 1) / kGemmBM), (unsigned)((nb + kGemmBN - 1) / kGemmBN),
+                        (unsigned)std::max(1, nsplit));
+        s1_gemm_kernel<T, TA, TB><<<grid, 256, 0, s>>>(M, nb, K, alpha, A, lda, Bj, ldb, beta,
+                                                        C + (long long)j0 * ldc, ldc, kchunk, cz);
+        const cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+// Inner block: reflectors per panel-kernel call; the rest of the matrix is
+// updated after every kInner reflectors.
+constexpr int kInner = 16;
+// Most partial products of a split inner dimension.
+constexpr int kMaxSplit = 16;
+
+// W[q qs + j ls] = sum_{l <= j} T(l, j) w_l, w_l = sum_z Wp[z zs + q qs + l ls]
+// (z ascending), for the nvec vectors q of nb <= kInner entries: with
+// columns of W this is T^T W, with rows W T.
 template <typename T>
-__global__ void s1_rank1_kernel(T* __restrict__ a, long long lda, int r0, int mr, int c0, int mc,
-                                const T* __restrict__ u, const T* __restrict__ y, const T* __restrict__ tau_p) {
-    const T tau = *tau_p;
-    if (tau == T(0)) return;
-    for (int c = blockIdx.y; c < mc; c += gridDim.y) {
-        T* col = a + (long long)(c0 + c) * lda + r0;
-        const T tu = tau * u[c];
-        for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < mr; r += gridDim.x * blockDim.x)
-            col[r] = fma(-y[r], tu, col[r]);
+__global__ void s1_reduce_tri_kernel(const T* __restrict__ Wp, int nsplit, long long zs, T* __restrict__ W,
+                                     int nvec, long long qs, long long ls, int nb, const T* __restrict__ Tm) {
+    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < nvec; q += gridDim.x * blockDim.x) {
+        T w[kInner];
+#pragma unroll
+        for (int l = 0; l < kInner; ++l) {
+            T sum = 0;
+            if (l < nb)
+                for (int z = 0; z < nsplit; ++z) sum += Wp[z * zs + (long long)q * qs + (long long)l * ls];
+            w[l] = sum;
+        }
+#pragma unroll
+        for (int j = 0; j < kInner; ++j) {
+            if (j < nb) {
+                T sum = 0;
+#pragma unroll
+                for (int l = 0; l <= j; ++l) sum = fma(Tm[l + (long long)j * nb], w[l], sum);
+                W[(long long)q * qs + (long long)j * ls] = sum;
+            }
+        }
     }
 }
 
@@ -186,37 +365,86 @@ __global__ void s1_pack_kernel(const T* __restrict__ a, long long lda, long long
     }
 }
 
+// Workspace (elements), b = min(bw, kInner): V or U (n x b), W (n x b), the
+// partial products (kMaxSplit x n x b), T (b x b), tau and dots (b each).
+static long long s1_workspace_elems(long long n, long long bw) {
+    const long long b = std::min<long long>(std::min(bw, n), kInner);
+    return (2 + kMaxSplit) * n * b + b * b + 2 * b + 64;
+}
+
+// Partial products for a product of nvec x nb outputs with a long inner
+// dimension K: enough to give the GPU a few waves of CTAs.
+static int s1_splits(long long tiles, long long K, int num_sms) {
+    long long z = (2LL * num_sms + tiles - 1) / std::max(1LL, tiles);
+    z = std::min<long long>(z, std::max(1LL, K / 256));
+    return (int)std::max(1LL, std::min<long long>(z, kMaxSplit));
+}
+
 template <typename T>
 static cudaError_t run_stage1(T* a, long long n, long long lda, int bw, T* ws, int num_sms, cudaStream_t s) {
-    T* v = ws;          // n entries
-    T* y = ws + n;      // n entries
-    T* tau = ws + 2 * n;  // 1 entry
-    const int apply_grid = std::max(1, 4 * num_sms);
+    const long long nb = std::min(kInner, bw);
+    T* V = ws;                   // m x nq (QR) or m x nl (LQ), ld m
+    T* W = V + n * nb;           // nq x N (QR, ld nq) or M x nl (LQ, ld M)
+    T* Wp = W + n * nb;          // kMaxSplit partial products of W
+    T* Tm = Wp + kMaxSplit * n * nb;  // nq x nq
+    T* tau = Tm + nb * nb;
+    T* dots = tau + nb;
+    const long long zs = n * nb;
+    const unsigned vec_grid = (unsigned)std::max(1, 4 * num_sms);
     cudaError_t err = cudaSuccess;
     for (long long k = 0; k < n && err == cudaSuccess; k += bw) {
         const long long kb = std::min(k + bw, n);
-        for (long long j = k; j < kb && err == cudaSuccess; ++j) {
-            if (j + 1 >= n) break;
-            const int m = (int)(n - j);
-            s1_larfg_kernel<T><<<1, kS1Threads, 0, s>>>(a + j + j * lda, 1, m, v, tau);
-            const int ncols = (int)(n - j - 1);
-            s1_apply_left_kernel<T><<<std::min(ncols, apply_grid), kS1Threads, 0, s>>>(
-                a, lda, (int)j, m, (int)(j + 1), (int)n, v, tau);
+        // QR of columns k .. kb-1, kInner reflectors at a time: reflectors
+        // j = cs .. cs+nq-1 (j < min(kb, n-1)) on the sub-panel of columns
+        // cs .. cs+nc-1, then columns cs+nc .. n-1 of rows cs .. updated
+        const long long qend = std::min(kb, n - 1);
+        for (long long cs = k; cs < qend && err == cudaSuccess; cs += nb) {
+            const int nq = (int)std::min<long long>(nb, qend - cs);
+            const int nc = (int)std::min<long long>(nb, kb - cs);
+            const int m = (int)(n - cs);
+            s1_panel_kernel<T><<<1, kPanelThreads, 0, s>>>(a + cs + cs * lda, 1, lda, m, nc, nq, V, tau, Tm, dots);
             err = cudaGetLastError();
-        }
-        for (long long i = k; i < kb && err == cudaSuccess; ++i) {
-            const long long c0 = i + bw;
-            if (c0 + 1 >= n) break;
-            const int mc = (int)(n - c0);
-            s1_larfg_kernel<T><<<1, kS1Threads, 0, s>>>(a + i + c0 * lda, lda, mc, v, tau);
-            const int mr = (int)(n - i - 1);
-            if (mr > 0) {
-                const unsigned gx = (unsigned)std::max(1, std::min((mr + 255) / 256, apply_grid));
-                s1_gemv_rows_kernel<T><<<gx, 256, 0, s>>>(a, lda, (int)(i + 1), mr, (int)c0, mc, v, y, tau);
-                const unsigned gy = (unsigned)std::max(1, std::min(mc, 2 * apply_grid));
-                s1_rank1_kernel<T><<<dim3(gx, gy), 256, 0, s>>>(a, lda, (int)(i + 1), mr, (int)c0, mc, v, y, tau);
+            const int N = (int)(n - cs - nc);
+            if (err == cudaSuccess && N > 0) {
+                T* At = a + cs + (cs + nc) * lda;  // rows cs .., columns cs + nc ..
+                const long long tiles = (N + kGemmBN - 1) / kGemmBN;
+                const int z = s1_splits(tiles, m, num_sms);
+                // W = T^T (V^T At)
+                err = s1_gemm<T, true, false>(nq, N, m, T(1), V, m, At, lda, T(0), Wp, nq, s, z, zs);
+                if (err == cudaSuccess) {
+                    s1_reduce_tri_kernel<T><<<std::min<unsigned>(vec_grid, (unsigned)((N + 127) / 128)), 128, 0, s>>>(
+                        Wp, z, zs, W, N, nq, 1, nq, Tm);
+                    err = cudaGetLastError();
+                }
+                // At -= V W
+                if (err == cudaSuccess) err = s1_gemm<T, false, false>(m, N, nq, T(-1), V, m, W, nq, T(1), At, lda, s);
             }
+        }
+        // LQ of rows k .. kb-1 right of the band, kInner rows at a time:
+        // reflectors i = rs .. rs+nl-1 (i + bw + 1 < n) on the block rows
+        // rs .., columns rs + bw ..; then rows rs+nl .. n-1 of those columns
+        const long long lend = std::min(kb, n - 1 - bw);
+        for (long long rs = k; rs < lend && err == cudaSuccess; rs += nb) {
+            const int nl = (int)std::min<long long>(nb, lend - rs);
+            const int m = (int)(n - rs - bw);  // columns rs + bw .. n-1
+            T* B = a + rs + (rs + bw) * lda;   // B(r, c) = A(rs + r, rs + bw + c)
+            s1_panel_kernel<T><<<1, kPanelThreads, 0, s>>>(B, lda, 1, m, nl, nl, V, tau, Tm, dots);
             err = cudaGetLastError();
+            const int M = (int)(n - rs - nl);  // rows rs + nl .. n-1
+            if (err == cudaSuccess && M > 0) {
+                T* At = a + (rs + nl) + (rs + bw) * lda;
+                const long long tiles = (M + kGemmBM - 1) / kGemmBM;
+                const int z = s1_splits(tiles, m, num_sms);
+                // W = (At U) T
+                err = s1_gemm<T, false, false>(M, nl, m, T(1), At, lda, V, m, T(0), Wp, M, s, z, zs);
+                if (err == cudaSuccess) {
+                    s1_reduce_tri_kernel<T><<<std::min<unsigned>(vec_grid, (unsigned)((M + 127) / 128)), 128, 0, s>>>(
+                        Wp, z, zs, W, M, 1, M, nl, Tm);
+                    err = cudaGetLastError();
+                }
+                // At -= W U^T
+                if (err == cudaSuccess) err = s1_gemm<T, false, true>(M, m, nl, T(-1), W, M, V, m, T(1), At, lda, s);
+            }
         }
     }
     return err;
@@ -239,9 +467,9 @@ bb_status s1_fail(bb_status st, const char* msg) {
 }
 }  // namespace
 
-extern "C" int64_t bb_dense_to_band_workspace(int64_t n, bb_dtype dtype) {
-    if (n < 1 || (dtype != BB_F32 && dtype != BB_F64)) return -1;
-    return (2 * n + 16) * (dtype == BB_F64 ? 8 : 4);
+extern "C" int64_t bb_dense_to_band_workspace(int64_t n, int64_t bw, bb_dtype dtype) {
+    if (n < 1 || n >= (int64_t)1 << 30 || bw < 1 || (dtype != BB_F32 && dtype != BB_F64)) return -1;
+    return bb::s1_workspace_elems(n, bw) * (dtype == BB_F64 ? 8 : 4);
 }
 
 extern "C" bb_status bb_dense_to_band(bb_dtype dtype, int64_t n, int64_t bw, void* a, int64_t lda, void* workspace,
@@ -249,7 +477,7 @@ extern "C" bb_status bb_dense_to_band(bb_dtype dtype, int64_t n, int64_t bw, voi
     if (dtype != BB_F32 && dtype != BB_F64) return s1_fail(BB_ERR_DTYPE, "bb_dense_to_band: float32 or float64 only");
     if (n < 1 || n >= (int64_t)1 << 30 || bw < 1 || lda < n)
         return s1_fail(BB_ERR_INVALID_ARG, "bb_dense_to_band: need 1 <= n < 2^30, bw >= 1, lda >= n");
-    if (workspace_bytes < bb_dense_to_band_workspace(n, dtype))
+    if (workspace_bytes < bb_dense_to_band_workspace(n, bw, dtype))
         return s1_fail(BB_ERR_INVALID_ARG, "bb_dense_to_band: workspace smaller than bb_dense_to_band_workspace");
     if (!a || !workspace || !device_ptr(a) || !device_ptr(workspace))
         return s1_fail(BB_ERR_INVALID_ARG, "bb_dense_to_band: a and workspace must be device pointers");

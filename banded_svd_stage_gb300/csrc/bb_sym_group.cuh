@@ -177,8 +177,9 @@ struct SymChase {
     __device__ static long long min_col(const PassArgs& P, int r, int h) {
         return (h == 0) ? (long long)r : (long long)r + P.bp + (long long)(h - 1) * P.b;
     }
-    template <typename T, int WMAX>
-    __device__ static void unit(const PassArgs& P, const ColBuf<T>& cb, int r, int h, int slot, T* vb, T* taub) {
+    template <typename T, typename ST, int WMAX>
+    __device__ static void unit(const PassArgs& P, const ColBuf<ST>& cb, int r, int h, int slot, T* vb, T* taub) {
+        static_assert(std::is_same<T, ST>::value, "the symmetric chase stores its band in its arithmetic type");
         const GGeom g = gstep(P, r, h);
         T* xb = vb + group_v_stride(WMAX, (int)sizeof(T));
         if (g.w == WMAX) group_sym_step<T, WMAX, true>(cb, g, slot, vb, xb, taub);

@@ -346,13 +346,18 @@ def run_half(w: bi.Workload, steps: int, warmup: int):
                 raise RuntimeError("binary16 reduction failed: " + bb.bb_last_error())
             if i >= warmup:
                 times.append(ev0.elapsed_time(ev1))
+        # per pass: the group kernel on binary16 columns or the binary16 flag kernel
+        names = {3: "pass_group_kernel<float, W, BidiagChase, __half>", 5: "pass_half_kernel"}
+        kernels = [names.get(bb.bb_last_pass_kernel(h, i), "?")
+                   + (f" g={bb.bb_last_pass_group(h, i)}" if bb.bb_last_pass_kernel(h, i) == 3 else "")
+                   for i in range(bb.bb_last_num_passes(h))]
+        launches = int(bb.bb_last_launches(h))
     finally:
         bb.bb_destroy(h)
     ms = statistics.median(times)
     mb = model_bytes_np(w.n, w.bw, w.tw, 2)
     return {"ms": ms, "n": w.n, "bw": w.bw, "tw": w.tw, "dtype": "f16 storage, f32 arithmetic",
-            "effective_gbs": mb / (ms * 1e-3) / 1e9, "kernel": "pass_half_kernel",
-            "launches": int(bb.bb_num_passes(w.bw, w.tw)) + 2}
+            "effective_gbs": mb / (ms * 1e-3) / 1e9, "kernels": kernels, "launches": launches}
 
 
 def stage1_flops(n: int, bw: int) -> float:
@@ -383,7 +388,7 @@ def run_stage1(w: bi.Workload, steps: int, warmup: int):
     pristine = torch.from_numpy(a_np).to(dev)
     a = pristine.clone()
     code = bb.dtype_code(w.dtype)
-    nbytes = bb.bb_dense_to_band_workspace(w.n, code)
+    nbytes = bb.bb_dense_to_band_workspace(w.n, w.bw, code)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     times = []
@@ -401,7 +406,7 @@ def run_stage1(w: bi.Workload, steps: int, warmup: int):
     fl = stage1_flops(w.n, w.bw)
     return {"ms": ms, "n": w.n, "bw": w.bw, "dtype": w.dtype, "gflops": fl / (ms * 1e-3) / 1e9,
             "flops_model": "4 flops per entry of every rank-one application",
-            "kernels": "s1_larfg_kernel, s1_apply_left_kernel, s1_gemv_rows_kernel, s1_rank1_kernel"}
+            "kernels": "s1_panel_kernel, s1_gemm_kernel, s1_tri_kernel"}
 
 
 def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):

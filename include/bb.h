@@ -45,9 +45,13 @@ extern "C" {
  * applies its reflectors in float, and writes every entry it changes back
  * rounded to binary16 (round to nearest even); d and e are binary16 too.
  * The paper runs the method in FP16 as well (Section V).  BB_F16 handles
- * run every pass on one persistent kernel with the flag kernel's progress
- * protocol (BB_PARAM_SCHEDULER does not apply), and are accepted by
- * bb_create, bb_reduce, bb_reduce_host and bb_status_sync only. */
+ * run each pass on the group kernel with binary16 columns in shared memory
+ * (where BB_PARAM_SCHEDULER 0 or 3 picks it, by the rule of bb_reduce, for
+ * reflectors of up to 33 elements; on a band whose column stride is not a
+ * multiple of 16 bytes through an aligned working copy) or on the binary16
+ * flag kernel (every other pass, and every pass under schedulers 1, 2 and
+ * 4); both give bitwise equal results.  They are accepted by bb_create,
+ * bb_reduce, bb_reduce_host and bb_status_sync only. */
 typedef enum { BB_F32 = 0, BB_F64 = 1, BB_F16 = 2 } bb_dtype;
 
 /* Return codes. */
@@ -211,13 +215,14 @@ int64_t bb_num_passes(int64_t bw, int64_t tw);
 bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t);
 
 /* Group-kernel plan of pass `pass` of an n x n reduction (element size
- * elem_bytes, 4 or 8): the sweeps per group g (0 when the group kernel
- * cannot take the pass), the columns of its shared-memory buffer (nslot),
+ * elem_bytes: 4 or 8, or 2 for binary16 storage, whose group kernel takes
+ * reflectors of up to 33 elements): the sweeps per group g (0 when the group
+ * kernel cannot take the pass), the columns of its shared-memory buffer (nslot),
  * the loader's run-ahead in ticks, and the rows a buffered column holds
  * (lds).  group_size as BB_PARAM_GROUP_SIZE (0 = the largest that fits).
  * Host-only, for inspection and tests.  BB_ERR_INVALID_ARG unless
  * 1 <= n < 2^30, 0 <= bw < n, 1 <= tw <= max(1, bw - 1), the pass is in the
- * plan, elem_bytes is 4 or 8 and group_size >= 0. */
+ * plan, elem_bytes is 2, 4 or 8 and group_size >= 0. */
 bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
                         int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds);
 
@@ -244,8 +249,9 @@ int64_t bb_model_steps(int64_t n, int64_t bw, int64_t tw, int64_t pass);
 int64_t bb_last_launches(const bb_handle* h);
 
 /* Kernel that ran pass i of the last reduction: 1 per-cycle, 2 flag kernel,
- * 3 group kernel, 4 per-cycle launches replayed from a CUDA graph, 5 the
- * binary16 storage kernel (-1 if out of range), and, for the group kernel,
+ * 3 group kernel (for BB_F16 handles: with binary16 columns), 4 per-cycle
+ * launches replayed from a CUDA graph, 5 the binary16 flag kernel (-1 if out
+ * of range), and, for the group kernel,
  * its group size (sweeps per CTA; 0 otherwise).  With scheduler 4, bb_last_launches counts the kernels the
  * graphs ran. */
 int64_t bb_last_pass_kernel(const bb_handle* h, int64_t i);
@@ -318,12 +324,20 @@ bb_status bb_singular_values_lanes(bb_dtype dtype, int64_t n, const void* d, con
  * A(j.., j), LAPACK xLARFG convention, applied from the left to every later
  * column), then LQ of the panel's rows right of the band (the reflector of
  * A(i, i+bw ..), applied from the right to every later row).  Entries outside
- * the band (0 <= j - i <= bw) become exactly zero.  workspace: device memory
- * of at least bb_dense_to_band_workspace(n, dtype) bytes, owned by the caller
- * and not read afterwards.  Asynchronous on `stream` (one or two kernel
- * launches per reflector); the return code covers arguments and launches.
- * bb_dense_to_band_workspace returns -1 for invalid arguments. */
-int64_t bb_dense_to_band_workspace(int64_t n, bb_dtype dtype);
+ * the band (0 <= j - i <= bw) become exactly zero.  Blocked, 16 reflectors
+ * at a time (a panel's QR reflectors in order, then its LQ reflectors): one
+ * kernel factorizes the block (reflectors, and the T of their compact WY
+ * form, LAPACK xLARFT), and the rest of the matrix is updated by matrix
+ * products, A -= V T^T (V^T A) for QR blocks and A -= (A U) T U^T for LQ
+ * blocks; the result equals the reflector-by-reflector sequence up to
+ * rounding.  workspace: device memory of at least
+ * bb_dense_to_band_workspace(n, bw, dtype) bytes (18 n b + b^2 + 2 b + 64
+ * elements, b = min(bw, n, 16)), owned by the caller and not read
+ * afterwards.  Asynchronous on `stream` (per block of reflectors: one panel
+ * kernel, two matrix products, one reduction); the return code covers
+ * arguments and launches.  bb_dense_to_band_workspace returns -1 for
+ * invalid arguments (n < 1, n >= 2^30, bw < 1, dtype). */
+int64_t bb_dense_to_band_workspace(int64_t n, int64_t bw, bb_dtype dtype);
 bb_status bb_dense_to_band(bb_dtype dtype, int64_t n, int64_t bw, void* a, int64_t lda, void* workspace,
                            int64_t workspace_bytes, bb_stream_t stream);
 

@@ -126,10 +126,19 @@ def test_pass_count_is_arithmetic_and_bounded(lib):
 
 
 def test_group_plan_rejects_inconsistent_shapes(lib):
-    for args in ((100, 100, 8, 4, 0), (100, 16, 0, 4, 0), (100, 16, 16, 4, 0), (100, 16, 8, 2, 0),
+    for args in ((100, 100, 8, 4, 0), (100, 16, 0, 4, 0), (100, 16, 16, 4, 0), (100, 16, 8, 3, 0),
                  (0, 0, 1, 4, 0), (100, 16, 8, 4, -1)):
         with pytest.raises(bb.BBError):
             bb.bb_group_plan(*args)
+
+
+def test_group_plan_of_binary16_storage(lib):
+    # elem_bytes 2: binary16 columns (rows rounded to 8 elements = 16 bytes),
+    # float scratch; reflectors of more than 33 elements have no group kernel
+    g, nslot, ahead, lds = bb.bb_group_plan(4096, 16, 8, 2, 0)
+    assert g == 13 and lds % 8 == 0 and lds >= 2 * 8 + 16 + 1
+    assert bb.bb_group_plan(4096, 16, 8, 4, 0)[1] == nslot
+    assert bb.bb_group_plan(4096, 128, 64, 2, 0)[0] == 0
 
 
 def test_singular_value_lanes_are_validated_without_a_gpu(lib):

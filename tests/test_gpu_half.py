@@ -104,15 +104,70 @@ def test_half_host_entry_and_grid_independence():
         e = np.zeros(n - 1, np.float16)
         src = band.copy()
         bb.bb_reduce_host(h, src, band.shape[1], tw, d, e)
-        assert [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))] == \
-            [5] * bb.bb_num_passes(bw, tw)
+        # the group kernel (3) where at least 5 sweeps' binary16 columns fit,
+        # else the binary16 flag kernel (5)
+        want = [3 if bb.bb_group_plan(n, bw, tw, 2, p)[0] >= 5 else 5 for p in range(bb.bb_num_passes(bw, tw))]
+        assert [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))] == want
+        assert 3 in want
     finally:
         bb.bb_destroy(h)
     assert np.array_equal(src, band)
     assert np.array_equal(d, d0) and np.array_equal(e, e0)
 
 
-def test_half_stalled_sweep_times_out_and_context_survives():
+def half_kernels(band, n, bw, tw, params):
+    """(d, e, band after, [(kernel, group) per pass]) of bb_reduce on cuda:0."""
+    dev = torch.device("cuda:0")
+    x = torch.from_numpy(np.ascontiguousarray(band)).to(dev)
+    d = torch.empty(n, dtype=x.dtype, device=dev)
+    e = torch.empty(max(n - 1, 1), dtype=x.dtype, device=dev)
+    h = bb.bb_create(n, bw, bb.BB_F16)
+    try:
+        for k, v in params.items():
+            bb.bb_set_param(h, k, v)
+        s = torch.cuda.current_stream(dev)
+        bb.bb_reduce(h, x, band.shape[1], tw, d, e, s)
+        assert bb.bb_status_sync(h, s) == bb.BB_OK, bb.bb_last_error()
+        ks = [(bb.bb_last_pass_kernel(h, i), bb.bb_last_pass_group(h, i)) for i in range(bb.bb_last_num_passes(h))]
+    finally:
+        bb.bb_destroy(h)
+    return d.cpu().numpy(), e[: max(n - 1, 0)].cpu().numpy(), x.cpu().numpy(), ks
+
+
+# one and several groups, ragged tails, reflectors of 8, 9, 13, 17 and 33
+# elements, b - t = 1 passes; ldab of the storage layout (unaligned: through
+# the working copy) and padded to a multiple of 8 (aligned: in place)
+HALF_GROUP_CASES = [(64, 16, 8, None), (257, 8, 7, None), (300, 40, 12, None), (1000, 64, 16, None),
+                    (600, 96, 32, None), (2000, 16, 8, None), (700, 24, 8, 48), (513, 33, 16, 72)]
+
+
+@pytest.mark.parametrize("n,bw,tw,ldab", HALF_GROUP_CASES)
+def test_half_group_kernel_bitwise_equals_flag_kernel(n, bw, tw, ldab):
+    band = half_band(n, bw, tw, seed=n + bw, ldab=ldab)
+    d2, e2, b2, k2 = half_kernels(band, n, bw, tw, {bb.BB_PARAM_SCHEDULER: 2})
+    d3, e3, b3, k3 = half_kernels(band, n, bw, tw, {bb.BB_PARAM_SCHEDULER: 3})
+    assert all(k == 5 for k, _ in k2)
+    planned = [bb.bb_group_plan(n, bw, tw, 2, p)[0] for p in range(len(k3))]
+    assert [k for k, _ in k3] == [3 if g > 0 else 5 for g in planned] and 3 in [k for k, _ in k3]
+    record("half_group_vs_flag", n=n, bw=bw, tw=tw, kernels=k3)
+    assert np.array_equal(d2, d3) and np.array_equal(e2, e3)
+    assert np.array_equal(b2.view(np.uint16), b3.view(np.uint16))
+
+
+@pytest.mark.parametrize("group_size,max_ctas", [(1, 0), (3, 2), (13, 1), (6, 0)])
+def test_half_group_sizes_and_grid_caps(group_size, max_ctas):
+    n, bw, tw = 700, 16, 8
+    band = half_band(n, bw, tw, seed=9)
+    ref = half_kernels(band, n, bw, tw, {bb.BB_PARAM_SCHEDULER: 2})
+    got = half_kernels(band, n, bw, tw, {bb.BB_PARAM_SCHEDULER: 3, bb.BB_PARAM_GROUP_SIZE: group_size,
+                                         bb.BB_PARAM_MAX_CTAS: max_ctas})
+    assert got[3] == [(3, group_size)] * len(got[3])
+    for a, b in zip(ref[:3], got[:3]):
+        assert np.array_equal(np.asarray(a).view(np.uint16), np.asarray(b).view(np.uint16))
+
+
+@pytest.mark.parametrize("scheduler", [2, 3])
+def test_half_stalled_sweep_times_out_and_context_survives(scheduler):
     n, bw, tw = 800, 16, 8
     band = half_band(n, bw, tw, seed=2)
     dev = torch.device("cuda:0")
@@ -121,11 +176,13 @@ def test_half_stalled_sweep_times_out_and_context_survives():
     e = torch.empty(n - 1, dtype=torch.float16, device=dev)
     h = bb.bb_create(n, bw, bb.BB_F16)
     try:
+        bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, scheduler)
         bb.bb_set_param(h, bb.BB_PARAM_WAIT_BUDGET_MS, 50)
         bb.bb_set_param(h, bb.BB_PARAM_STALL_SWEEP, 5)
         s = torch.cuda.current_stream(dev)
         bb.bb_reduce(h, x, band.shape[1], tw, d, e, s)
         assert bb.bb_status_sync(h, s) == bb.BB_ERR_TIMEOUT
+        assert bb.bb_last_pass_kernel(h, 0) == (3 if scheduler == 3 else 5)
         bb.bb_set_param(h, bb.BB_PARAM_STALL_SWEEP, -1)
         x.copy_(torch.from_numpy(band).to(dev))
         bb.bb_reduce(h, x, band.shape[1], tw, d, e, s)

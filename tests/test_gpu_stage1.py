@@ -1,5 +1,5 @@
 """Stage 1 on the GPU (bb_dense_to_band: dense -> upper band by block
-Householder) against the oracle's stage 1 (oracle.dense_to_band), and the two
+Householder, panels plus matrix-product updates) against the oracle's stage 1 (oracle.dense_to_band), and the two
 stages chained on the GPU (bb_dense_to_band, bb_pack_band, bb_reduce).
 
 Bars:
@@ -33,7 +33,7 @@ def gpu_stage1(a: np.ndarray, bw: int):
     dt = "f64" if a.dtype == np.float64 else "f32"
     code = bb.dtype_code(dt)
     x = torch.from_numpy(np.ascontiguousarray(a.T)).to(dev)  # column-major n x n
-    nbytes = bb.bb_dense_to_band_workspace(n, code)
+    nbytes = bb.bb_dense_to_band_workspace(n, bw, code)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     s = torch.cuda.current_stream(dev)
     bb.bb_dense_to_band(code, n, bw, x, n, ws, nbytes, s)
@@ -138,8 +138,9 @@ def test_stage1_argument_errors():
     dev = torch.device("cuda:0")
     n = 16
     x = torch.zeros((n, n), dtype=torch.float64, device=dev)
-    nbytes = bb.bb_dense_to_band_workspace(n, bb.BB_F64)
-    assert nbytes >= 2 * n * 8 and bb.bb_dense_to_band_workspace(0, bb.BB_F64) == -1
+    nbytes = bb.bb_dense_to_band_workspace(n, 4, bb.BB_F64)
+    assert nbytes == (18 * n * 4 + 16 + 8 + 64) * 8 and bb.bb_dense_to_band_workspace(0, 4, bb.BB_F64) == -1
+    assert bb.bb_dense_to_band_workspace(n, 0, bb.BB_F64) == -1
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     with pytest.raises(bb.BBError):
         bb.bb_dense_to_band(bb.BB_F64, n, 4, x, n, ws, nbytes - 8)       # workspace too small

@@ -231,7 +231,7 @@ def simulate(n, bw, tw, elem, pass_index, r0, seed, sym=False):
 
 
 @pytest.mark.parametrize("n,bw,tw,elem", [(200, 16, 8, 4), (150, 9, 8, 8), (300, 24, 7, 4), (160, 12, 5, 8),
-                                          (257, 8, 7, 8), (400, 40, 12, 8)])
+                                          (257, 8, 7, 8), (400, 40, 12, 8), (200, 16, 8, 2), (300, 24, 7, 2)])
 def test_buffer_protocol_random_interleavings(n, bw, tw, elem):
     npass = bb.bb_num_passes(bw, tw)
     checked = 0
