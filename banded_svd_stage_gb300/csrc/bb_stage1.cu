@@ -13,8 +13,9 @@
 //   A(i, i+bw ..) is applied from the right to every later row.
 // Annihilated entries are set to exactly zero.
 //
-// Blocked (compact WY) form of that sequence, kInner reflectors at a time
-// (the QR reflectors of a panel in order, then its LQ reflectors in order):
+// Blocked (compact WY) form of that sequence, kInner reflectors at a time,
+// or fewer where the block would not fit shared memory (the QR reflectors
+// of a panel in order, then its LQ reflectors in order):
 //   1. s1_panel_kernel (one CTA) factorizes a block of kInner columns:
 //      reflector j is built from P(j.., j) and applied to the block's later
 //      columns only; it writes V (unit lower trapezoidal), tau and the upper
@@ -41,6 +42,11 @@
 
 namespace bb {
 
+// Inner block: reflectors per panel-kernel call; the rest of the matrix is
+// updated after every kInner reflectors.
+constexpr int kInner = 16;
+// Most partial products of a split inner dimension.
+constexpr int kMaxSplit = 16;
 constexpr int kPanelThreads = 512;
 constexpr int kPanelWarps = kPanelThreads / 32;
 constexpr int kDotChunk = 16;  // dot products are reduced kDotChunk at a time
@@ -223,6 +229,193 @@ s1_panel_kernel(T* __restrict__ p, long long si, long long sc, int m, int nc, in
     }
 }
 
+// Panel factorization as s1_panel_kernel, with the panel staged in shared
+// memory (m x nc, column-major, ld m) when it fits: one copy in, the steps
+// on shared memory, one copy out.  v_j is kept below the diagonal of
+// column j (LAPACK's storage) and beta aside until the copy out, which
+// writes beta and the zeros to the matrix and v (1 on the diagonal) to V.
+// The operations and their order per entry are those of s1_panel_kernel.
+constexpr size_t kPanelSmemMax = 200 * 1024;
+template <typename T>
+__global__ void __launch_bounds__(kPanelThreads)
+s1_panel_smem_kernel(T* __restrict__ p, long long si, long long sc, int m, int nc, int nq, T* __restrict__ V,
+                     T* __restrict__ tau_out, T* __restrict__ Tm_out) {
+    extern __shared__ __align__(16) unsigned char s1_smem[];
+    T* Ps = reinterpret_cast<T*>(s1_smem);  // m x nc
+    __shared__ T red[kPanelWarps];
+    __shared__ T part[kPanelWarps][kDotChunk];
+    __shared__ T sdots[kInner];
+    __shared__ T sbeta[kInner], stau[kInner];
+    __shared__ T sT[kInner * kInner];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    // copy in, consecutive threads on the matrix's contiguous index (32-bit
+    // indices: the panel has at most kPanelSmemMax / sizeof(T) entries)
+    if (sc == 1) {  // rows of the matrix: lane group c = tid % kInner of row i
+        const int c = tid % kInner;
+        for (int i = tid / kInner; i < m; i += kPanelThreads / kInner)
+            if (c < nc) Ps[i + c * m] = p[(long long)i * si + c];
+    } else {
+        for (int c = 0; c < nc; ++c)
+            for (int i = tid; i < m; i += kPanelThreads) Ps[i + c * m] = p[i + (long long)c * sc];
+    }
+    __syncthreads();
+    auto P = [&](int i, int c) -> T& { return Ps[i + c * m]; };
+    for (int j = 0; j < nq; ++j) {
+        const T alpha = P(j, j);
+        T ss = 0;
+        for (int i = j + 1 + tid; i < m; i += kPanelThreads) {
+            const T x = P(i, j);
+            ss = fma(x, x, ss);
+        }
+        ss = s1_block_sum(ss, red);
+        T beta, tau, scal, mult = T(1);
+        int knt = 0;
+        bool identity = false;
+        if (isfinite(ss) && ss >= Lim<T>::min_normal()) {
+            const T nrm = dev_sqrt(fma(alpha, alpha, ss));
+            beta = (alpha >= T(0)) ? -nrm : nrm;
+        } else {
+            T amax = 0;
+            for (int i = j + 1 + tid; i < m; i += kPanelThreads) amax = fmax(amax, fabs(P(i, j)));
+            const T scale = s1_block_max(amax, red);
+            if (scale == T(0)) {
+                identity = true;
+                beta = alpha;
+            } else {
+                T s2 = 0;
+                for (int i = j + 1 + tid; i < m; i += kPanelThreads) {
+                    const T u = P(i, j) / scale;
+                    s2 = fma(u, u, s2);
+                }
+                s2 = s1_block_sum(s2, red);
+                const T xnorm = scale * dev_sqrt(s2);
+                beta = (alpha >= T(0)) ? -dev_hypot(alpha, xnorm) : dev_hypot(alpha, xnorm);
+                const T safmin = Lim<T>::safmin();
+                if (fabs(beta) < safmin) {
+                    const T rsafmn = T(1) / safmin;
+                    T a2 = alpha;
+                    do {
+                        ++knt;
+                        mult = mult * rsafmn;
+                        beta = beta * rsafmn;
+                        a2 = a2 * rsafmn;
+                    } while (fabs(beta) < safmin && knt < 20);
+                    const T xn2 = xnorm * mult;
+                    beta = (a2 >= T(0)) ? -dev_hypot(a2, xn2) : dev_hypot(a2, xn2);
+                    tau = (beta - a2) / beta;
+                    scal = T(1) / (a2 - beta);
+                }
+            }
+        }
+        if (!identity && knt == 0) {
+            tau = (beta - alpha) / beta;
+            scal = T(1) / (alpha - beta);
+        }
+        if (identity) {
+            tau = T(0);
+            scal = T(0);
+        }
+        // v_j below the diagonal (each thread its own rows: the rows it reads
+        // next), 1 on the diagonal
+        for (int i = j + 1 + tid; i < m; i += kPanelThreads) {
+            T& x = P(i, j);
+            x = identity ? T(0) : (x * mult) * scal;
+        }
+        if (tid == 0) {
+            T b = beta;
+            for (int q = 0; q < knt; ++q) b = b * Lim<T>::safmin();
+            sbeta[j] = b;
+            stau[j] = tau;
+            P(j, j) = T(1);
+        }
+        __syncthreads();
+        const int R = (tau != T(0)) ? nc - 1 : j;
+        for (int c0 = 0; c0 < R; c0 += kDotChunk) {
+            const int cn = min(kDotChunk, R - c0);
+            T d[kDotChunk];
+#pragma unroll
+            for (int q = 0; q < kDotChunk; ++q) d[q] = T(0);
+            if (tau != T(0)) {
+                for (int i = j + tid; i < m; i += kPanelThreads) {
+                    const T vi = P(i, j);
+#pragma unroll
+                    for (int q = 0; q < kDotChunk; ++q) {
+                        if (q < cn) {
+                            const int c = (c0 + q < j) ? c0 + q : c0 + q + 1;
+                            // v_c(i) for an earlier reflector (i >= j > c: below its diagonal)
+                            d[q] = fma(vi, P(i, c), d[q]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kDotChunk; ++q) {
+                const T w = warp_sum(d[q]);
+                if (lane == 0) part[warp][q] = w;
+            }
+            __syncthreads();
+            for (int q = tid; q < cn; q += kPanelThreads) {
+                T sum = 0;
+#pragma unroll
+                for (int w = 0; w < kPanelWarps; ++w) sum += part[w][q];
+                sdots[(c0 + q < j) ? c0 + q : c0 + q + 1] = sum;
+            }
+            __syncthreads();
+        }
+        if (tau != T(0)) {
+            for (int i = j + tid; i < m; i += kPanelThreads) {
+                const T vi = P(i, j);
+                for (int c = j + 1; c < nc; ++c) P(i, c) = fma(-(tau * sdots[c]), vi, P(i, c));
+            }
+        }
+        for (int l = tid; l <= j; l += kPanelThreads) {
+            T t = tau;
+            if (l < j) {
+                T sum = 0;
+                for (int q = l; q < j; ++q) sum = fma(sT[l + q * nq], sdots[q], sum);
+                t = -tau * sum;
+            }
+            sT[l + j * nq] = t;
+        }
+        __syncthreads();
+    }
+    // copy out: R and the zeros to the matrix, v to V, tau and T
+    auto out_of = [&](int i, int c) -> T {
+        if (c < nq) {
+            if (i > c) return T(0);
+            if (i == c) return sbeta[c];
+        }
+        return P(i, c);
+    };
+    if (sc == 1) {
+        const int c = tid % kInner;
+        for (int i = tid / kInner; i < m; i += kPanelThreads / kInner)
+            if (c < nc) p[(long long)i * si + c] = out_of(i, c);
+    } else {
+        for (int c = 0; c < nc; ++c)
+            for (int i = tid; i < m; i += kPanelThreads) p[i + (long long)c * sc] = out_of(i, c);
+    }
+    for (int c = 0; c < nq; ++c)
+        for (int i = tid; i < m; i += kPanelThreads)
+            V[i + (long long)c * m] = (i < c) ? T(0) : (i == c) ? T(1) : P(i, c);
+    for (int e = tid; e < nq * nq; e += kPanelThreads) Tm_out[e] = sT[e];
+    for (int e = tid; e < nq; e += kPanelThreads) tau_out[e] = stau[e];
+}
+
+// Launch of one panel factorization: shared memory when the panel fits.
+template <typename T>
+static cudaError_t s1_panel(T* p, long long si, long long sc, int m, int nc, int nq, T* V, T* tau, T* Tm, T* dots,
+                            cudaStream_t s) {
+    const size_t bytes = sizeof(T) * (size_t)m * (size_t)nc;
+    if (bytes <= kPanelSmemMax) {  // (run_stage1 raised the kernel's dynamic shared memory limit)
+        s1_panel_smem_kernel<T><<<1, kPanelThreads, bytes, s>>>(p, si, sc, m, nc, nq, V, tau, Tm);
+    } else {
+        s1_panel_kernel<T><<<1, kPanelThreads, 0, s>>>(p, si, sc, m, nc, nq, V, tau, Tm, dots);
+    }
+    return cudaGetLastError();
+}
+
 // C = alpha op(A) op(B) + beta C, column-major (M x N, inner dimension K):
 // op(A)(i, l) = TA ? A[l + i lda] : A[i + l lda], op(B)(l, j) = TB ?
 // B[j + l ldb] : B[l + j ldb].  64 x 64 tiles of C per CTA, 16 x 16 threads
@@ -317,36 +510,38 @@ static cudaError_t s1_gemm(int M, int N, int K, T alpha, const T* A, long long l
     return cudaSuccess;
 }
 
-// Inner block: reflectors per panel-kernel call; the rest of the matrix is
-// updated after every kInner reflectors.
-constexpr int kInner = 16;
-// Most partial products of a split inner dimension.
-constexpr int kMaxSplit = 16;
-
 // W[q qs + j ls] = sum_{l <= j} T(l, j) w_l, w_l = sum_z Wp[z zs + q qs + l ls]
 // (z ascending), for the nvec vectors q of nb <= kInner entries: with
-// columns of W this is T^T W, with rows W T.
+// columns of W this is T^T W, with rows W T.  A block takes kInner vectors,
+// one thread per entry: the partial sums are added with consecutive threads
+// on the contiguous index (l when ls == 1, else q), the vectors staged in
+// shared memory, then each thread forms one output entry.
 template <typename T>
-__global__ void s1_reduce_tri_kernel(const T* __restrict__ Wp, int nsplit, long long zs, T* __restrict__ W,
-                                     int nvec, long long qs, long long ls, int nb, const T* __restrict__ Tm) {
-    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < nvec; q += gridDim.x * blockDim.x) {
-        T w[kInner];
-#pragma unroll
-        for (int l = 0; l < kInner; ++l) {
-            T sum = 0;
-            if (l < nb)
-                for (int z = 0; z < nsplit; ++z) sum += Wp[z * zs + (long long)q * qs + (long long)l * ls];
-            w[l] = sum;
+__global__ void __launch_bounds__(kInner * kInner)
+s1_reduce_tri_kernel(const T* __restrict__ Wp, int nsplit, long long zs, T* __restrict__ W, int nvec,
+                     long long qs, long long ls, int nb, const T* __restrict__ Tm) {
+    __shared__ T w[kInner][kInner + 1];  // [vector][entry]
+    __shared__ T t[kInner * kInner];
+    const int tid = threadIdx.x;
+    const bool l_fast = (ls == 1);
+    const int a = tid % kInner, b2 = tid / kInner;
+    const int l = l_fast ? a : b2, qq = l_fast ? b2 : a;  // entry l of vector qq of the block
+    if (tid < nb * nb) t[tid] = Tm[tid];
+    for (int q0 = blockIdx.x * kInner; q0 < nvec; q0 += gridDim.x * kInner) {
+        const int q = q0 + qq;
+        T sum = 0;
+        if (q < nvec && l < nb) {
+            const long long off = (long long)q * qs + (long long)l * ls;
+            for (int z = 0; z < nsplit; ++z) sum += Wp[z * zs + off];
         }
-#pragma unroll
-        for (int j = 0; j < kInner; ++j) {
-            if (j < nb) {
-                T sum = 0;
-#pragma unroll
-                for (int l = 0; l <= j; ++l) sum = fma(Tm[l + (long long)j * nb], w[l], sum);
-                W[(long long)q * qs + (long long)j * ls] = sum;
-            }
+        w[qq][l] = sum;
+        __syncthreads();
+        if (q < nvec && l < nb) {
+            T out = 0;
+            for (int k = 0; k <= l; ++k) out = fma(t[k + l * nb], w[qq][k], out);
+            W[(long long)q * qs + (long long)l * ls] = out;
         }
+        __syncthreads();
     }
 }
 
@@ -373,11 +568,25 @@ static long long s1_workspace_elems(long long n, long long bw) {
 }
 
 // Partial products for a product of nvec x nb outputs with a long inner
-// dimension K: enough to give the GPU a few waves of CTAs.
+// dimension K: enough for several CTAs per SM, at least 256 of K each.
 static int s1_splits(long long tiles, long long K, int num_sms) {
-    long long z = (2LL * num_sms + tiles - 1) / std::max(1LL, tiles);
+    long long z = (8LL * num_sms + tiles - 1) / std::max(1LL, tiles);
     z = std::min<long long>(z, std::max(1LL, K / 256));
     return (int)std::max(1LL, std::min<long long>(z, kMaxSplit));
+}
+
+// Reflectors per block for a panel of m rows: kInner, or fewer so that the
+// block fits the shared-memory panel kernel; below the narrowest width
+// worth its extra passes over the trailing matrix (1 in float; 8 in double,
+// whose products are bound by the FP64 rate) the global-memory panel kernel
+// takes kInner.  Measured on a dense 4096 x 4096, bw 16: float 174 -> 105
+// ms with narrowing down to 1; double 917 ms without narrowing, 1425 ms
+// narrowing down to 6.
+template <typename T>
+static int s1_block_width(long long m, long long nb) {
+    const long long fit = (long long)(kPanelSmemMax / sizeof(T)) / std::max(1LL, m);
+    const long long narrowest = std::min<long long>(nb, sizeof(T) == 8 ? 8 : 1);
+    return (int)(fit >= narrowest ? std::min(nb, fit) : nb);
 }
 
 template <typename T>
@@ -391,19 +600,20 @@ static cudaError_t run_stage1(T* a, long long n, long long lda, int bw, T* ws, i
     T* dots = tau + nb;
     const long long zs = n * nb;
     const unsigned vec_grid = (unsigned)std::max(1, 4 * num_sms);
-    cudaError_t err = cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(s1_panel_smem_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kPanelSmemMax);
     for (long long k = 0; k < n && err == cudaSuccess; k += bw) {
         const long long kb = std::min(k + bw, n);
         // QR of columns k .. kb-1, kInner reflectors at a time: reflectors
         // j = cs .. cs+nq-1 (j < min(kb, n-1)) on the sub-panel of columns
         // cs .. cs+nc-1, then columns cs+nc .. n-1 of rows cs .. updated
         const long long qend = std::min(kb, n - 1);
-        for (long long cs = k; cs < qend && err == cudaSuccess; cs += nb) {
-            const int nq = (int)std::min<long long>(nb, qend - cs);
-            const int nc = (int)std::min<long long>(nb, kb - cs);
+        for (long long cs = k, nbs = 0; cs < qend && err == cudaSuccess; cs += nbs) {
+            nbs = s1_block_width<T>(n - cs, nb);
+            const int nq = (int)std::min<long long>(nbs, qend - cs);
+            const int nc = (int)std::min<long long>(nbs, kb - cs);
             const int m = (int)(n - cs);
-            s1_panel_kernel<T><<<1, kPanelThreads, 0, s>>>(a + cs + cs * lda, 1, lda, m, nc, nq, V, tau, Tm, dots);
-            err = cudaGetLastError();
+            err = s1_panel<T>(a + cs + cs * lda, 1, lda, m, nc, nq, V, tau, Tm, dots, s);
             const int N = (int)(n - cs - nc);
             if (err == cudaSuccess && N > 0) {
                 T* At = a + cs + (cs + nc) * lda;  // rows cs .., columns cs + nc ..
@@ -412,8 +622,8 @@ static cudaError_t run_stage1(T* a, long long n, long long lda, int bw, T* ws, i
                 // W = T^T (V^T At)
                 err = s1_gemm<T, true, false>(nq, N, m, T(1), V, m, At, lda, T(0), Wp, nq, s, z, zs);
                 if (err == cudaSuccess) {
-                    s1_reduce_tri_kernel<T><<<std::min<unsigned>(vec_grid, (unsigned)((N + 127) / 128)), 128, 0, s>>>(
-                        Wp, z, zs, W, N, nq, 1, nq, Tm);
+                    s1_reduce_tri_kernel<T><<<std::min<unsigned>(vec_grid, (unsigned)((N + kInner - 1) / kInner)),
+                                              kInner * kInner, 0, s>>>(Wp, z, zs, W, N, nq, 1, nq, Tm);
                     err = cudaGetLastError();
                 }
                 // At -= V W
@@ -424,12 +634,12 @@ static cudaError_t run_stage1(T* a, long long n, long long lda, int bw, T* ws, i
         // reflectors i = rs .. rs+nl-1 (i + bw + 1 < n) on the block rows
         // rs .., columns rs + bw ..; then rows rs+nl .. n-1 of those columns
         const long long lend = std::min(kb, n - 1 - bw);
-        for (long long rs = k; rs < lend && err == cudaSuccess; rs += nb) {
-            const int nl = (int)std::min<long long>(nb, lend - rs);
+        for (long long rs = k, nbs = 0; rs < lend && err == cudaSuccess; rs += nbs) {
+            nbs = s1_block_width<T>(n - rs - bw, nb);
+            const int nl = (int)std::min<long long>(nbs, lend - rs);
             const int m = (int)(n - rs - bw);  // columns rs + bw .. n-1
             T* B = a + rs + (rs + bw) * lda;   // B(r, c) = A(rs + r, rs + bw + c)
-            s1_panel_kernel<T><<<1, kPanelThreads, 0, s>>>(B, lda, 1, m, nl, nl, V, tau, Tm, dots);
-            err = cudaGetLastError();
+            err = s1_panel<T>(B, lda, 1, m, nl, nl, V, tau, Tm, dots, s);
             const int M = (int)(n - rs - nl);  // rows rs + nl .. n-1
             if (err == cudaSuccess && M > 0) {
                 T* At = a + (rs + nl) + (rs + bw) * lda;
@@ -438,8 +648,8 @@ static cudaError_t run_stage1(T* a, long long n, long long lda, int bw, T* ws, i
                 // W = (At U) T
                 err = s1_gemm<T, false, false>(M, nl, m, T(1), At, lda, V, m, T(0), Wp, M, s, z, zs);
                 if (err == cudaSuccess) {
-                    s1_reduce_tri_kernel<T><<<std::min<unsigned>(vec_grid, (unsigned)((M + 127) / 128)), 128, 0, s>>>(
-                        Wp, z, zs, W, M, 1, M, nl, Tm);
+                    s1_reduce_tri_kernel<T><<<std::min<unsigned>(vec_grid, (unsigned)((M + kInner - 1) / kInner)),
+                                              kInner * kInner, 0, s>>>(Wp, z, zs, W, M, 1, M, nl, Tm);
                     err = cudaGetLastError();
                 }
                 // At -= W U^T

@@ -710,6 +710,27 @@ def profile_pass(spec: str) -> int:
     return 0 if st == 0 else 1
 
 
+def profile_stage1(spec: str) -> int:
+    """--profile-stage1 N:BW:DTYPE -- one bb_dense_to_band call on a seeded
+    dense N x N matrix (DTYPE f32 or f64) to bandwidth BW, for an ncu launch
+    list of stage 1; prints one line, no timing."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    n_s, bw_s, dt = spec.split(":")
+    n, bw = int(n_s), int(bw_s)
+    torch.cuda.set_device(0)
+    rng = np.random.default_rng(n + bw)
+    a = torch.from_numpy(rng.standard_normal((n, n)).astype(np.float32 if dt == "f32" else np.float64)).cuda()
+    code = bb.dtype_code(dt)
+    nbytes = bb.bb_dense_to_band_workspace(n, bw, code)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    bb.bb_dense_to_band(code, n, bw, a, n, ws, nbytes, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    print(f"profile stage1: n={n} bw={bw} dtype={dt}")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -723,11 +744,15 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (e2e) leg")
+    ap.add_argument("--profile-stage1", default=None, metavar="N:BW:DTYPE",
+                    help="one stage-1 call (dense -> band), for an ncu launch list")
     ap.add_argument("--profile-pass", default=None, metavar="WORKLOAD:N:PASS:SCHEDULER:DTYPE[:MAX_CTAS]",
                     help="run one pass once for a profiler capture and exit (no measurement)")
     args = ap.parse_args()
     if args.profile_pass:
         return profile_pass(args.profile_pass)
+    if args.profile_stage1:
+        return profile_stage1(args.profile_stage1)
     rank, world, local = dist_env()
     w = bi.by_name(args.workload)
 

@@ -92,6 +92,37 @@ def test_two_stages_chained_on_the_gpu(n, bw, tw, dt):
     assert err <= TOL[dt], f"singular values differ by {err:.3e} sigma_1"
 
 
+@pytest.mark.parametrize("n,bw,dt", [(1700, 16, "f64"), (3400, 16, "f32")])
+def test_two_stages_chained_with_tall_panels(n, bw, dt):
+    """Panels taller than the shared-memory panel kernel takes (16 columns
+    of more than 1600 doubles or 3200 floats) go to the global-memory panel
+    kernel: the chain's singular values against LAPACK's SVD of the input,
+    and the exact band form."""
+    rng = np.random.default_rng(n + bw)
+    a = rng.standard_normal((n, n)).astype(np.float32 if dt == "f32" else np.float64)
+    got, x = gpu_stage1(a, bw)
+    assert outside_band_nonzeros(got, bw) == 0
+    tw = 8
+    code = bb.dtype_code(dt)
+    ldab = bb.bb_required_ldab(bw, tw)
+    band = torch.empty((n, ldab), dtype=x.dtype, device=x.device)
+    s = torch.cuda.current_stream(x.device)
+    bb.bb_pack_band(code, n, bw, tw, x, n, band, ldab, s)
+    d = torch.empty(n, dtype=x.dtype, device=x.device)
+    e = torch.empty(n - 1, dtype=x.dtype, device=x.device)
+    h = bb.bb_create(n, bw, code)
+    try:
+        bb.bb_reduce(h, band, ldab, tw, d, e, s)
+        assert bb.bb_status_sync(h, s) == bb.BB_OK
+    finally:
+        bb.bb_destroy(h)
+    sigma = sigma_bidiagonal(d.cpu().numpy(), e.cpu().numpy())
+    ref = np.linalg.svd(a.astype(np.float64), compute_uv=False)
+    err = float(np.abs(sigma - ref).max()) / ref[0]
+    record("two_stages_tall", n=n, bw=bw, dt=dt, err=err)
+    assert err <= TOL[dt], f"singular values differ by {err:.3e} sigma_1"
+
+
 @pytest.mark.parametrize("kind", bi.SPECTRA)
 def test_two_stages_prescribed_spectrum(kind):
     n, bw, tw = 400, 32, 8
