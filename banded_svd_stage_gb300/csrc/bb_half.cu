@@ -218,27 +218,8 @@ bool half_choose_group(const PassArgs& P, int scheduler, int group_size, GroupAr
 template <int WMAX>
 static cudaError_t run_half_group_w(__half* band, const PassArgs& P, const GroupArgs& GA, const HalfLaunch& L,
                                     cudaStream_t s) {
-    auto kern = pass_group_kernel<float, WMAX, BidiagChase, __half>;
-    const size_t smem = group_smem_bytes(GA, WMAX, sizeof(float), BidiagChase::kVecs, sizeof(__half));
-    // always raise the dynamic limit: static shared memory counts against 48 KB too
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 3), smem);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    long long grid = std::min<long long>((long long)per_sm * L.num_sms, GA.ngroups);
-    if (L.max_ctas > 0) grid = std::min<long long>(grid, L.max_ctas);
-    err = cudaMemsetAsync(L.progress, 0, sizeof(int) * (size_t)GA.ngroups, s);
-    if (err != cudaSuccess) return err;
-    __half* band_arg = band;
-    PassArgs p_arg = P;
-    GroupArgs g_arg = GA;
-    int* wm_arg = L.progress;
-    int* stat_arg = L.status;
-    void* args[] = {&band_arg, &p_arg, &g_arg, &wm_arg, &stat_arg};
-    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 3)), args, smem,
-                                       s);
+    return launch_group_pass<float, WMAX, BidiagChase, __half>(band, P, GA, L.num_sms, L.max_ctas, L.progress,
+                                                                L.status, s);
 }
 
 cudaError_t run_half_pass(void* band, const PassArgs& P, const HalfLaunch& L, const GroupArgs* GA,

@@ -51,6 +51,38 @@ inline size_t group_smem_bytes(const GroupArgs& GA, int wmax, size_t elem, int n
     return group_cols_offset(GA.g, wmax, elem, nvec) + (selem ? selem : elem) * (size_t)GA.nslot * GA.lds;
 }
 
+// Cooperative launch of the group kernel (arithmetic T, storage ST, chase
+// Chase) for one pass: as many CTAs as can be co-resident, at most max_ctas
+// (when > 0) and at most one per group; the groups' watermarks wm zeroed
+// first, on the same stream.  *grid_out (if given) receives the grid.
+template <typename T, int WMAX, class Chase, typename ST>
+cudaError_t launch_group_pass(ST* band, const PassArgs& P, const GroupArgs& GA, int num_sms, int max_ctas, int* wm,
+                              int* status, cudaStream_t s, int* grid_out = nullptr) {
+    auto kern = pass_group_kernel<T, WMAX, Chase, ST>;
+    const size_t smem = group_smem_bytes(GA, WMAX, sizeof(T), Chase::kVecs, sizeof(ST));
+    // always raise the dynamic limit: static shared memory counts against 48 KB too
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 3), smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    long long grid = (long long)per_sm * num_sms;
+    if (grid > GA.ngroups) grid = GA.ngroups;
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+    err = cudaMemsetAsync(wm, 0, sizeof(int) * (size_t)GA.ngroups, s);
+    if (err != cudaSuccess) return err;
+    ST* band_arg = band;
+    PassArgs p_arg = P;
+    GroupArgs g_arg = GA;
+    int* wm_arg = wm;
+    int* stat_arg = status;
+    void* args[] = {&band_arg, &p_arg, &g_arg, &wm_arg, &stat_arg};
+    if (grid_out) *grid_out = (int)grid;
+    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 3)), args, smem,
+                                       s);
+}
+
 // Largest group (<= requested, or the most the kernel is compiled for when
 // requested == 0) whose column buffer fits in shared memory; false if not
 // even one sweep fits.  elem: the arithmetic type's size; selem: the

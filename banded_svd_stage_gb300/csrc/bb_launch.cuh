@@ -23,31 +23,13 @@ cudaError_t run_pass_w(T* band, const PassArgs& P, int scheduler, const LaunchCf
     cudaError_t err;
     if (scheduler == 3) {
         if (P.nsweeps <= 0) return cudaSuccess;
-        GroupArgs GA = cfg.group;
-        auto kern = pass_group_kernel<T, WMAX>;
-        const size_t gsmem = group_smem_bytes(GA, WMAX, sizeof(T));
-        // always raise the dynamic limit: static shared memory counts against 48 KB too
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
-        if (err != cudaSuccess) return err;
-        int per_sm = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 3), gsmem);
-        if (err != cudaSuccess) return err;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        long long grid = std::min<long long>((long long)per_sm * cfg.num_sms, GA.ngroups);
-        if (cfg.max_ctas > 0) grid = std::min<long long>(grid, cfg.max_ctas);
-        err = cudaMemsetAsync(progress, 0, sizeof(int) * (size_t)GA.ngroups, stream);
-        if (err != cudaSuccess) return err;
-        T* band_arg = band;
-        PassArgs p_arg = P;
-        GroupArgs g_arg = GA;
-        int* prog_arg = progress;
-        int* stat_arg = status;
-        void* args[] = {&band_arg, &p_arg, &g_arg, &prog_arg, &stat_arg};
-        err = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 3)), args,
-                                          gsmem, stream);
+        const GroupArgs& GA = cfg.group;
+        int grid = 0;
+        err = launch_group_pass<T, WMAX, BidiagChase, T>(band, P, GA, cfg.num_sms, cfg.max_ctas, progress, status,
+                                                         stream, &grid);
         if (stats) {
             stats->launches += 1;
-            stats->grid = (int)grid;
+            stats->grid = grid;
             stats->kernel = 3;
             stats->group = GA.g;
         }

@@ -418,68 +418,91 @@ static cudaError_t s1_panel(T* p, long long si, long long sc, int m, int nc, int
 
 // C = alpha op(A) op(B) + beta C, column-major (M x N, inner dimension K):
 // op(A)(i, l) = TA ? A[l + i lda] : A[i + l lda], op(B)(l, j) = TB ?
-// B[j + l ldb] : B[l + j ldb].  64 x 64 tiles of C per CTA, 16 x 16 threads
-// with 4 x 4 entries each (rows tx + 16 p, columns ty + 16 q), the inner
-// dimension in steps of 16 through shared memory.  beta is 0 (C is not
-// read) or 1.  Split inner dimension: CTA z sums l in [z kchunk, (z + 1)
-// kchunk) into C + z cz (partial products, reduced by the caller).
-constexpr int kGemmBM = 64, kGemmBN = 64, kGemmBK = 16;
-template <typename T, bool TA, bool TB>
+// B[j + l ldb] : B[l + j ldb].  A CTA of 16 x 16 threads computes a
+// (16 PM) x (16 PN) tile of C, each thread PM x PN entries (rows tx + 16 p,
+// columns ty + 16 q), the inner dimension in steps of 16 through shared
+// memory with the next step's tiles fetched into registers meanwhile.
+// PM = PN = 4 for the square products; 1 x 16 and 16 x 1 for the skinny
+// ones (16 rows or columns of output).  beta is 0 (C is not read) or 1.
+// Split inner dimension: CTA z sums l in [z kchunk, (z + 1) kchunk) into
+// C + z cz (partial products, reduced by the caller).
+constexpr int kGemmBK = 16;
+template <typename T, bool TA, bool TB, int PM, int PN>
 __global__ void __launch_bounds__(256)
 s1_gemm_kernel(int M, int N, int K, T alpha, const T* __restrict__ A, long long lda, const T* __restrict__ B,
                long long ldb, T beta, T* __restrict__ C, long long ldc, int kchunk, long long cz) {
-    __shared__ T As[kGemmBK][kGemmBM + 1];
-    __shared__ T Bs[kGemmBK][kGemmBN + 1];
+    constexpr int BM = 16 * PM, BN = 16 * PN;
+    __shared__ T As[kGemmBK][BM + 1];
+    __shared__ T Bs[kGemmBK][BN + 1];
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
-    const int i0 = blockIdx.x * kGemmBM, j0 = blockIdx.y * kGemmBN;
+    const int i0 = blockIdx.x * BM, j0 = blockIdx.y * BN;
     const int lbeg = blockIdx.z * kchunk, lend = min(K, lbeg + kchunk);
     C += blockIdx.z * cz;
-    T acc[4][4];
+    T acc[PM][PN];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < PM; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = T(0);
-    for (int l0 = lbeg; l0 < lend; l0 += kGemmBK) {
-        for (int e = tid; e < kGemmBK * kGemmBM; e += 256) {
-            // consecutive threads on the contiguous index of A
-            const int ii = TA ? e / kGemmBK : e % kGemmBM;
-            const int ll = TA ? e % kGemmBK : e / kGemmBM;
+        for (int b = 0; b < PN; ++b) acc[a][b] = T(0);
+    // tile loads: element e of the 16 x BM (16 x BN) tile, consecutive
+    // threads on the contiguous index of A (B)
+    constexpr int kPerA = kGemmBK * BM / 256, kPerB = kGemmBK * BN / 256;
+    T ra[kPerA], rb[kPerB];
+    auto fetch = [&](int l0) {
+#pragma unroll
+        for (int u = 0; u < kPerA; ++u) {
+            const int e = tid + 256 * u;
+            const int ii = TA ? e / kGemmBK : e % BM;
+            const int ll = TA ? e % kGemmBK : e / BM;
             const int gi = i0 + ii, gl = l0 + ll;
-            T x = T(0);
-            if (gi < M && gl < lend) x = TA ? A[gl + (long long)gi * lda] : A[gi + (long long)gl * lda];
-            As[ll][ii] = x;
+            ra[u] = (gi < M && gl < lend) ? (TA ? A[gl + (long long)gi * lda] : A[gi + (long long)gl * lda]) : T(0);
         }
-        for (int e = tid; e < kGemmBK * kGemmBN; e += 256) {
-            const int jj = TB ? e % kGemmBN : e / kGemmBK;
-            const int ll = TB ? e / kGemmBN : e % kGemmBK;
+#pragma unroll
+        for (int u = 0; u < kPerB; ++u) {
+            const int e = tid + 256 * u;
+            const int jj = TB ? e % BN : e / kGemmBK;
+            const int ll = TB ? e / BN : e % kGemmBK;
             const int gj = j0 + jj, gl = l0 + ll;
-            T x = T(0);
-            if (gj < N && gl < lend) x = TB ? B[gj + (long long)gl * ldb] : B[gl + (long long)gj * ldb];
-            Bs[ll][jj] = x;
+            rb[u] = (gj < N && gl < lend) ? (TB ? B[gj + (long long)gl * ldb] : B[gl + (long long)gj * ldb]) : T(0);
         }
+    };
+    auto stash = [&]() {
+#pragma unroll
+        for (int u = 0; u < kPerA; ++u) {
+            const int e = tid + 256 * u;
+            As[TA ? e % kGemmBK : e / BM][TA ? e / kGemmBK : e % BM] = ra[u];
+        }
+#pragma unroll
+        for (int u = 0; u < kPerB; ++u) {
+            const int e = tid + 256 * u;
+            Bs[TB ? e / BN : e % kGemmBK][TB ? e % BN : e / kGemmBK] = rb[u];
+        }
+    };
+    if (lbeg < lend) fetch(lbeg);
+    for (int l0 = lbeg; l0 < lend; l0 += kGemmBK) {
+        stash();
         __syncthreads();
+        if (l0 + kGemmBK < lend) fetch(l0 + kGemmBK);
 #pragma unroll
         for (int l = 0; l < kGemmBK; ++l) {
-            T a[4], b[4];
+            T a[PM], b[PN];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                a[q] = As[l][tx + 16 * q];
-                b[q] = Bs[l][ty + 16 * q];
-            }
+            for (int q = 0; q < PM; ++q) a[q] = As[l][tx + 16 * q];
 #pragma unroll
-            for (int pa = 0; pa < 4; ++pa)
+            for (int q = 0; q < PN; ++q) b[q] = Bs[l][ty + 16 * q];
 #pragma unroll
-                for (int pb = 0; pb < 4; ++pb) acc[pa][pb] = fma(a[pa], b[pb], acc[pa][pb]);
+            for (int pa = 0; pa < PM; ++pa)
+#pragma unroll
+                for (int pb = 0; pb < PN; ++pb) acc[pa][pb] = fma(a[pa], b[pb], acc[pa][pb]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int pb = 0; pb < 4; ++pb) {
+    for (int pb = 0; pb < PN; ++pb) {
         const int gj = j0 + ty + 16 * pb;
         if (gj >= N) continue;
 #pragma unroll
-        for (int pa = 0; pa < 4; ++pa) {
+        for (int pa = 0; pa < PM; ++pa) {
             const int gi = i0 + tx + 16 * pa;
             if (gi >= M) continue;
             T* c = C + gi + (long long)gj * ldc;
@@ -489,21 +512,32 @@ s1_gemm_kernel(int M, int N, int K, T alpha, const T* __restrict__ A, long long 
 }
 
 // nsplit > 1: nsplit partial products of the inner dimension into C + z cz
-// (beta must be 0).
+// (beta must be 0).  The output shape picks the tile: 16 x 256 when M <= 16,
+// 256 x 16 when N <= 16, else 64 x 64.
 template <typename T, bool TA, bool TB>
 static cudaError_t s1_gemm(int M, int N, int K, T alpha, const T* A, long long lda, const T* B, long long ldb,
                            T beta, T* C, long long ldc, cudaStream_t s, int nsplit = 1, long long cz = 0) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     const int kchunk = (nsplit > 1) ? ((K + nsplit - 1) / nsplit + kGemmBK - 1) / kGemmBK * kGemmBK : K;
+    const int pm = (M <= 16) ? 1 : (N <= 16 ? 16 : 4);
+    const int pn = (M <= 16) ? 16 : (N <= 16 ? 1 : 4);
+    const int bm = 16 * pm, bn = 16 * pn;
     // column blocks of C within the grid's y limit
-    const int nmax = 65535 * kGemmBN;
+    const int nmax = 65535 * bn;
     for (int j0 = 0; j0 < N; j0 += nmax) {
         const int nb = std::min(nmax, N - j0);
         const T* Bj = TB ? B + j0 : B + (long long)j0 * ldb;
-        const dim3 grid((unsigned)((M + kGemmBM - 1) / kGemmBM), (unsigned)((nb + kGemmBN - 1) / kGemmBN),
-                        (unsigned)std::max(1, nsplit));
-        s1_gemm_kernel<T, TA, TB><<<grid, 256, 0, s>>>(M, nb, K, alpha, A, lda, Bj, ldb, beta,
-                                                        C + (long long)j0 * ldc, ldc, kchunk, cz);
+        T* Cj = C + (long long)j0 * ldc;
+        const dim3 grid((unsigned)((M + bm - 1) / bm), (unsigned)((nb + bn - 1) / bn), (unsigned)std::max(1, nsplit));
+        if (pm == 1)
+            s1_gemm_kernel<T, TA, TB, 1, 16><<<grid, 256, 0, s>>>(M, nb, K, alpha, A, lda, Bj, ldb, beta, Cj, ldc,
+                                                                  kchunk, cz);
+        else if (pm == 16)
+            s1_gemm_kernel<T, TA, TB, 16, 1><<<grid, 256, 0, s>>>(M, nb, K, alpha, A, lda, Bj, ldb, beta, Cj, ldc,
+                                                                  kchunk, cz);
+        else
+            s1_gemm_kernel<T, TA, TB, 4, 4><<<grid, 256, 0, s>>>(M, nb, K, alpha, A, lda, Bj, ldb, beta, Cj, ldc,
+                                                                 kchunk, cz);
         const cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
@@ -617,7 +651,7 @@ static cudaError_t run_stage1(T* a, long long n, long long lda, int bw, T* ws, i
             const int N = (int)(n - cs - nc);
             if (err == cudaSuccess && N > 0) {
                 T* At = a + cs + (cs + nc) * lda;  // rows cs .., columns cs + nc ..
-                const long long tiles = (N + kGemmBN - 1) / kGemmBN;
+                const long long tiles = (N + 255) / 256;  // 16 x 256 tiles of W (nq <= 16 rows)
                 const int z = s1_splits(tiles, m, num_sms);
                 // W = T^T (V^T At)
                 err = s1_gemm<T, true, false>(nq, N, m, T(1), V, m, At, lda, T(0), Wp, nq, s, z, zs);
@@ -643,7 +677,7 @@ static cudaError_t run_stage1(T* a, long long n, long long lda, int bw, T* ws, i
             const int M = (int)(n - rs - nl);  // rows rs + nl .. n-1
             if (err == cudaSuccess && M > 0) {
                 T* At = a + (rs + nl) + (rs + bw) * lda;
-                const long long tiles = (M + kGemmBM - 1) / kGemmBM;
+                const long long tiles = (M + 255) / 256;  // 256 x 16 tiles of W (nl <= 16 columns)
                 const int z = s1_splits(tiles, m, num_sms);
                 // W = (At U) T
                 err = s1_gemm<T, false, false>(M, nl, m, T(1), At, lda, V, m, T(0), Wp, M, s, z, zs);

@@ -193,27 +193,7 @@ template <typename T, int WMAX>
 cudaError_t run_sym_group_pass(T* band, const PassArgs& P, const GroupArgs& GA, int num_sms, int max_ctas,
                                int* wm, int* status, cudaStream_t s) {
     if (P.nsweeps <= 0) return cudaSuccess;
-    auto kern = pass_group_kernel<T, WMAX, SymChase>;
-    const size_t smem = group_smem_bytes(GA, WMAX, sizeof(T), SymChase::kVecs);
-    // always raise the dynamic limit: static shared memory counts against 48 KB too
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (GA.g + 3), smem);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    long long grid = std::min<long long>((long long)per_sm * num_sms, GA.ngroups);
-    if (max_ctas > 0) grid = std::min<long long>(grid, max_ctas);
-    err = cudaMemsetAsync(wm, 0, sizeof(int) * (size_t)GA.ngroups, s);
-    if (err != cudaSuccess) return err;
-    T* band_arg = band;
-    PassArgs p_arg = P;
-    GroupArgs g_arg = GA;
-    int* wm_arg = wm;
-    int* stat_arg = status;
-    void* args[] = {&band_arg, &p_arg, &g_arg, &wm_arg, &stat_arg};
-    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(32 * (GA.g + 3)), args, smem,
-                                       s);
+    return launch_group_pass<T, WMAX, SymChase, T>(band, P, GA, num_sms, max_ctas, wm, status, s);
 }
 
 #define BB_SYM_GROUP_INSTANTIATE(T, W)                                                                         \
