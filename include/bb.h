@@ -28,7 +28,9 @@
  *   bb_reduce.  ldab >= bw + 2*tw + 1.  Rows beyond ku + tw are not touched.
  *
  * Threading: a handle may be used by one host thread at a time, with at most
- * one bb_reduce in flight.  All calls are asynchronous on the given stream
+ * one reduction in flight (bb_reduce, bb_reduce_host, bb_sym_reduce or
+ * bb_back_transform: they share the handle's progress counters, status
+ * word and working band).  All calls are asynchronous on the given stream
  * unless stated otherwise.
  */
 #ifndef BB_H_
@@ -138,7 +140,12 @@ enum {
                                    (allocated by the handle on first use, n x ldab
                                    rounded up; copied in and back on the stream)   */
     BB_PARAM_TPB = 1,           /* threads per block, multiple of 32 in [32, 1024];
-                                   0 = automatic (default)                              */
+                                   0 = automatic (default).  With MAX_CTAS, the
+                                   "Threads per block" and "Max blocks" of the
+                                   hyperparameter study of "Accelerating
+                                   Bidiagonalization of Banded Matrices through
+                                   Memory-Aware Bulge-Chasing on GPUs", Section V-B
+                                   (its third, the inner tile width, is tw)        */
     BB_PARAM_MAX_CTAS = 2,      /* cap on the persistent grid; 0 = co-resident maximum  */
     BB_PARAM_WAIT_BUDGET_MS = 3,/* bound of one device-side wait, in ms (default 4000)  */
     BB_PARAM_PASS_LO = 4,       /* run only passes [PASS_LO, PASS_HI) (default 0 .. all); */
