@@ -92,12 +92,14 @@ def test_two_stages_chained_on_the_gpu(n, bw, tw, dt):
     assert err <= TOL[dt], f"singular values differ by {err:.3e} sigma_1"
 
 
-@pytest.mark.parametrize("n,bw,dt", [(1700, 16, "f64"), (3400, 16, "f32")])
+@pytest.mark.parametrize("n,bw,dt", [(1700, 16, "f64"), (3400, 16, "f32"), (3300, 16, "f64")])
 def test_two_stages_chained_with_tall_panels(n, bw, dt):
-    """Panels taller than the shared-memory panel kernel takes (16 columns
-    of more than 1600 doubles or 3200 floats) go to the global-memory panel
-    kernel: the chain's singular values against LAPACK's SVD of the input,
-    and the exact band form."""
+    """Panels taller than 16 columns of shared memory hold (1600 doubles,
+    3200 floats) run in narrower blocks (n = 1700 double, 3400 float); in
+    double, blocks narrower than 8 are not used, so panels taller than 3200
+    rows go to the global-memory panel kernel (n = 3300).  The chain's
+    singular values against LAPACK's SVD of the input, and the exact band
+    form."""
     rng = np.random.default_rng(n + bw)
     a = rng.standard_normal((n, n)).astype(np.float32 if dt == "f32" else np.float64)
     got, x = gpu_stage1(a, bw)
