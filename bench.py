@@ -406,7 +406,8 @@ def run_stage1(w: bi.Workload, steps: int, warmup: int):
     fl = stage1_flops(w.n, w.bw)
     return {"ms": ms, "n": w.n, "bw": w.bw, "dtype": w.dtype, "gflops": fl / (ms * 1e-3) / 1e9,
             "flops_model": "4 flops per entry of every rank-one application",
-            "kernels": "s1_panel_kernel, s1_gemm_kernel, s1_tri_kernel"}
+            "kernels": "s1_panel_smem_kernel (s1_panel_kernel for panels too tall for shared memory), "
+                       "s1_gemm_kernel, s1_reduce_tri_kernel"}
 
 
 def run_e2e(w, band_np, steps, warmup, scheduler, model_bytes):
