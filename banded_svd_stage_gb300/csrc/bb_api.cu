@@ -143,12 +143,16 @@ bb_status bb_pass_info(int64_t bw, int64_t tw, int64_t i, int64_t* b, int64_t* t
     return BB_OK;
 }
 
-bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
-                        int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds) {
+// The group-kernel plan queries of bb_group_plan (sym = false: the
+// bidiagonal chase; elem_bytes 2 = binary16 columns) and bb_sym_group_plan
+// (sym = true, elem_bytes 4 or 8).
+static bb_status group_plan_query(const char* who, bool sym, int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes,
+                                  int64_t pass, int64_t group_size, int64_t* g, int64_t* nslot, int64_t* ahead,
+                                  int64_t* lds) {
+    const bool elem_ok = (elem_bytes == 4 || elem_bytes == 8 || (!sym && elem_bytes == 2));
     if (n < 1 || n >= bb::kGroupMaxN || bw < 0 || bw >= n || tw < 1 || tw > std::max<int64_t>(1, bw - 1) ||
-        pass < 0 || pass >= count_passes(bw, tw) || !g || !nslot || !ahead || !lds ||
-        (elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
-        return fail(BB_ERR_INVALID_ARG, "bb_group_plan: argument out of range");
+        pass < 0 || pass >= count_passes(bw, tw) || !g || !nslot || !ahead || !lds || !elem_ok || group_size < 0)
+        return fail(BB_ERR_INVALID_ARG, std::string(who) + ": argument out of range");
     try {
         const PassPlan ps = pass_at(bw, tw, pass);
         bb::PassArgs P{};
@@ -156,59 +160,46 @@ bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, i
         P.b = ps.b;
         P.t = ps.t;
         P.bp = P.b - P.t;
-        P.ku = (int)(bw + tw);
         P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
-        P.lagh = bb::pass_lag_half(P.b, P.t);
         bb::GroupArgs ga{};
         bool ok;
-        if (elem_bytes == 2)  // binary16 storage, float arithmetic
-            ok = bb::half_choose_group(P, 3, (int)group_size, &ga);
-        else
-            ok = P.nsweeps > 0 &&
-                 bb::plan_group(P, bb::wmax_bucket(P.t + 1), (size_t)elem_bytes, (int)group_size, &ga);
+        if (sym) {  // lower band storage, one two-sided step per tick
+            P.ku = 0;
+            P.lag = bb::sym_pass_lag(P.b, P.t);
+            P.lagh = P.lag;
+            const int wmax = bb::sym_group_wmax(P.t + 1);
+            ok = P.nsweeps > 0 && wmax > 0 &&
+                 bb::plan_group(P, wmax, (size_t)elem_bytes, (int)group_size, &ga, bb::ChaseKind::kSym);
+        } else {
+            P.ku = (int)(bw + tw);
+            P.lagh = bb::pass_lag_half(P.b, P.t);
+            if (elem_bytes == 2)  // binary16 storage, float arithmetic
+                ok = bb::half_choose_group(P, 3, (int)group_size, &ga);
+            else
+                ok = P.nsweeps > 0 &&
+                     bb::plan_group(P, bb::wmax_bucket(P.t + 1), (size_t)elem_bytes, (int)group_size, &ga);
+        }
         *g = ok ? ga.g : 0;
         *nslot = ok ? ga.nslot : 0;
         *ahead = ok ? ga.ahead : 0;
         *lds = ok ? ga.lds : 0;
         return BB_OK;
     } catch (const std::bad_alloc&) {
-        return fail(BB_ERR_NOMEM, "bb_group_plan: host allocation failed");
+        return fail(BB_ERR_NOMEM, std::string(who) + ": host allocation failed");
     } catch (...) {
-        return fail(BB_ERR_INTERNAL, "bb_group_plan: unexpected host exception");
+        return fail(BB_ERR_INTERNAL, std::string(who) + ": unexpected host exception");
     }
+}
+
+bb_status bb_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass, int64_t group_size,
+                        int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds) {
+    return group_plan_query("bb_group_plan", false, n, bw, tw, elem_bytes, pass, group_size, g, nslot, ahead, lds);
 }
 
 bb_status bb_sym_group_plan(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass,
                             int64_t group_size, int64_t* g, int64_t* nslot, int64_t* ahead, int64_t* lds) {
-    if (n < 1 || n >= bb::kGroupMaxN || bw < 0 || bw >= n || tw < 1 || tw > std::max<int64_t>(1, bw - 1) ||
-        pass < 0 || pass >= count_passes(bw, tw) || !g || !nslot || !ahead || !lds ||
-        (elem_bytes != 4 && elem_bytes != 8) || group_size < 0)
-        return fail(BB_ERR_INVALID_ARG, "bb_sym_group_plan: argument out of range");
-    try {
-        const PassPlan ps = pass_at(bw, tw, pass);
-        bb::PassArgs P{};
-        P.n = n;
-        P.b = ps.b;
-        P.t = ps.t;
-        P.bp = P.b - P.t;
-        P.ku = 0;
-        P.nsweeps = (int)std::max<int64_t>(0, n - P.bp - 1);
-        P.lag = bb::sym_pass_lag(P.b, P.t);
-        P.lagh = P.lag;
-        const int wmax = bb::sym_group_wmax(P.t + 1);
-        bb::GroupArgs ga{};
-        const bool ok = P.nsweeps > 0 && wmax > 0 &&
-                        bb::plan_group(P, wmax, (size_t)elem_bytes, (int)group_size, &ga, bb::ChaseKind::kSym);
-        *g = ok ? ga.g : 0;
-        *nslot = ok ? ga.nslot : 0;
-        *ahead = ok ? ga.ahead : 0;
-        *lds = ok ? ga.lds : 0;
-        return BB_OK;
-    } catch (const std::bad_alloc&) {
-        return fail(BB_ERR_NOMEM, "bb_sym_group_plan: host allocation failed");
-    } catch (...) {
-        return fail(BB_ERR_INTERNAL, "bb_sym_group_plan: unexpected host exception");
-    }
+    return group_plan_query("bb_sym_group_plan", true, n, bw, tw, elem_bytes, pass, group_size, g, nslot, ahead,
+                            lds);
 }
 
 double bb_model_bytes(int64_t n, int64_t bw, int64_t tw, int64_t elem_bytes, int64_t pass) {

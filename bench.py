@@ -732,6 +732,32 @@ def profile_stage1(spec: str) -> int:
     return 0
 
 
+def profile_sym(spec: str) -> int:
+    """--profile-sym N:BW:TW:DTYPE:SCHEDULER -- one bb_sym_reduce on a seeded
+    symmetric band (uniform entries, DTYPE f32 or f64), for an ncu capture of
+    the symmetric chase's kernels; prints one line, no timing."""
+    import torch
+
+    import banded_svd_stage_gb300 as bb
+    n_s, bw_s, tw_s, dt, sched_s = spec.split(":")
+    n, bw, tw, sched = int(n_s), int(bw_s), int(tw_s), int(sched_s)
+    torch.cuda.set_device(0)
+    sb = torch.from_numpy(bi.make_sym_band(n, bw, tw, dt, "uniform", seed=n + bw)).cuda()
+    d = torch.empty(n, dtype=sb.dtype, device="cuda")
+    e = torch.empty(max(n - 1, 1), dtype=sb.dtype, device="cuda")
+    h = bb.bb_create(n, bw, bb.dtype_code(dt))
+    try:
+        bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, sched)
+        s = torch.cuda.current_stream()
+        bb.bb_sym_reduce(h, sb, sb.shape[1], tw, d, e, s)
+        st = bb.bb_status_sync(h, s)
+        ks = [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))]
+    finally:
+        bb.bb_destroy(h)
+    print(f"profile sym: n={n} bw={bw} tw={tw} dtype={dt} scheduler={sched} kernels={ks} status={st}")
+    return 0 if st == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -745,6 +771,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (e2e) leg")
+    ap.add_argument("--profile-sym", default=None, metavar="N:BW:TW:DTYPE:SCHEDULER",
+                    help="one symmetric reduction, for an ncu capture")
     ap.add_argument("--profile-stage1", default=None, metavar="N:BW:DTYPE",
                     help="one stage-1 call (dense -> band), for an ncu launch list")
     ap.add_argument("--profile-pass", default=None, metavar="WORKLOAD:N:PASS:SCHEDULER:DTYPE[:MAX_CTAS]",
@@ -754,6 +782,8 @@ def main():
         return profile_pass(args.profile_pass)
     if args.profile_stage1:
         return profile_stage1(args.profile_stage1)
+    if args.profile_sym:
+        return profile_sym(args.profile_sym)
     rank, world, local = dist_env()
     w = bi.by_name(args.workload)
 

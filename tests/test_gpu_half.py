@@ -210,3 +210,40 @@ def test_half_entry_points_that_do_not_take_it():
     xb = torch.zeros((n, bw + 2 * tw + 1), dtype=torch.float16, device=dev)
     with pytest.raises(bb.BBError):
         bb.bb_reduce_noalloc(xb, n, bw, bw + 2 * tw + 1, tw, bb.BB_F16, d, e)
+
+
+def test_half_group_kernel_on_unaligned_band_pointer():
+    """A binary16 band one element past a 16-byte boundary (column stride a
+    multiple of 16 bytes): the group kernel runs on the aligned working
+    copy, bitwise equal to the binary16 flag kernel; nothing outside the
+    band is written."""
+    n, bw, tw = 500, 24, 8
+    ld = (bw + 2 * tw + 1 + 7) // 8 * 8
+    band = half_band(n, bw, tw, seed=31, ldab=ld)
+    dev = torch.device("cuda:0")
+
+    def run(sched):
+        flat = torch.zeros(n * ld + 2, dtype=torch.float16, device=dev)
+        x = flat[1:-1].view(n, ld)
+        x.copy_(torch.from_numpy(band))
+        assert x.data_ptr() % 16 != 0
+        d = torch.empty(n, dtype=torch.float16, device=dev)
+        e = torch.empty(n - 1, dtype=torch.float16, device=dev)
+        h = bb.bb_create(n, bw, bb.BB_F16)
+        try:
+            bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, sched)
+            s = torch.cuda.current_stream(dev)
+            bb.bb_reduce(h, x, ld, tw, d, e, s)
+            assert bb.bb_status_sync(h, s) == bb.BB_OK
+            ks = [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))]
+        finally:
+            bb.bb_destroy(h)
+        assert flat[0].item() == 0.0 and flat[-1].item() == 0.0
+        return d.cpu().numpy(), e.cpu().numpy(), x.cpu().numpy(), ks
+
+    d3, e3, b3, k3 = run(3)
+    d2, e2, b2, k2 = run(2)
+    assert 3 in k3 and all(k == 5 for k in k2)
+    assert np.array_equal(d2.view(np.uint16), d3.view(np.uint16))
+    assert np.array_equal(e2.view(np.uint16), e3.view(np.uint16))
+    assert np.array_equal(b2.view(np.uint16), b3.view(np.uint16))

@@ -227,3 +227,41 @@ def test_argument_errors():
     finally:
         bb.bb_destroy(h)
     assert bb.bb_sym_required_ldab(bw, tw) == bw + tw + 1
+
+
+@pytest.mark.parametrize("dt", ["f32", "f64"])
+def test_group_kernel_on_unaligned_band_pointer(dt):
+    """A band that starts one element past a 16-byte boundary, with a
+    16-byte aligned column stride: the group kernel runs on the handle's
+    aligned working copy, and the result (band included) equals the flag
+    kernel's on the same storage; nothing outside the band is written."""
+    n, bw, tw = 600, 24, 8
+    q = 4 if dt == "f32" else 2
+    ld = (bw + tw + 1 + q - 1) // q * q
+    sb = bi.make_sym_band(n, bw, tw, dt, seed=21, ldab=ld)
+    dev = torch.device("cuda:0")
+    tdt = torch.float32 if dt == "f32" else torch.float64
+
+    def run(sched):
+        flat = torch.zeros(n * ld + 2, dtype=tdt, device=dev)
+        x = flat[1:-1].view(n, ld)
+        x.copy_(torch.from_numpy(sb))
+        assert x.data_ptr() % 16 != 0
+        d = torch.empty(n, dtype=tdt, device=dev)
+        e = torch.empty(n - 1, dtype=tdt, device=dev)
+        h = bb.bb_create(n, bw, bb.dtype_code(dt))
+        try:
+            bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, sched)
+            s = torch.cuda.current_stream(dev)
+            bb.bb_sym_reduce(h, x, ld, tw, d, e, s)
+            assert bb.bb_status_sync(h, s) == bb.BB_OK
+            ks = [bb.bb_last_pass_kernel(h, i) for i in range(bb.bb_last_num_passes(h))]
+        finally:
+            bb.bb_destroy(h)
+        assert flat[0].item() == 0.0 and flat[-1].item() == 0.0
+        return d.cpu().numpy(), e.cpu().numpy(), x.cpu().numpy(), ks
+
+    d3, e3, b3, k3 = run(3)
+    d2, e2, b2, k2 = run(2)
+    assert 3 in k3 and all(k == 2 for k in k2)
+    assert np.array_equal(d2, d3) and np.array_equal(e2, e3) and np.array_equal(b2, b3)
