@@ -677,6 +677,12 @@ def traffic_for(kernel: str, workload: str):
         return None
 
 
+# Bound of one device-side wait in the profiling modes: a profiler's
+# instrumented replay can run a pass far slower than normal, and a CTA then
+# waits on its predecessor for longer than the library's default 4 s.
+PROFILE_WAIT_MS = 60000
+
+
 def profile_pass(spec: str) -> int:
     """--profile-pass WORKLOAD:N:PASS:SCHEDULER:DTYPE[:MAX_CTAS] -- one run of
     one pass of the workload's recipe at order N (DTYPE f32, f64 or f16), for
@@ -699,6 +705,7 @@ def profile_pass(spec: str) -> int:
     h = bb.bb_create(n, w.bw, bb.dtype_code(dt))
     try:
         bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, sched)
+        bb.bb_set_param(h, bb.BB_PARAM_WAIT_BUDGET_MS, PROFILE_WAIT_MS)
         bb.bb_set_param(h, bb.BB_PARAM_MAX_CTAS, ctas)
         bb.bb_set_param(h, bb.BB_PARAM_PASS_LO, p)
         bb.bb_set_param(h, bb.BB_PARAM_PASS_HI, p + 1)
@@ -748,6 +755,7 @@ def profile_sym(spec: str) -> int:
     h = bb.bb_create(n, bw, bb.dtype_code(dt))
     try:
         bb.bb_set_param(h, bb.BB_PARAM_SCHEDULER, sched)
+        bb.bb_set_param(h, bb.BB_PARAM_WAIT_BUDGET_MS, PROFILE_WAIT_MS)
         s = torch.cuda.current_stream()
         bb.bb_sym_reduce(h, sb, sb.shape[1], tw, d, e, s)
         st = bb.bb_status_sync(h, s)
