@@ -55,7 +55,14 @@ bool sym_choose_group(const PassArgs& P, int scheduler, int group_size, size_t e
     if (wmax == 0) return false;
     GroupArgs ga;
     if (!plan_group(P, wmax, elem, group_size, &ga, ChaseKind::kSym)) return false;
-    if (scheduler == 0 && ga.g < kAutoGroupMin) return false;
+    // automatic: the group kernel from 3 sweeps per group in float, from
+    // kAutoGroupMin in double.  Measured against this file's flag kernel:
+    // float, n = 8192, bw 64, pass 0 on the group kernel with g = 4: 414 ->
+    // 351 ms for the reduction; float, n = 32768, bw 256, passes with g = 1
+    // and 3: 12.3 -> 10.9 s; double, n = 8192, bw 64, passes with g = 1 and
+    // 3: 844 -> 1050 ms (the FP64 work of g sweeps shares one SM)
+    const int gmin = (elem == 4) ? 3 : kAutoGroupMin;
+    if (scheduler == 0 && ga.g < gmin) return false;
     if (out) *out = ga;
     return true;
 }

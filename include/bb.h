@@ -192,7 +192,8 @@ int64_t bb_get_param(const bb_handle* h, int param);
  *     columns in shared memory (bb_sym_group_plan); it takes a pass with a
  *     reflector of at most 33 elements on a band whose base and ldab *
  *     element size are multiples of 16 bytes: under scheduler 0 (default)
- *     where at least 5 sweeps fit, under 3 wherever one fits; every other
+ *     where at least 3 sweeps fit (float) or 5 (double), under 3 wherever
+ *     one fits; every other
  *     pass, and every pass under schedulers 1, 2 and 4, runs on the flag
  *     kernel.
  * Both give bitwise equal results; bb_last_pass_kernel / bb_last_pass_group
