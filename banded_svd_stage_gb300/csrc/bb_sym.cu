@@ -200,6 +200,162 @@ sym_pass_kernel(T* __restrict__ band, PassArgs P, int* __restrict__ progress, in
     }
 }
 
+// One step of sweep r by the whole CTA on a shared-memory copy of its
+// window, with the operations and their order of sym_step (so the two give
+// bitwise equal results):
+//   Lt: columns p .. c-1, rows c .. ce: Lt[(j - p) ws + m] = A(c + m, j)
+//       (ws = WMAX | 1, an odd stride);
+//   Rt: columns c .. ce, rows c .. cend: Rt[q rs + i] = A(c + i, c + q),
+//       i >= q (rs = b + t + 1).
+// The window is read once after the wait and written back once; in between
+// the three parts, alpha and the rank-2 update work on shared memory.
+template <typename T, int WMAX>
+__device__ __forceinline__ void sym_step_smem(T* __restrict__ band, const PassArgs& P, long long r, int k, T* Lt,
+                                              T* Rt, T* s_v, T* s_x, T* s_tau) {
+    constexpr int NPL = (WMAX + 31) / 32;
+    constexpr int ws = WMAX | 1;
+    const int rs = P.b + P.t + 1;
+    const long long n = P.n, ld = P.ldab;
+    const long long c = r + P.bp + (long long)k * P.b;
+    const long long p = (k == 0) ? r : c - P.b;
+    const long long ce = min(c + (long long)P.t, n - 1);
+    const long long cend = min(ce + (long long)P.b, n - 1);
+    const int w = (int)(ce - c + 1);
+    const int nl = (int)(c - p);        // columns p .. c-1
+    const int nr = (int)(cend - c + 1);  // rows c .. cend
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+    // read the window (through L2: other CTAs wrote it), a warp per column
+    // of the band, lanes along the column
+    for (int jl = warp; jl < nl; jl += nwarps) {
+        const T* col = band + (c - (p + jl)) + (p + jl) * ld;  // A(c + m, p + jl) = col[m]
+        for (int m = lane; m < w; m += 32) Lt[jl * ws + m] = __ldcg(col + m);
+    }
+    for (int q = warp; q < w; q += nwarps) {
+        const T* col = band + (c + q) * ld - q;  // A(c + i, c + q) = col[i], i >= q
+        for (int i = q + lane; i < nr; i += 32) Rt[q * rs + i] = __ldcg(col + i);
+    }
+    __syncthreads();
+    if (tid < 32) {
+        T x[NPL];
+#pragma unroll
+        for (int q = 0; q < NPL; ++q) {
+            const int m = lane + 32 * q;
+            x[q] = (m < w) ? Lt[m] : T(0);
+        }
+        const T beta = warp_larfg<T, NPL>(x, w, lane, s_v, s_tau);
+#pragma unroll
+        for (int q = 0; q < NPL; ++q) {
+            const int m = lane + 32 * q;
+            if (m < w) Lt[m] = (m == 0) ? beta : T(0);
+        }
+    }
+    __syncthreads();
+    const T tau = *s_tau;  // the same value in every thread
+    if (tau != T(0)) {
+        // the three parts on disjoint entries: a column left of the block, a
+        // row below it, a row u of x = tau S v; each task's entries are read
+        // for the dot product and again for the update (shared memory)
+        const int nleft = nl - 1;
+        const int nbelow = nr - w;
+        for (int idx = tid; idx < nleft + nbelow + w; idx += nt) {
+            if (idx < nleft + nbelow) {
+                T* a0;
+                int st;
+                if (idx < nleft) {
+                    a0 = Lt + (idx + 1) * ws;  // column p + 1 + idx
+                    st = 1;
+                } else {
+                    a0 = Rt + w + (idx - nleft);  // row c + w + (idx - nleft)
+                    st = rs;
+                }
+                T y = 0;
+#pragma unroll
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < w) y = fma(s_v[m], a0[m * st], y);
+                const T sc = tau * y;
+#pragma unroll
+                for (int m = 0; m < WMAX; ++m)
+                    if (m < w) a0[m * st] = fma(-sc, s_v[m], a0[m * st]);
+            } else {
+                const int u = idx - nleft - nbelow;
+                T y = 0;
+#pragma unroll
+                for (int q = 0; q < WMAX; ++q)
+                    if (q < w) {
+                        const T sq = (u >= q) ? Rt[q * rs + u] : Rt[u * rs + q];
+                        y = fma(sq, s_v[q], y);
+                    }
+                s_x[u] = tau * y;
+            }
+        }
+        __syncthreads();
+        if (tid < 32) {
+            T dot = 0;
+            for (int u = tid; u < w; u += 32) dot = fma(s_x[u], s_v[u], dot);
+            dot = warp_sum(dot);
+            const T alpha = -(T(0.5) * tau) * dot;
+            for (int u = tid; u < w; u += 32) s_x[u] = fma(alpha, s_v[u], s_x[u]);
+        }
+        __syncthreads();
+        const int npairs = w * (w + 1) / 2;
+        for (int e = tid; e < npairs; e += nt) {
+            int u, q;
+            sym_pair(e, u, q);
+            T& a = Rt[q * rs + u];
+            a = sym_rank2(a, s_v[u], s_x[q], s_x[u], s_v[q]);
+        }
+        __syncthreads();
+    }
+    // write the window back, as it was read
+    for (int jl = warp; jl < nl; jl += nwarps) {
+        T* col = band + (c - (p + jl)) + (p + jl) * ld;
+        for (int m = lane; m < w; m += 32) col[m] = Lt[jl * ws + m];
+    }
+    for (int q = warp; q < w; q += nwarps) {
+        T* col = band + (c + q) * ld - q;
+        for (int i = q + lane; i < nr; i += 32) col[i] = Rt[q * rs + i];
+    }
+}
+
+// Shared memory of sym_step_smem: the two tiles of pass (b, t).
+template <typename T, int WMAX>
+__host__ __device__ inline size_t sym_tile_bytes(int b, int t) {
+    return sizeof(T) * ((size_t)b * (WMAX | 1) + (size_t)(t + 1) * (size_t)(b + t + 1));
+}
+
+// The flag kernel with each step's window in shared memory.
+template <typename T, int WMAX, int NT>
+__global__ void __launch_bounds__(NT)
+sym_pass_smem_kernel(T* __restrict__ band, PassArgs P, int* __restrict__ progress, int* __restrict__ status) {
+    extern __shared__ __align__(16) unsigned char sym_smem[];
+    T* Lt = reinterpret_cast<T*>(sym_smem);
+    T* Rt = Lt + (size_t)P.b * (WMAX | 1);
+    __shared__ T s_v[WMAX];
+    __shared__ T s_x[WMAX];
+    __shared__ T s_tau;
+    __shared__ int s_flag;
+    if (threadIdx.x == 0) s_flag = ld_relaxed_gpu(status);
+    __syncthreads();
+    if (s_flag != kStatusOk) return;
+    for (int r = blockIdx.x; r < P.nsweeps; r += gridDim.x) {
+        const int K = sweep_steps(P, r);
+        const int Kp = (r > 0) ? sweep_steps(P, r - 1) : 0;
+        const bool publish = (r != P.stall_sweep);
+        for (int k = 0; k < K; ++k) {
+            if (r > 0) {
+                const int need = (k == K - 1) ? Kp : min(k + P.lag, Kp);
+                if (!block_wait(progress + r - 1, need, status, P, &s_flag)) return;
+            } else {
+                __syncthreads();  // the tiles and s_v, s_x of the previous step are no longer read
+            }
+            sym_step_smem<T, WMAX>(band, P, r, k, Lt, Rt, s_v, s_x, &s_tau);
+            if (publish) block_publish(progress + r, k + 1);
+            else __syncthreads();
+        }
+    }
+}
+
 // Zero the fill rows bw+1 .. bw+tw of every column.
 template <typename T>
 __global__ void sym_zero_fill_kernel(T* __restrict__ band, long long n, long long ldab, int bw, int tw) {
@@ -223,10 +379,45 @@ __global__ void sym_extract_kernel(const T* __restrict__ band, long long n, long
     }
 }
 
+// Most shared memory the window copy of sym_pass_smem_kernel may take.
+constexpr size_t kSymTileMax = 200 * 1024;
+
+// The flag kernel with the window in shared memory, NT threads per CTA.
+template <typename T, int WMAX, int NT>
+static cudaError_t run_sym_pass_smem(T* band, const PassArgs& P, int num_sms, int max_ctas, int* progress,
+                                     int* status, cudaStream_t s) {
+    auto kern = sym_pass_smem_kernel<T, WMAX, NT>;
+    const size_t smem = sym_tile_bytes<T, WMAX>(P.b, P.t);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    long long grid = std::min<long long>((long long)per_sm * num_sms, P.nsweeps);
+    if (max_ctas > 0) grid = std::min<long long>(grid, max_ctas);
+    err = cudaMemsetAsync(progress, 0, sizeof(int) * (size_t)P.nsweeps, s);
+    if (err != cudaSuccess) return err;
+    T* band_arg = band;
+    PassArgs p_arg = P;
+    int* prog_arg = progress;
+    int* stat_arg = status;
+    void* args[] = {&band_arg, &p_arg, &prog_arg, &stat_arg};
+    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(NT), args, smem, s);
+}
+
 template <typename T, int WMAX>
 static cudaError_t run_sym_pass(T* band, const PassArgs& P, int num_sms, int max_ctas, int* progress, int* status,
                                 cudaStream_t s) {
     if (P.nsweeps <= 0) return cudaSuccess;
+    // 512 threads for the 32-wide kernel on wide passes; the wider kernels
+    // keep 256 (their registers would spill at 512)
+    if (sym_tile_bytes<T, WMAX>(P.b, P.t) <= kSymTileMax) {
+        if constexpr (WMAX == 32) {
+            if (P.b >= 96) return run_sym_pass_smem<T, WMAX, 512>(band, P, num_sms, max_ctas, progress, status, s);
+        }
+        return run_sym_pass_smem<T, WMAX, 256>(band, P, num_sms, max_ctas, progress, status, s);
+    }
     auto kern = sym_pass_kernel<T, WMAX>;
     int per_sm = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSymThreads, 0);
