@@ -283,3 +283,29 @@ def test_group_plan_matches_workloads():
     assert [bb.bb_group_plan(32768, 256, 32, 4, p)[0] for p in range(8)] == [0, 0, 0, 0, 0, 2, 5, 5]
     with pytest.raises(bb.BBError):
         bb.bb_group_plan(100, 16, 8, 4, 9)
+
+
+def sym_tiles(n, b, t, r, k):
+    """Entries the shared-memory flag kernel of the symmetric chase copies
+    for step k of sweep r: the left tile (columns p .. c-1 on rows c .. ce)
+    and the right tile (columns c .. ce on rows c .. cend, lower triangle)."""
+    c = r + (b - t) + k * b
+    p = r if k == 0 else c - b
+    ce = min(c + t, n - 1)
+    cend = min(ce + b, n - 1)
+    left = {(c + m, j) for j in range(p, c) for m in range(ce - c + 1)}
+    right = {(c + i, c + q) for q in range(ce - c + 1) for i in range(q, cend - c + 1)}
+    assert not (left & right)
+    return left | right
+
+
+@pytest.mark.parametrize("b,t", [(2, 1), (8, 7), (16, 8), (24, 7), (40, 12), (64, 16)])
+def test_sym_window_tiles_cover_exactly_the_step(b, t):
+    """What the symmetric flag kernel reads into shared memory and writes
+    back is exactly the step's window: every entry the step reads or writes,
+    and no other (so the write-back of unchanged entries touches nothing
+    another sweep may be changing)."""
+    for n in (3 * b + 7, 6 * b + 5):
+        for r in range(n - (b - t) - 1):
+            for k in range(steps(n, b, t, r)):
+                assert sym_tiles(n, b, t, r, k) == sym_entries(n, b, t, r, k), (n, r, k)
